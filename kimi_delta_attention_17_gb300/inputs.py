@@ -1,0 +1,158 @@
+"""Seeded synthetic inputs for the KDA prefill and decode paths.
+
+This module only draws random numbers and shapes them; it holds none of the
+method's arithmetic, so both the CUDA path's tests/benchmark and the CPU oracle
+can consume the very same buffers.
+
+Recipe (one torch CPU ``Generator`` per workload, seeded with the workload's
+seed; fixed draw order: sequence lengths, q, k, v, beta, g, initial state):
+
+* q, k ~ N(0, 1), then L2-normalised over the key channels of each
+  (token, head), then rounded to the storage dtype (bf16 or fp32);
+* v ~ N(0, 1), rounded to the storage dtype;
+* beta = sigmoid(N(0, 1)), fp32, one per (token, head);
+* g = -softplus(N(0, 1) - 2), fp32, one per (token, head, key channel): the
+  per-token log-decay log a_t, so a_t = exp(g) lies in (0, 1);
+* the "mixture" gate: in each head, key channels [0, d_k/2) draw
+  -softplus(N(0, 1) - 5) (slow, long half-lives) and [d_k/2, d_k) draw
+  -softplus(N(0, 1)) (fast);
+* initial states are zero or N(0, 0.1^2), fp32, [N, H, d_k, d_v];
+* varlen lengths are uniform integers in [lo, hi], packed back to back and
+  described by int32 ``cu_seqlens``;
+* the query scale is d_k^{-1/2}, passed separately (q itself is not scaled).
+"""
+from dataclasses import dataclass, field, replace
+from typing import Optional, Tuple
+
+import torch
+
+
+@dataclass(frozen=True)
+class PrefillSpec:
+    name: str
+    H: int
+    d: int
+    B: int = 1
+    T: int = 0                      # per-sequence length when lengths is None
+    num_seqs: int = 0               # varlen: number of packed sequences
+    lengths: Optional[Tuple[int, int]] = None   # varlen: uniform length range
+    fixed_lengths: Optional[Tuple[int, ...]] = None  # varlen: explicit lengths
+    dtype: str = "bf16"             # storage dtype of q, k, v and the output
+    init: str = "zero"              # "zero" or "normal0.1"
+    gate: str = "base"              # "base" or "mixture"
+    seed: int = 0
+
+
+@dataclass(frozen=True)
+class DecodeSpec:
+    name: str
+    N: int
+    H: int
+    d: int
+    steps: int
+    dtype: str = "bf16"
+    seed: int = 4
+
+
+# The five workloads the method is exercised on. The first is small enough
+# for the oracle to finish in seconds; the long prefill and the decode batch
+# are the ones timed.
+SMALL_FP32 = PrefillSpec("prefill fp32 B=1 H=2 T=256 d=64", H=2, d=64, B=1, T=256,
+                         dtype="f32", seed=0)
+PREFILL_B2 = PrefillSpec("prefill bf16 B=2 H=16 T=4096 d=128", H=16, d=128, B=2, T=4096, seed=1)
+VARLEN_8 = PrefillSpec("varlen prefill bf16 8 seqs in [512,16384] H=32 d=128", H=32, d=128,
+                       num_seqs=8, lengths=(512, 16384), init="normal0.1", gate="mixture", seed=2)
+LONG_128K = PrefillSpec("prefill bf16 B=1 H=32 T=131072 d=128", H=32, d=128, B=1, T=131072,
+                        seed=3)
+DECODE_256 = DecodeSpec("decode bf16 256 seqs x H=32 d=128, 128 steps", N=256, H=32, d=128,
+                        steps=128, seed=4)
+
+
+def _dtype(name):
+    return {"bf16": torch.bfloat16, "f32": torch.float32}[name]
+
+
+def _unit(x):
+    return x / x.norm(dim=-1, keepdim=True).clamp_min(1e-12)
+
+
+def _gate(gen, shape, kind):
+    d = shape[-1]
+    if kind == "base":
+        return -torch.nn.functional.softplus(torch.randn(shape, generator=gen) - 2.0)
+    if kind == "mixture":
+        z = torch.randn(shape, generator=gen)
+        shift = torch.zeros(d)
+        shift[: d // 2] = 5.0
+        return -torch.nn.functional.softplus(z - shift)
+    raise ValueError(kind)
+
+
+def seq_lengths(spec: PrefillSpec):
+    """Per-sequence lengths (list of ints) without drawing the tensors."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    if spec.fixed_lengths is not None:
+        return list(spec.fixed_lengths)
+    if spec.lengths is not None:
+        lo, hi = spec.lengths
+        return [int(x) for x in torch.randint(lo, hi + 1, (spec.num_seqs,), generator=gen)]
+    return [spec.T] * spec.B
+
+
+def make_prefill(spec: PrefillSpec):
+    """Returns a dict of CPU tensors: q, k, v [B, T, H, d] (storage dtype),
+    g [B, T, H, d] fp32, beta [B, T, H] fp32, init_state [N, H, d, d] fp32 or
+    None, cu_seqlens int32 [N+1] or None, scale (float), lengths (list)."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    varlen = spec.lengths is not None or spec.fixed_lengths is not None
+    if spec.fixed_lengths is not None:
+        lengths = list(spec.fixed_lengths)
+    elif spec.lengths is not None:
+        lo, hi = spec.lengths
+        lengths = [int(x) for x in torch.randint(lo, hi + 1, (spec.num_seqs,), generator=gen)]
+    else:
+        lengths = [spec.T] * spec.B
+    if varlen:
+        B, T = 1, sum(lengths)
+        cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    else:
+        B, T = spec.B, spec.T
+        cu = None
+    H, d = spec.H, spec.d
+    st = _dtype(spec.dtype)
+    q = _unit(torch.randn((B, T, H, d), generator=gen)).to(st)
+    k = _unit(torch.randn((B, T, H, d), generator=gen)).to(st)
+    v = torch.randn((B, T, H, d), generator=gen).to(st)
+    beta = torch.sigmoid(torch.randn((B, T, H), generator=gen))
+    g = _gate(gen, (B, T, H, d), spec.gate)
+    N = len(lengths)
+    if spec.init == "zero":
+        init = None
+    elif spec.init == "normal0.1":
+        init = 0.1 * torch.randn((N, H, d, d), generator=gen)
+    else:
+        raise ValueError(spec.init)
+    return dict(q=q, k=k, v=v, g=g, beta=beta, init_state=init, cu_seqlens=cu,
+                scale=d ** -0.5, lengths=lengths)
+
+
+def make_decode(spec: DecodeSpec):
+    """Returns a dict of CPU tensors for ``steps`` successive decode steps:
+    q, k, v [steps, N, H, d] (storage dtype), g [steps, N, H, d] fp32,
+    beta [steps, N, H] fp32, state0 [N, H, d, d] fp32 ~ N(0, 0.1^2), scale."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    s, N, H, d = spec.steps, spec.N, spec.H, spec.d
+    st = _dtype(spec.dtype)
+    q = _unit(torch.randn((s, N, H, d), generator=gen)).to(st)
+    k = _unit(torch.randn((s, N, H, d), generator=gen)).to(st)
+    v = torch.randn((s, N, H, d), generator=gen).to(st)
+    beta = torch.sigmoid(torch.randn((s, N, H), generator=gen))
+    g = _gate(gen, (s, N, H, d), "base")
+    state0 = 0.1 * torch.randn((N, H, d, d), generator=gen)
+    return dict(q=q, k=k, v=v, g=g, beta=beta, state0=state0, scale=d ** -0.5)
+
+
+def with_(spec, **kw):
+    """A copy of a spec with some fields replaced (smaller parity variants)."""
+    return replace(spec, **kw)
