@@ -1,0 +1,477 @@
+"""Benchmark of the KDA hot path on GB300: chunkwise prefill tokens/s (headline)
+and recurrent decode steps/s, with roofline fractions, an end-to-end number
+through host buffers, SM clocks sampled during the timed region, and the CPU
+oracle timed on the host cores beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on stdout (rank 0). Under torchrun each rank runs the same
+per-GPU workload on its own GPU (independent sequences and heads need no
+exchange: weak scaling, no collective on the data path); the timed region is
+bracketed by a barrier and device synchronisation and the time is the maximum
+over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kimi_delta_attention_17_gb300 import inputs as kin  # noqa: E402
+
+PREFILL_WORKLOADS = {"long": kin.LONG_128K, "b2": kin.PREFILL_B2, "varlen": kin.VARLEN_8}
+L2_BYTES = 129 * 10 ** 6
+KIB = 1024
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def prefill_bytes(spec, tokens, num_seqs, has_init):
+    """Bytes the prefill must move: q, k, v, out in the storage dtype, g fp32,
+    beta fp32 per (token, head); the final state (and the initial one when
+    given) per (sequence, head)."""
+    e = 2 if spec.dtype == "bf16" else 4
+    d = spec.d
+    per_token_head = 4 * d * e + d * 4 + 4   # q, k, v, out + g + beta
+    state = d * d * 4
+    return tokens * spec.H * per_token_head + num_seqs * spec.H * state * (2 if has_init else 1)
+
+
+def prefill_flops(spec, tokens):
+    """Dense-contraction flops per (token, head) of the chunk algebra with
+    C = 64 full tiles: A, H, W, U, H*Z at 2*C*d each and the three state
+    products (W S, Qbar S, Kbar^T Z) at 2*d*d each."""
+    C, d = 64, spec.d
+    return tokens * spec.H * (5 * 2 * C * d + 3 * 2 * d * d)
+
+
+def decode_bytes(spec):
+    e = 2 if spec.dtype == "bf16" else 4
+    d = spec.d
+    per = 2 * d * d * 4 + 4 * d * e + d * 4 + 4   # state in+out, q k v out, g, beta
+    return spec.N * spec.H * per
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(backend):
+    world, rank, _ = dist_info()
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+    return world, rank
+
+
+def barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, device=None):
+    """Maximum of a float over all ranks (the slowest rank sets the time)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def units_for_world(units_per_rank, world):
+    """Whole-job units for weak scaling: every rank processes its own batch."""
+    return units_per_rank * world
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", "clocks_%d.csv" % os.getpid())
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ roofline peaks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ the oracle on the host cores
+
+def oracle_prefill_sample(inp, spec, target_s=10.0, max_tokens=None):
+    """Times the oracle (as it stands) on the first tokens of every head of
+    the workload; grows the sample until one run takes about target_s.
+    Returns (tokens/s, cores, sample description)."""
+    import numpy as np
+    import oracle
+
+    T = inp["q"].shape[1]
+    max_tokens = min(T, max_tokens or T)
+
+    def run(n):
+        arr = {k: inp[k][:, :n].to(torch.float64).numpy() for k in ("q", "k", "v", "g", "beta")}
+        # The sample treats each row of q as one sequence (for packed inputs:
+        # the first n tokens as one sequence starting from the first state).
+        init = None if inp["init_state"] is None else \
+            inp["init_state"][: arr["q"].shape[0]].double().numpy()
+        t0 = time.perf_counter()
+        oracle.scan(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], inp["scale"], init)
+        return time.perf_counter() - t0
+
+    n = min(512, max_tokens)
+    dt = run(n)
+    if dt < target_s and n < max_tokens:
+        n = int(min(max_tokens, max(n, n * target_s / max(dt, 1e-3))))
+        dt = run(n)
+    B = inp["q"].shape[0]
+    sample = "first %d tokens of each of the %d sequences x %d heads (fp64 scan)" % (n, B, spec.H)
+    return n * B / dt, oracle.hw_threads(), sample, n
+
+
+def oracle_decode_sample(inp, spec, n_seq=16, n_steps=4):
+    import oracle
+    t = 0.0
+    state = inp["state0"][:n_seq].double().numpy()
+    for s in range(n_steps):
+        args = [inp[k][s][:n_seq].to(torch.float64).numpy() for k in ("q", "k", "v", "g", "beta")]
+        t0 = time.perf_counter()
+        _, state = oracle.decode_step(*args, inp["scale"], state)
+        t += time.perf_counter() - t0
+    per_step_full = t / n_steps * (spec.N / n_seq)
+    sample = ("%d of %d sequences x %d heads, %d steps; steps/s scaled to all %d sequences"
+              % (n_seq, spec.N, spec.H, n_steps, spec.N))
+    return 1.0 / per_step_full, oracle.hw_threads(), sample
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def to_dev(inp, dev, keys):
+    return {k: (None if inp[k] is None else inp[k].to(dev)) for k in keys}
+
+
+def bench_ours(args):
+    from kimi_delta_attention_17_gb300 import build, chunk_fwd, decode_step, workspace_size
+
+    world, rank = init_dist("nccl")
+    _, _, local = dist_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    peaks = measured_peaks()
+
+    # ---------------- prefill inputs
+    spec = PREFILL_WORKLOADS[args.workload]
+    if args.T:
+        spec = kin.with_(spec, T=args.T)
+    inp = kin.make_prefill(spec)
+    keys = ("q", "k", "v", "g", "beta", "init_state", "cu_seqlens")
+    d_in = to_dev(inp, dev, keys)
+    B, T, H, d = inp["q"].shape
+    N = len(inp["lengths"])
+    tokens = B * T
+    dt_storage = inp["q"].dtype
+    out = torch.empty((B, T, H, d), dtype=dt_storage, device=dev)
+    fin = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, workspace_size(B, T, H, d, d, N, dt_storage)), dtype=torch.uint8,
+                     device=dev)
+
+    def prefill(phase_events=None):
+        chunk_fwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"], inp["scale"],
+                  d_in["init_state"], d_in["cu_seqlens"], out=out, final_state=fin, workspace=ws,
+                  phase_events=phase_events)
+
+    # ---------------- decode inputs
+    dspec = kin.DECODE_256
+    dinp = kin.make_decode(dspec)
+    dd = {k: dinp[k].to(dev) for k in ("q", "k", "v", "g", "beta")}
+    state = dinp["state0"].to(dev)
+    dout = torch.empty((dspec.N, dspec.H, dspec.d), dtype=dd["q"].dtype, device=dev)
+
+    def decode_iteration():
+        for t in range(dspec.steps):
+            decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t],
+                        dinp["scale"], state, out=dout)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        prefill()
+        decode_iteration()
+    torch.cuda.synchronize()
+
+    # ---------------- timed prefill (device-resident inputs)
+    K = args.steps
+    phase = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+    with ClockSampler(gpu_index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(K):
+            prefill(phase_events=phase[s])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        prefill_ms = t_start.elapsed_time(t_end)
+
+        # ---------------- timed decode
+        d_start = torch.cuda.Event(enable_timing=True)
+        d_end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        d_start.record(stream)
+        for _ in range(K):
+            decode_iteration()
+        d_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        decode_ms = d_start.elapsed_time(d_end)
+    clocks = clk.summary()
+
+    prefill_ms = max_over_ranks(prefill_ms, dev)
+    decode_ms = max_over_ranks(decode_ms, dev)
+    names = ["chunk_table", "intra_chunk", "state_pass"]
+    phase_ms = {n: statistics.mean(phase[s][i].elapsed_time(phase[s][i + 1]) for s in range(K))
+                for i, n in enumerate(names)}
+    ms_step = prefill_ms / K
+    tok_per_s = units_for_world(tokens, world) * K / (prefill_ms / 1e3)
+    pbytes = prefill_bytes(spec, tokens, N, inp["init_state"] is not None)
+    dominant = max(phase_ms, key=phase_ms.get)
+
+    # ---------------- end to end through host buffers (pinned), prefill
+    h_in = {k: (None if inp[k] is None else inp[k].pin_memory()) for k in keys}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values() if t is not None)
+    d2h = h_out.numel() * h_out.element_size() + h_fin.numel() * h_fin.element_size()
+    e2e_steps = max(1, min(K, 3))
+    barrier()
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        for k in keys:
+            if h_in[k] is not None:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+        prefill()
+        h_out.copy_(out, non_blocking=True)
+        h_fin.copy_(fin, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
+    e2e_tok_s = units_for_world(tokens, world) * e2e_steps / (e2e_ms / 1e3)
+
+    # ---------------- end to end, decode
+    hd = {k: dinp[k].pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    h_dout = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    d_h2d = sum(hd[k][0].numel() * hd[k][0].element_size() for k in hd)
+    d_d2h = h_dout.numel() * h_dout.element_size()
+    barrier()
+    torch.cuda.synchronize()
+    de_start = torch.cuda.Event(enable_timing=True)
+    de_end = torch.cuda.Event(enable_timing=True)
+    de_start.record(stream)
+    for t in range(dspec.steps):
+        for k in hd:
+            dd[k][t].copy_(hd[k][t], non_blocking=True)
+        decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t],
+                    dinp["scale"], state, out=dout)
+        h_dout.copy_(dout, non_blocking=True)
+    de_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    de_ms = max_over_ranks(de_start.elapsed_time(de_end), dev)
+
+    steps_total = dspec.steps * K
+    dec_steps_s = world * steps_total / (decode_ms / 1e3)
+    dbytes = decode_bytes(dspec)
+    dec_ms_launch = decode_ms / steps_total
+    dec_gbs = dbytes / (dec_ms_launch / 1e3) / 1e9
+
+    result = None
+    if rank == 0:
+        cpu_val, cores, sample, _ = oracle_prefill_sample(inp, spec, target_s=args.cpu_seconds)
+        dcpu_val, dcores, dsample = oracle_decode_sample(dinp, dspec)
+        achieved_gbs = pbytes / (ms_step / 1e3) / 1e9
+        flops = prefill_flops(spec, tokens)
+        result = {
+            "metric": "KDA prefill tokens/s (%s)" % spec.name,
+            "value": tok_per_s,
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": ms_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": spec.name, "B": B, "T": T, "H": H, "d_k": d, "d_v": d,
+                       "chunk": 64, "storage": spec.dtype, "num_seqs": N,
+                       "l2": "inputs (%.2f GB) larger than L2, no flush" % (pbytes / 1e9),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "kernel": "kda_chunk_fwd (all phases)",
+                         "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes_per_launch": pbytes,
+                         "peak_source": peaks["source"],
+                         "phases_ms": phase_ms, "dominant_phase": dominant,
+                         "tensor_tflops": flops / (ms_step / 1e3) / 1e12,
+                         "tensor_frac": flops / (ms_step / 1e3) / 1e12 / peaks["bf16_tflops"]},
+            "cpu_baseline": {"value": cpu_val, "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": e2e_tok_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": 3 * K + steps_total,
+            "clocks": clocks,
+            "decode": {
+                "metric": "KDA decode steps/s (%s)" % dspec.name,
+                "value": dec_steps_s, "unit": "steps/s", "ms_per_step": dec_ms_launch,
+                "roofline": {"bound": "hbm", "kernel": "decode_step_kernel",
+                             "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": dec_gbs / peaks["hbm_gbs"], "traffic": None,
+                             "algorithmic_bytes_per_launch": dbytes},
+                "e2e": {"value": world * dspec.steps / (de_ms / 1e3), "unit": "steps/s",
+                        "h2d_bytes_per_step": d_h2d, "d2h_bytes_per_step": d_d2h},
+                "cpu_baseline": {"value": dcpu_val, "unit": "steps/s", "cores": dcores,
+                                 "kind": "oracle", "sample": dsample},
+            },
+        }
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    return result
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def bench_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return None
+    spec = PREFILL_WORKLOADS[args.workload]
+    if args.T:
+        spec = kin.with_(spec, T=args.T)
+    inp = kin.make_prefill(spec)
+    B = inp["q"].shape[0]
+    # Size each step so the whole run stays within a few minutes.
+    budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    _, cores, sample, n_tok = oracle_prefill_sample(inp, spec,
+                                                    target_s=min(budget, args.cpu_seconds))
+    times = []
+    import oracle
+    arr = {k: inp[k][:, :n_tok].to(torch.float64).numpy() for k in ("q", "k", "v", "g", "beta")}
+    init = None if inp["init_state"] is None else inp["init_state"][:B].double().numpy()
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.scan(arr["q"], arr["k"], arr["v"], arr["g"], arr["beta"], inp["scale"], init)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    val = n_tok * B * len(times) / total
+    return {
+        "impl": "reference",
+        "metric": "KDA prefill tokens/s (%s)" % spec.name,
+        "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": spec.name, "B": B, "T": inp["q"].shape[1], "H": spec.H,
+                   "d_k": spec.d, "d_v": spec.d, "chunk": 64, "storage": spec.dtype},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(PREFILL_WORKLOADS), default="long")
+    ap.add_argument("--T", type=int, default=0, help="override the per-sequence length")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target duration of the oracle baseline sample")
+    args = ap.parse_args(argv)
+    res = bench_reference(args) if args.impl == "reference" else bench_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,159 @@
+/*
+ * kda.h — C ABI of the Kimi Delta Attention (KDA) gated delta-rule scan for
+ * NVIDIA GB300 (sm_103a). Library: libkda.so.
+ *
+ * The operation, per sequence and head, with state S in R^{d_k x d_v}
+ * (row c = key channel c), per-token log-decay g_t (a_t = exp(g_t) in (0,1]^{d_k}),
+ * write strength beta_t and query scale s:
+ *
+ *     S~_t = Diag(a_t) S_{t-1}
+ *     S_t  = S~_t + beta_t k_t (v_t - S~_t^T k_t)^T
+ *     o_t  = S_t^T (s q_t)
+ *
+ * ("Understanding Kimi Delta Attention", box "KDA: Retain, predict, correct";
+ *  the query scale as in "Demystifying Kimi Delta Attention", opening KDA
+ *  equations.)
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    keeps no reference after the call returns. Scratch memory is passed in
+ *    explicitly (kda_chunk_fwd's workspace); the library itself allocates no
+ *    device memory.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream); there
+ *    is no implicit synchronisation. Results are valid once the stream
+ *    reaches the call.
+ *  - Layouts are dense row-major with the last dimension contiguous:
+ *      q, k, g    [tokens][H][d_k]     v, out [tokens][H][d_v]
+ *      beta       [tokens][H]
+ *      states     [num_seqs][H][d_k][d_v]  (fp32; row c = key channel c)
+ *    where `tokens` is B*T for fixed-length batches (sequence b occupies
+ *    tokens [b*T, (b+1)*T)) and cu_seqlens[num_seqs] for packed sequences.
+ *  - q, k, v and out share one storage dtype (kda_dtype); g, beta and the
+ *    states are always fp32. Arithmetic is fp32 (bf16 tensor-core operands
+ *    with fp32 accumulation on the bf16 prefill path).
+ *  - Supported sizes: d_k == d_v, and d_k in {64, 128}. Other sizes return
+ *    KDA_ERR_UNSUPPORTED.
+ *  - Tensor pointers must be 16-byte aligned, except beta and cu_seqlens
+ *    (4-byte aligned).
+ *  - Errors are returned as kda_status; nothing is thrown and nothing is
+ *    printed. Argument checks happen on the host before any CUDA call; a
+ *    launch failure returns KDA_ERR_CUDA (the CUDA error is left for the
+ *    caller's cudaGetLastError()/cudaPeekAtLastError() to inspect).
+ *  - Inputs are expected to satisfy g <= 0 (finite), beta in [0, 1]; the
+ *    chunked prefill factors each pair decay through references at most
+ *    eight tokens away, so a per-token log-decay below about -10 can
+ *    overflow fp32 in the bf16 path. Values outside these ranges are not
+ *    checked on the device.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* NULL required pointer, bad size or alignment */
+    KDA_ERR_UNSUPPORTED = 2,      /* valid request this build does not implement */
+    KDA_ERR_WORKSPACE = 3,        /* workspace NULL or smaller than required */
+    KDA_ERR_CUDA = 4,             /* a CUDA runtime call or kernel launch failed */
+    KDA_ERR_TIMEOUT = 5           /* a bounded device-side wait gave up */
+} kda_status;
+
+typedef enum {
+    KDA_DTYPE_F32 = 0, /* q, k, v, out are fp32 */
+    KDA_DTYPE_BF16 = 1 /* q, k, v, out are bf16 */
+} kda_dtype;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *kda_status_string(kda_status status);
+
+/*
+ * Bytes of device workspace kda_chunk_fwd needs for these sizes.
+ * B, T: batch and per-sequence length when cu_seqlens is NULL; with packed
+ * sequences pass B = 1, T = total tokens (= cu_seqlens[num_seqs]) and
+ * num_seqs = number of sequences. The bound holds for every split of T into
+ * num_seqs sequences. Returns 0 for invalid or unsupported sizes (and for
+ * T == 0 with no sequence to carry).
+ */
+size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs,
+                                    kda_dtype dtype);
+
+/*
+ * Chunkwise-parallel prefill ("Understanding Kimi Delta Attention", sections
+ * "The triangular system", "Putting the chunks together" and Figure 04):
+ * each chunk of up to 64 tokens forms its cumulative log-decay, the
+ * correction matrix A, T = (I - A)^{-1} by a triangular solve, and the WY/UT
+ * factors; the state then crosses chunk boundaries one chunk at a time, and
+ * every token's output is read from the state entering its chunk plus the
+ * chunk's own corrections.
+ *
+ *  q, k       [tokens][H][dk], dtype      query (unscaled) and key
+ *  v          [tokens][H][dv], dtype      value
+ *  g          [tokens][H][dk], fp32       per-token log-decay log a_t (<= 0)
+ *  beta       [tokens][H], fp32           write strength
+ *  scale      query scale (normally dk^-1/2), applied to q only
+ *  init_state [num_seqs][H][dk][dv] fp32, or NULL for zero initial states
+ *  cu_seqlens int32 [num_seqs + 1] device array, or NULL. When given: B must
+ *             be 1, T = cu_seqlens[num_seqs], values non-decreasing from 0.
+ *             The contents are trusted (not read on the host).
+ *  out        [tokens][H][dv], dtype      token outputs o_t (written)
+ *  final_state[num_seqs][H][dk][dv] fp32 (written), or NULL. May alias
+ *             init_state exactly (in-place state carry).
+ *  B, T, H, dk, dv, num_seqs: sizes; without cu_seqlens num_seqs must be B.
+ *  workspace  device scratch of at least kda_chunk_fwd_workspace_size(...)
+ *             bytes, 256-byte aligned; contents on entry are ignored and on
+ *             return are unspecified. Must not alias any other argument.
+ *  stream     CUDA stream for all work.
+ *
+ * A zero-length sequence writes its initial state (or zeros) to final_state.
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                         const float *beta, float scale, const float *init_state,
+                         const int32_t *cu_seqlens, void *out, float *final_state, int B, int T,
+                         int H, int dk, int dv, int num_seqs, kda_dtype dtype, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * kda_chunk_fwd with phase markers for timing: identical arguments, results
+ * and errors, plus `events`, an array of 4 caller-created CUDA events (any
+ * entry may be NULL) recorded on `stream` at the start of the call (0), after
+ * the chunk table is built (1), after the intra-chunk phase (2) and after the
+ * inter-chunk state pass (3). Pass events created without
+ * cudaEventDisableTiming to read phase durations with cudaEventElapsedTime.
+ */
+kda_status kda_chunk_fwd_timed(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, float scale, const float *init_state,
+                               const int32_t *cu_seqlens, void *out, float *final_state, int B,
+                               int T, int H, int dk, int dv, int num_seqs, kda_dtype dtype,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream,
+                               cudaEvent_t *events);
+
+/*
+ * One recurrent decode step for N independent sequences ("Kimi Delta
+ * Attention: How It Works, Step by Step", section 11; the update of
+ * "Understanding Kimi Delta Attention", box "KDA: Retain, predict, correct"),
+ * fused into one pass over the state: with a = exp(g),
+ *     vhat = (a o k)^T S,  e = beta (v - vhat),
+ *     o    = (a o (s q))^T S + (s q^T k) e,   S <- Diag(a) S + k e^T.
+ *
+ *  q, k   [N][H][dk], dtype;  v, out [N][H][dv], dtype
+ *  g      [N][H][dk] fp32;    beta [N][H] fp32
+ *  state  [N][H][dk][dv] fp32, read and updated in place
+ *  No workspace is needed.
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float scale, float *state, void *out, int N, int H,
+                           int dk, int dv, kda_dtype dtype, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,9 @@
+"""Kimi Delta Attention gated delta-rule scan for GB300 (sm_103a).
+
+The compute lives in libkda.so (C ABI: include/kda.h); this package is its thin
+Python binding plus the seeded synthetic-input generator. Importing the package
+does not load the library; the first call does, and raises if it is missing.
+"""
+from .kda import chunk_fwd, decode_step, status_string, workspace_size  # noqa: F401
+
+__all__ = ["chunk_fwd", "decode_step", "status_string", "workspace_size"]

@@ -1,0 +1,208 @@
+// The C ABI of libkda.so: argument validation, workspace sizing, the chunk
+// table, and dispatch to the prefill and decode kernels. Every argument check
+// happens here, on the host, before any CUDA call.
+#include <math.h>
+
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+// Builds the chunk table on the device (cu_seqlens lives there; reading it on
+// the host would need a synchronising copy). One CTA: an exclusive scan of
+// per-sequence chunk counts, then each sequence writes its own slots; the
+// slots past the last used one are marked unused.
+constexpr int kTableThreads = 1024;
+
+__global__ void __launch_bounds__(kTableThreads)
+chunk_table_kernel(const int32_t *__restrict__ cu_seqlens, int num_seqs, int T_fixed,
+                   long long slots, ChunkEntry *__restrict__ table,
+                   int *__restrict__ seq_first_slot) {
+    __shared__ int part[kTableThreads];
+    const int tid = threadIdx.x;
+    // Sequences [lo, hi) belong to this thread.
+    const int per = (num_seqs + kTableThreads - 1) / kTableThreads;
+    const int lo = min(num_seqs, tid * per), hi = min(num_seqs, lo + per);
+    auto seq_bounds = [&](int n, int &bos, int &len) {
+        if (cu_seqlens) {
+            bos = cu_seqlens[n];
+            len = cu_seqlens[n + 1] - bos;
+        } else {
+            bos = n * T_fixed;
+            len = T_fixed;
+        }
+    };
+    int mine = 0;
+    for (int n = lo; n < hi; ++n) {
+        int bos, len;
+        seq_bounds(n, bos, len);
+        mine += (len + kChunk - 1) / kChunk;
+    }
+    part[tid] = mine;
+    __syncthreads();
+    // Inclusive Hillis-Steele scan over the per-thread totals.
+    for (int off = 1; off < kTableThreads; off <<= 1) {
+        const int add = tid >= off ? part[tid - off] : 0;
+        __syncthreads();
+        part[tid] += add;
+        __syncthreads();
+    }
+    int slot = part[tid] - mine;
+    for (int n = lo; n < hi; ++n) {
+        int bos, len;
+        seq_bounds(n, bos, len);
+        seq_first_slot[n] = slot;
+        for (int c = 0; c * kChunk < len; ++c, ++slot) {
+            ChunkEntry e;
+            e.seq = n;
+            e.bos = bos + c * kChunk;
+            e.len = min(kChunk, len - c * kChunk);
+            e.idx = c;
+            if (slot < slots) table[slot] = e;  // cu_seqlens is trusted; never write past the table
+        }
+    }
+    const int used = part[kTableThreads - 1];
+    if (tid == 0) seq_first_slot[num_seqs] = used;
+    for (long long s = used + tid; s < slots; s += kTableThreads) {
+        ChunkEntry e;
+        e.seq = -1;
+        e.bos = 0;
+        e.len = 0;
+        e.idx = 0;
+        table[s] = e;
+    }
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dims_ok(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
+
+// Bytes of the per-path region that follows the chunk table.
+size_t path_region_bytes(long long slots, int H, int d, kda_dtype /*dtype*/) {
+    return (size_t)slots * (size_t)H * simt_region_bytes(d);
+}
+
+}  // namespace
+
+cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fixed,
+                               long long slots, ChunkEntry *table, int *seq_first_slot,
+                               cudaStream_t stream) {
+    chunk_table_kernel<<<1, kTableThreads, 0, stream>>>(cu_seqlens, num_seqs, T_fixed, slots,
+                                                        table, seq_first_slot);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" const char *kda_status_string(kda_status status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+extern "C" size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num_seqs,
+                                               kda_dtype dtype) {
+    if (B <= 0 || T < 0 || H <= 0 || num_seqs <= 0) return 0;
+    if (!dims_ok(dk, dv)) return 0;
+    if (dtype != KDA_DTYPE_F32 && dtype != KDA_DTYPE_BF16) return 0;
+    const bool packed = num_seqs != B;
+    if (packed && B != 1) return 0;
+    const long long slots = max_chunk_slots(B, T, num_seqs, packed);
+    return table_bytes(slots, num_seqs) + path_region_bytes(slots, H, dk, dtype);
+}
+
+namespace {
+
+kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float scale, const float *init_state,
+                          const int32_t *cu_seqlens, void *out, float *final_state, int B, int T,
+                          int H, int dk, int dv, int num_seqs, kda_dtype dtype, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream, cudaEvent_t *events) {
+    if (dtype != KDA_DTYPE_F32 && dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (B <= 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0 || num_seqs <= 0)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARGUMENT;
+    if (cu_seqlens ? B != 1 : num_seqs != B) return KDA_ERR_INVALID_ARGUMENT;
+    if ((long long)B * T * H * (dk > dv ? dk : dv) >= (1LL << 40)) return KDA_ERR_INVALID_ARGUMENT;
+    if ((long long)B * T >= (1LL << 31) - kChunk) return KDA_ERR_INVALID_ARGUMENT;
+    const bool have_tokens = (long long)B * T > 0;
+    if (have_tokens && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(out) ||
+        !aligned16(init_state) || !aligned16(final_state))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(beta) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    const size_t need = kda_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dtype);
+    if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_WORKSPACE;
+
+    // The same slot bound as kda_chunk_fwd_workspace_size (one packed sequence
+    // is bounded like a fixed-length batch of one).
+    const bool packed = cu_seqlens != nullptr;
+    const long long slots = max_chunk_slots(B, T, num_seqs, num_seqs != B);
+    char *ws = static_cast<char *>(workspace);
+    ChunkEntry *table = reinterpret_cast<ChunkEntry *>(ws);
+    int *seq_first_slot =
+        reinterpret_cast<int *>(ws + align_up((size_t)slots * sizeof(ChunkEntry), 256));
+    float *region = reinterpret_cast<float *>(ws + table_bytes(slots, num_seqs));
+    const int T_fixed = packed ? 0 : T;
+
+    if (events && events[0] && cudaEventRecord(events[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaError_t err = launch_chunk_table(cu_seqlens, num_seqs, T_fixed, slots, table,
+                                         seq_first_slot, stream);
+    if (err != cudaSuccess) return KDA_ERR_CUDA;
+    err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                              T_fixed, H, dk, num_seqs, dtype, slots, table, seq_first_slot, region,
+                              stream, events);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
+                                    const float *beta, float scale, const float *init_state,
+                                    const int32_t *cu_seqlens, void *out, float *final_state,
+                                    int B, int T, int H, int dk, int dv, int num_seqs,
+                                    kda_dtype dtype, void *workspace, size_t workspace_bytes,
+                                    cudaStream_t stream) {
+    return chunk_fwd_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B, T,
+                          H, dk, dv, num_seqs, dtype, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" kda_status kda_chunk_fwd_timed(const void *q, const void *k, const void *v,
+                                          const float *g, const float *beta, float scale,
+                                          const float *init_state, const int32_t *cu_seqlens,
+                                          void *out, float *final_state, int B, int T, int H,
+                                          int dk, int dv, int num_seqs, kda_dtype dtype,
+                                          void *workspace, size_t workspace_bytes,
+                                          cudaStream_t stream, cudaEvent_t *events) {
+    return chunk_fwd_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B, T,
+                          H, dk, dv, num_seqs, dtype, workspace, workspace_bytes, stream, events);
+}
+
+extern "C" kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
+                                      const float *beta, float scale, float *state, void *out,
+                                      int N, int H, int dk, int dv, kda_dtype dtype,
+                                      cudaStream_t stream) {
+    if (dtype != KDA_DTYPE_F32 && dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARGUMENT;
+    if ((long long)N * H >= (1LL << 31)) return KDA_ERR_INVALID_ARGUMENT;
+    if (N > 0 && (!q || !k || !v || !g || !beta || !state || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(state) ||
+        !aligned16(out))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(beta) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    const cudaError_t err = launch_decode(q, k, v, g, beta, scale, state, out, N, H, dk, dtype, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}

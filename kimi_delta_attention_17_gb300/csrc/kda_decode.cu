@@ -1,0 +1,139 @@
+// Single-token recurrent decode step, fused into one pass over the state.
+//
+// Per (sequence, head), with a = exp(g), the update of "Understanding Kimi
+// Delta Attention" (box "KDA: Retain, predict, correct") reads
+//     S' = Diag(a) S + k e^T,  e = beta (v - (Diag(a) S)^T k),  o = S'^T (s q).
+// Expanding the read, S'^T (s q) = S^T (a o s q) + (s q^T k) e, so the old
+// state is read exactly once: both reductions over the key channels,
+//     vhat = S^T (a o k)   and   p = S^T (a o s q),
+// come from the same registers, then e and o follow, then S' is written.
+//
+// The step is pure HBM streaming (64 KiB read + 64 KiB written per head at
+// d = 128 against ~1.3 KiB of token inputs). One CTA of 128 threads owns a
+// 32-column slab of one head's state: 16 row groups x 8 column quads, each
+// thread holding d/16 float4 rows of the slab in registers; all loads are
+// issued before any arithmetic and each warp touches 4 full 128-byte rows.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kDecodeThreads = 128;
+constexpr int kSlab = 32;  // state columns per CTA
+
+template <int D, typename InT>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_step_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT *__restrict__ v,
+                   const float *__restrict__ g, const float *__restrict__ beta, float scale,
+                   float *__restrict__ state, InT *__restrict__ out) {
+    constexpr int R = D / 16;  // rows per thread
+    const int nh = blockIdx.x;           // (sequence, head) flattened
+    const int col0 = blockIdx.y * kSlab;  // first state column of this slab
+    const int tid = threadIdx.x;
+    const int cq = tid & 7;   // column quad within the slab
+    const int rg = tid >> 3;  // row group 0..15; rows rg + 16 m
+
+    float *S = state + (size_t)nh * D * D + col0 + 4 * cq;
+    float4 s[R];
+#pragma unroll
+    for (int m = 0; m < R; ++m)
+        s[m] = *reinterpret_cast<const float4 *>(S + (size_t)(rg + 16 * m) * D);
+
+    const size_t tok = (size_t)nh * D;
+    float av[R], ak[R], aq[R], kr[R];
+    float qk = 0.f;
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const int r = rg + 16 * m;
+        const float a = expf(g[tok + r]);
+        const float kk = to_f32(k[tok + r]);
+        const float qq = scale * to_f32(q[tok + r]);
+        av[m] = a;
+        kr[m] = kk;
+        ak[m] = a * kk;
+        aq[m] = a * qq;
+        qk += qq * kk;
+    }
+    float4 vh = make_float4(0.f, 0.f, 0.f, 0.f), po = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        vh.x += ak[m] * s[m].x; vh.y += ak[m] * s[m].y; vh.z += ak[m] * s[m].z; vh.w += ak[m] * s[m].w;
+        po.x += aq[m] * s[m].x; po.y += aq[m] * s[m].y; po.z += aq[m] * s[m].z; po.w += aq[m] * s[m].w;
+    }
+    // Sum over the 4 row groups of this warp (lanes 8 apart) ...
+#pragma unroll
+    for (int off = 8; off < 32; off <<= 1) {
+        vh.x += __shfl_xor_sync(0xffffffffu, vh.x, off);
+        vh.y += __shfl_xor_sync(0xffffffffu, vh.y, off);
+        vh.z += __shfl_xor_sync(0xffffffffu, vh.z, off);
+        vh.w += __shfl_xor_sync(0xffffffffu, vh.w, off);
+        po.x += __shfl_xor_sync(0xffffffffu, po.x, off);
+        po.y += __shfl_xor_sync(0xffffffffu, po.y, off);
+        po.z += __shfl_xor_sync(0xffffffffu, po.z, off);
+        po.w += __shfl_xor_sync(0xffffffffu, po.w, off);
+        qk += __shfl_xor_sync(0xffffffffu, qk, off);
+    }
+    // ... then over the 4 warps.
+    __shared__ float red[4][8][9];
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane < 8) {
+        float *r = red[warp][lane];
+        r[0] = vh.x; r[1] = vh.y; r[2] = vh.z; r[3] = vh.w;
+        r[4] = po.x; r[5] = po.y; r[6] = po.z; r[7] = po.w;
+        r[8] = qk;
+    }
+    __syncthreads();
+    float tot[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) tot[i] = red[0][cq][i] + red[1][cq][i] + red[2][cq][i] + red[3][cq][i];
+
+    const float b = beta[nh];
+    const size_t vo = (size_t)nh * D + col0 + 4 * cq;
+    float e[4], o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        e[i] = b * (to_f32(v[vo + i]) - tot[i]);
+        o[i] = tot[4 + i] + tot[8] * e[i];
+    }
+    if (rg == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) out[vo + i] = from_f32<InT>(o[i]);
+    }
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        const float a = av[m];
+        float4 n;
+        n.x = a * s[m].x + kr[m] * e[0];
+        n.y = a * s[m].y + kr[m] * e[1];
+        n.z = a * s[m].z + kr[m] * e[2];
+        n.w = a * s[m].w + kr[m] * e[3];
+        *reinterpret_cast<float4 *>(S + (size_t)(rg + 16 * m) * D) = n;
+    }
+}
+
+template <int D, typename InT>
+cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, float scale, float *state, void *out, int N, int H,
+                            cudaStream_t stream) {
+    dim3 grid((unsigned)(N * H), D / kSlab);
+    decode_step_kernel<D, InT><<<grid, kDecodeThreads, 0, stream>>>(
+        static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g,
+        beta, scale, state, static_cast<InT *>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float scale, float *state, void *out, int N, int H,
+                          int d, kda_dtype dtype, cudaStream_t stream) {
+    if (N == 0) return cudaSuccess;
+    if (dtype == KDA_DTYPE_BF16) {
+        return d == 128 ? launch_decode_t<128, __nv_bfloat16>(q, k, v, g, beta, scale, state, out, N, H, stream)
+                        : launch_decode_t<64, __nv_bfloat16>(q, k, v, g, beta, scale, state, out, N, H, stream);
+    }
+    return d == 128 ? launch_decode_t<128, float>(q, k, v, g, beta, scale, state, out, N, H, stream)
+                    : launch_decode_t<64, float>(q, k, v, g, beta, scale, state, out, N, H, stream);
+}
+
+}  // namespace kda

@@ -1,0 +1,78 @@
+// Internal declarations shared by the translation units of libkda.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// Tokens per chunk of the chunkwise prefill.
+constexpr int kChunk = 64;
+
+// One chunk of one sequence: tokens [bos, bos + len) of sequence `seq`,
+// the `idx`-th chunk of that sequence. seq < 0 marks an unused slot.
+struct ChunkEntry {
+    int seq;
+    int bos;
+    int len;
+    int idx;
+};
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Upper bound on chunk slots: exact for fixed-length batches, and for packed
+// sequences sum_n ceil(len_n / 64) <= ceil(T / 64) + num_seqs.
+inline long long max_chunk_slots(int B, int T, int num_seqs, bool packed) {
+    const long long per = (T + kChunk - 1) / kChunk;
+    return packed ? per + num_seqs : (long long)B * per;
+}
+
+// Workspace part 1: the chunk table, then per-sequence first-slot offsets.
+inline size_t table_bytes(long long slots, int num_seqs) {
+    return align_up((size_t)slots * sizeof(ChunkEntry), 256) +
+           align_up((size_t)(num_seqs + 1) * sizeof(int), 256);
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Fills `table` and `seq_first_slot` from cu_seqlens (device) or, when
+// cu_seqlens is NULL, from num_seqs sequences of length T_fixed.
+cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fixed,
+                               long long slots, ChunkEntry *table, int *seq_first_slot,
+                               cudaStream_t stream);
+
+// fp32 SIMT prefill (any storage dtype; the reference-precision path).
+size_t simt_region_bytes(int d);
+cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float scale, const float *init_state,
+                                const int32_t *cu_seqlens, void *out, float *final_state,
+                                int T_fixed, int H, int d, int num_seqs, kda_dtype dtype,
+                                long long slots, const ChunkEntry *table,
+                                const int *seq_first_slot, float *region, cudaStream_t stream,
+                                cudaEvent_t *events);
+
+// Records events[i] (when non-NULL) on the stream: the prefill marks the
+// start (0), the end of the chunk table (1), of the intra-chunk phase (2) and
+// of the state pass (3).
+inline cudaError_t mark(cudaEvent_t *events, int i, cudaStream_t stream) {
+    return (events && events[i]) ? cudaEventRecord(events[i], stream) : cudaSuccess;
+}
+
+// Decode step.
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float scale, float *state, void *out, int N, int H,
+                          int d, kda_dtype dtype, cudaStream_t stream);
+
+}  // namespace kda

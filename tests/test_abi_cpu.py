@@ -1,0 +1,100 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every
+function include/kda.h declares, and its host-side validation rejects bad
+arguments before any CUDA call (so these run without a GPU)."""
+import ctypes
+
+import pytest
+
+from kimi_delta_attention_17_gb300 import _lib, build
+
+INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return _lib.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = _lib.declared_symbols()
+    assert set(names) >= {"kda_chunk_fwd", "kda_decode_step", "kda_chunk_fwd_workspace_size",
+                          "kda_status_string"}
+    for n in names:
+        assert hasattr(L, n), "libkda.so does not export %s" % n
+
+
+def test_status_strings(L):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert L.kda_status_string(code).decode() == name
+    assert L.kda_status_string(99).decode() == "KDA_ERR_UNKNOWN"
+
+
+def test_workspace_size_rules(L):
+    ws = L.kda_chunk_fwd_workspace_size
+    assert ws(2, 4096, 16, 128, 128, 2, 1) > 0
+    assert ws(1, 100, 2, 64, 64, 1, 0) > 0
+    # Unsupported head sizes and invalid shapes report 0.
+    assert ws(1, 64, 1, 96, 96, 1, 1) == 0
+    assert ws(1, 64, 1, 128, 64, 1, 1) == 0
+    assert ws(2, 64, 1, 128, 128, 3, 1) == 0      # packed needs B == 1
+    assert ws(1, 64, 0, 128, 128, 1, 1) == 0
+    # Monotone in T and H; packed bound covers one extra chunk per sequence.
+    assert ws(1, 128, 4, 64, 64, 1, 1) < ws(1, 129, 4, 64, 64, 1, 1)
+    assert ws(1, 1000, 4, 64, 64, 1, 1) < ws(1, 1000, 8, 64, 64, 1, 1)
+    assert ws(1, 1000, 4, 64, 64, 1, 1) < ws(1, 1000, 4, 64, 64, 5, 1)
+    # Zero tokens with sequences to carry is valid.
+    assert ws(1, 0, 4, 64, 64, 3, 1) > 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned address that is never dereferenced on these paths
+
+
+def fwd(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.1, init=None, cu=None, out=FAKE,
+             fin=FAKE, B=1, T=64, H=1, dk=64, dv=64, N=1, dt=1, ws=FAKE, wsb=1 << 40, stream=None)
+    a.update(kw)
+    return L.kda_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["init"],
+                           a["cu"], a["out"], a["fin"], a["B"], a["T"], a["H"], a["dk"], a["dv"],
+                           a["N"], a["dt"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_chunk_fwd_rejects_bad_arguments(L):
+    assert fwd(L, q=None) == INVALID
+    assert fwd(L, out=None) == INVALID
+    assert fwd(L, beta=None) == INVALID
+    assert fwd(L, H=0) == INVALID
+    assert fwd(L, T=-1) == INVALID
+    assert fwd(L, dt=7) == INVALID
+    assert fwd(L, scale=float("nan")) == INVALID
+    assert fwd(L, N=2) == INVALID                 # N must equal B without cu_seqlens
+    assert fwd(L, cu=FAKE, B=2, N=2) == INVALID   # packed needs B == 1
+    assert fwd(L, q=FAKE + 4) == INVALID          # misaligned
+    assert fwd(L, beta=FAKE + 2) == INVALID
+    assert fwd(L, dk=96, dv=96) == UNSUPPORTED
+    assert fwd(L, dk=128, dv=64) == UNSUPPORTED
+    assert fwd(L, ws=None) == WORKSPACE
+    assert fwd(L, wsb=16) == WORKSPACE
+    assert fwd(L, ws=FAKE + 16) == WORKSPACE      # workspace must be 256-byte aligned
+
+
+def test_decode_rejects_bad_arguments(L):
+    def dec(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, scale=0.1, S=FAKE, out=FAKE, N=4, H=2,
+                 dk=128, dv=128, dt=1, stream=None)
+        a.update(kw)
+        return L.kda_decode_step(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["S"],
+                                 a["out"], a["N"], a["H"], a["dk"], a["dv"], a["dt"], a["stream"])
+    assert dec(S=None) == INVALID
+    assert dec(N=-1) == INVALID
+    assert dec(H=0) == INVALID
+    assert dec(S=FAKE + 8) == INVALID
+    assert dec(dk=32, dv=32) == UNSUPPORTED
+    assert dec(dt=3) == INVALID
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.lib()
