@@ -136,6 +136,41 @@ kda_status kda_chunk_fwd_timed(const void *q, const void *k, const void *v, cons
                                cudaEvent_t *events);
 
 /*
+ * Capacity, in bytes, of the scratch array kda_chunk_fwd_noalloc uses: 64 MiB.
+ * A problem fits when kda_chunk_fwd_workspace_size(...) for its sizes is at
+ * most this value.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * The chunkwise prefill for callers that cannot allocate device memory: code
+ * that may not call cudaMalloc (for instance a host callback or stream-ordered
+ * work where allocation is forbidden, a process whose allocator must not be
+ * re-entered, or an embedding that owns all memory statically). The paper has
+ * no counterpart; it is a deployment convenience.
+ *
+ * Same arguments, results and errors as kda_chunk_fwd, without `workspace`:
+ * the scratch is a 256-byte aligned file-scope device array of
+ * KDA_NOALLOC_SCRATCH_BYTES inside libkda.so, which every GPU that loads the
+ * library holds until the process exits. This call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *  - Sizes whose kda_chunk_fwd_workspace_size exceeds KDA_NOALLOC_SCRATCH_BYTES
+ *    are rejected with KDA_ERR_WORKSPACE before any CUDA call.
+ *  - The first call on each device resolves the array's device address with
+ *    cudaGetSymbolAddress (with that device current) and caches it; make that
+ *    first call before any stream capture begins.
+ *  - Every call, on every stream, shares the one array and it keeps the last
+ *    call's contents. Nothing in it needs to start at zero (each call rebuilds
+ *    everything it reads), but calls whose work overlaps on the GPU race on it:
+ *    order them on one stream or synchronise between them.
+ */
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, float scale, const float *init_state,
+                                 const int32_t *cu_seqlens, void *out, float *final_state, int B,
+                                 int T, int H, int dk, int dv, int num_seqs, kda_dtype dtype,
+                                 cudaStream_t stream);
+
+/*
  * One recurrent decode step for N independent sequences ("Kimi Delta
  * Attention: How It Works, Step by Step", section 11; the update of
  * "Understanding Kimi Delta Attention", box "KDA: Retain, predict, correct"),

@@ -23,6 +23,8 @@ _SIGNATURES = {
                       + [ctypes.c_int] * 7 + [_vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "kda_chunk_fwd_timed": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
                             + [ctypes.c_int] * 7 + [_vp, ctypes.c_size_t, _vp, _vp], ctypes.c_int),
+    "kda_chunk_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
+                              + [ctypes.c_int] * 7 + [_vp], ctypes.c_int),
     "kda_decode_step": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]
                         + [ctypes.c_int] * 5 + [_vp], ctypes.c_int),
 }
