@@ -17,9 +17,10 @@ constexpr int kTableThreads = 1024;
 __global__ void __launch_bounds__(kTableThreads)
 chunk_table_kernel(const int32_t *__restrict__ cu_seqlens, int num_seqs, int T_fixed,
                    long long slots, ChunkEntry *__restrict__ table,
-                   int *__restrict__ seq_first_slot) {
+                   int *__restrict__ seq_first_slot, int *__restrict__ status) {
     __shared__ int part[kTableThreads];
     const int tid = threadIdx.x;
+    if (tid == 0) *status = 0;
     // Sequences [lo, hi) belong to this thread.
     const int per = (num_seqs + kTableThreads - 1) / kTableThreads;
     const int lo = min(num_seqs, tid * per), hi = min(num_seqs, lo + per);
@@ -77,18 +78,22 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool dims_ok(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
 
+// The tensor-core path serves bf16 storage with d = 128; the fp32 SIMT path
+// serves everything else (fp32 storage, and d = 64).
+bool use_tc(int d, kda_dtype dtype) { return dtype == KDA_DTYPE_BF16 && d == 128; }
+
 // Bytes of the per-path region that follows the chunk table.
-size_t path_region_bytes(long long slots, int H, int d, kda_dtype /*dtype*/) {
-    return (size_t)slots * (size_t)H * simt_region_bytes(d);
+size_t path_region_bytes(long long slots, int H, int d, kda_dtype dtype) {
+    return (size_t)slots * (size_t)H * (use_tc(d, dtype) ? tc_region_bytes() : simt_region_bytes(d));
 }
 
 }  // namespace
 
 cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fixed,
                                long long slots, ChunkEntry *table, int *seq_first_slot,
-                               cudaStream_t stream) {
+                               int *status, cudaStream_t stream) {
     chunk_table_kernel<<<1, kTableThreads, 0, stream>>>(cu_seqlens, num_seqs, T_fixed, slots,
-                                                        table, seq_first_slot);
+                                                        table, seq_first_slot, status);
     return cudaGetLastError();
 }
 
@@ -150,19 +155,26 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     const bool packed = cu_seqlens != nullptr;
     const long long slots = max_chunk_slots(B, T, num_seqs, num_seqs != B);
     char *ws = static_cast<char *>(workspace);
-    ChunkEntry *table = reinterpret_cast<ChunkEntry *>(ws);
-    int *seq_first_slot =
-        reinterpret_cast<int *>(ws + align_up((size_t)slots * sizeof(ChunkEntry), 256));
-    float *region = reinterpret_cast<float *>(ws + table_bytes(slots, num_seqs));
+    int *status = reinterpret_cast<int *>(ws);
+    ChunkEntry *table = reinterpret_cast<ChunkEntry *>(ws + kWsHeader);
+    int *seq_first_slot = reinterpret_cast<int *>(
+        ws + kWsHeader + align_up((size_t)slots * sizeof(ChunkEntry), 256));
+    char *region = ws + table_bytes(slots, num_seqs);
     const int T_fixed = packed ? 0 : T;
 
     if (events && events[0] && cudaEventRecord(events[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
     cudaError_t err = launch_chunk_table(cu_seqlens, num_seqs, T_fixed, slots, table,
-                                         seq_first_slot, stream);
+                                         seq_first_slot, status, stream);
     if (err != cudaSuccess) return KDA_ERR_CUDA;
-    err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
-                              T_fixed, H, dk, num_seqs, dtype, slots, table, seq_first_slot, region,
-                              stream, events);
+    if (use_tc(dk, dtype))
+        err = launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                                T_fixed, H, num_seqs, slots, table, seq_first_slot,
+                                reinterpret_cast<unsigned char *>(region), status, stream, events);
+    else
+        err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
+                                  final_state, T_fixed, H, dk, num_seqs, dtype, slots, table,
+                                  seq_first_slot, reinterpret_cast<float *>(region), stream,
+                                  events);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -30,9 +30,20 @@ inline long long max_chunk_slots(int B, int T, int num_seqs, bool packed) {
     return packed ? per + num_seqs : (long long)B * per;
 }
 
-// Workspace part 1: the chunk table, then per-sequence first-slot offsets.
+// Grid over (head, chunk slot) with heads fastest; slots fold over y and z
+// because gridDim.y is limited to 65535.
+inline dim3 head_slot_grid(int H, long long slots) {
+    const long long y = slots < 65535 ? slots : 65535;
+    return dim3((unsigned)H, (unsigned)(y > 0 ? y : 1), (unsigned)((slots + y - 1) / (y > 0 ? y : 1)));
+}
+
+// Workspace layout: a 256-byte header whose first int is the device status
+// word (0, or a kda_status a kernel left after a bounded wait gave up), then
+// the chunk table, the per-sequence first-slot offsets, and the per-path
+// regions.
+constexpr size_t kWsHeader = 256;
 inline size_t table_bytes(long long slots, int num_seqs) {
-    return align_up((size_t)slots * sizeof(ChunkEntry), 256) +
+    return kWsHeader + align_up((size_t)slots * sizeof(ChunkEntry), 256) +
            align_up((size_t)(num_seqs + 1) * sizeof(int), 256);
 }
 
@@ -48,10 +59,11 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 
 // Fills `table` and `seq_first_slot` from cu_seqlens (device) or, when
-// cu_seqlens is NULL, from num_seqs sequences of length T_fixed.
+// cu_seqlens is NULL, from num_seqs sequences of length T_fixed, and clears
+// the status word.
 cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fixed,
                                long long slots, ChunkEntry *table, int *seq_first_slot,
-                               cudaStream_t stream);
+                               int *status, cudaStream_t stream);
 
 // fp32 SIMT prefill (any storage dtype; the reference-precision path).
 size_t simt_region_bytes(int d);
@@ -62,6 +74,16 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 long long slots, const ChunkEntry *table,
                                 const int *seq_first_slot, float *region, cudaStream_t stream,
                                 cudaEvent_t *events);
+
+// Tensor-core prefill (bf16 storage, d = 128).
+size_t tc_region_bytes();
+cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, float scale, const float *init_state,
+                              const int32_t *cu_seqlens, void *out, float *final_state,
+                              int T_fixed, int H, int num_seqs, long long slots,
+                              const ChunkEntry *table, const int *seq_first_slot,
+                              unsigned char *region, int *status, cudaStream_t stream,
+                              cudaEvent_t *events);
 
 // Records events[i] (when non-NULL) on the stream: the prefill marks the
 // start (0), the end of the chunk table (1), of the intra-chunk phase (2) and

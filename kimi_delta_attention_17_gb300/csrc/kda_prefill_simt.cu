@@ -57,11 +57,14 @@ template <int D, typename InT>
 __global__ void __launch_bounds__(kThreads)
 simt_chunk_prep(const InT *__restrict__ q, const InT *__restrict__ k, const InT *__restrict__ v,
                 const float *__restrict__ g, const float *__restrict__ beta, float scale,
-                const ChunkEntry *__restrict__ table, int H, float *__restrict__ ws) {
+                const ChunkEntry *__restrict__ table, long long nslots, int H,
+                float *__restrict__ ws) {
     constexpr int P = D + 1;  // padded row stride
-    const ChunkEntry ce = table[blockIdx.x];
+    const int h = blockIdx.x;  // heads fastest: resident CTAs read whole token rows
+    const long long slot = (long long)blockIdx.z * gridDim.y + blockIdx.y;
+    if (slot >= nslots) return;
+    const ChunkEntry ce = table[slot];
     if (ce.seq < 0) return;
-    const int h = blockIdx.y;
     const int tid = threadIdx.x;
 
     extern __shared__ float sm[];
@@ -129,7 +132,7 @@ simt_chunk_prep(const InT *__restrict__ q, const InT *__restrict__ k, const InT 
         }
     }
 
-    float *reg = ws + ((size_t)blockIdx.x * H + h) * region_floats<D>();
+    float *reg = ws + ((size_t)slot * H + h) * region_floats<D>();
     // Kbar and exp(G_n) (G is flat past the last real token, so row 63 holds G_n).
     for (int idx = tid; idx < kChunk * D; idx += kThreads) {
         const int i = idx / D, c = idx % D;
@@ -283,9 +286,9 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
     if (err != cudaSuccess) return err;
     if ((err = mark(events, 1, stream)) != cudaSuccess) return err;
     if (slots > 0) {
-        simt_chunk_prep<D, InT><<<dim3((unsigned)slots, H), kThreads, s1, stream>>>(
+        simt_chunk_prep<D, InT><<<head_slot_grid(H, slots), kThreads, s1, stream>>>(
             static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g,
-            beta, scale, table, H, region);
+            beta, scale, table, slots, H, region);
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }

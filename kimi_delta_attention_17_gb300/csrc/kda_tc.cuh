@@ -1,0 +1,159 @@
+// Inline-PTX helpers for the tensor-core (tcgen05 / TMEM / bulk-copy)
+// kernels of the prefill. sm_100-family only.
+//
+// Shared-memory operand tiles use the no-swizzle canonical layouts of
+// tcgen05.mma: 8 x 16-byte "core matrices" of 128 contiguous bytes. In a
+// K-major tile a core holds 8 rows (M or N index) x 8 consecutive K elements;
+// in an MN-major tile a core holds 8 consecutive K rows x 8 consecutive M/N
+// elements. The descriptor's leading byte offset (LBO) is the distance between
+// cores adjacent along K, its stride byte offset (SBO) the distance between
+// cores adjacent along M/N.
+#pragma once
+
+#include <stdint.h>
+
+namespace kda {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Byte offset of element (mn, k) of a 16-bit K-major tile.
+__host__ __device__ constexpr uint32_t kmaj(int mn, int k, uint32_t lbo, uint32_t sbo) {
+    return (uint32_t)(mn >> 3) * sbo + (uint32_t)(k >> 3) * lbo + (uint32_t)(mn & 7) * 16u +
+           (uint32_t)(k & 7) * 2u;
+}
+// Byte offset of element (mn, k) of a 16-bit MN-major tile.
+__host__ __device__ constexpr uint32_t mnmaj(int mn, int k, uint32_t lbo, uint32_t sbo) {
+    return (uint32_t)(mn >> 3) * sbo + (uint32_t)(k >> 3) * lbo + (uint32_t)(k & 7) * 16u +
+           (uint32_t)(mn & 7) * 2u;
+}
+
+// Shared-memory matrix descriptor, no swizzle.
+__device__ __forceinline__ uint64_t desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator.
+// a_mn / b_mn select MN-major (1) or K-major (0) operands.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A * B^T over one K=16 step.
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{.reg .pred p; setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void commit(uint64_t *mbar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(mbar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// async proxy (tensor core, bulk copies).
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Allocates `ncols` TMEM columns (power of two >= 32); one whole warp calls.
+template <int ncols>
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "n"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+}
+template <int ncols>
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(ncols));
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective;
+// the address must name the warp's own 32-lane slice).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%"
+        "15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mbar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Bounded wait for the phase with the given parity to complete. Returns false
+// if it gave up (after roughly a second or more of polling).
+__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
+    const uint32_t a = smem_u32(mbar);
+    for (uint32_t it = 0; it < (1u << 22); ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, "
+            "0, p;}"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` transactions on mbar.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+        : "memory");
+}
+
+// Packs 8 floats as 8 bf16 (round to nearest even) into one 16-byte vector.
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    uint4 r;
+    r.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[0])) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[1])) << 16);
+    r.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[2])) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[3])) << 16);
+    r.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[4])) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[5])) << 16);
+    r.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[6])) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[7])) << 16);
+    return r;
+}
+
+}  // namespace tc
+}  // namespace kda

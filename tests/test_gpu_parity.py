@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from kimi_delta_attention_17_gb300 import build, chunk_fwd, decode_step
+from kimi_delta_attention_17_gb300 import build, chunk_fwd, decode_step, workspace_size
 from kimi_delta_attention_17_gb300.inputs import (SMALL_FP32, DecodeSpec, PrefillSpec, make_decode,
                                                   make_prefill)
 from tests.helpers import assert_parity, f64, oracle_prefill
@@ -28,9 +28,15 @@ def run_prefill(inp, alias=False, want_final=True):
     init = None if inp["init_state"] is None else inp["init_state"].to(dev)
     cu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].to(dev)
     final = init if alias else None
+    B, T, H, d = q.shape
+    ws = torch.empty(workspace_size(B, T, H, d, d, len(inp["lengths"]), q.dtype),
+                     dtype=torch.uint8, device=dev)
     out, fin = chunk_fwd(q, k, v, g, beta, inp["scale"], init, cu, final_state=final,
-                         output_final_state=want_final)
+                         output_final_state=want_final, workspace=ws)
     torch.cuda.synchronize()
+    # The device status word (first int of the workspace) stays 0 unless a
+    # bounded device-side wait gave up.
+    assert int(ws[:4].view(torch.int32).item()) == 0
     return f64(out), (None if fin is None else f64(fin))
 
 
