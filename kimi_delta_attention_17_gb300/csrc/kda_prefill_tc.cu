@@ -55,7 +55,7 @@ constexpr int kTN = 32;  // state columns per phase-2 CTA
 struct TcRegion {
     static constexpr size_t A1 = 0;        // [W; Q'] bf16, MN-major, 128 tokens x 128 ch
     static constexpr size_t A2 = 32768;    // Kbar^T bf16, K-major, 128 ch x 64 tokens
-    static constexpr size_t U = 49152;     // fp32 [D/kTN][64][kTN], rows swizzled
+    static constexpr size_t U = 49152;     // fp32 [128 columns][64 tokens] (transposed)
     static constexpr size_t Ou = 81920;    // same layout as U
     static constexpr size_t Gam = 114688;  // fp32 [128] exp(G_n)
     static constexpr size_t bytes = 115200;
@@ -64,357 +64,454 @@ struct TcRegion {
 constexpr uint32_t kA1Lbo = 128, kA1Sbo = 2048;  // MN-major: channel cores adjacent
 constexpr uint32_t kA2Lbo = 2048, kA2Sbo = 128;  // K-major: channel groups adjacent
 
-// Position of U/Ou element (token i, column j within a kTN slab): float4
-// groups of a row are XOR-swizzled by (i & 7) so that one thread per row
-// reads its row without bank conflicts.
-__device__ __forceinline__ int slab_idx(int i, int j) {
-    return i * kTN + ((((j >> 2) ^ (i & 7))) << 2) + (j & 3);
-}
-
 // ---------------------------------------------------------------- phase 1
-// Shared memory of the intra-chunk kernel (bytes).
-constexpr int kP1R1 = 0;        // 36 KiB: [Ktilde; Qtilde] -> A, T fp32 -> L^T, V^T -> W^T, U^T
-constexpr int kP1R2 = 36864;    // 40 KiB: column versions -> H, T*B, scratch X
-constexpr int kP1E = 77824;     // 32 KiB: E fp32 [64][128]
-constexpr int kP1Beta = 110592; // 64 floats
-constexpr int kP1Bar = 110848;  // mbarrier
-constexpr int kP1Tmem = 110856; // TMEM base address
-constexpr int kP1Smem = 110880;
-constexpr int kAS = 65;         // row stride (floats) of A and T in shared memory
+// Persistent: one CTA per SM walks the (chunk slot, head) items, heads
+// fastest. The raw rows of the next item (q, k, v bf16 and g fp32, one 1-D
+// bulk copy per token row and tensor, issued by 256 threads at once) stream
+// into the staging area while the current item runs its MMAs, solve and
+// stores. Thread (c, half) owns key/value channel c and tokens
+// [32 half, 32 half + 32) in the elementwise pass; for TMEM read-back thread
+// t owns lane t mod 128, the two halves of the CTA splitting the columns.
+constexpr int kP1Threads = 256;
+struct P1 {  // shared-memory offsets, bytes
+    static constexpr int q = 0, k = 16384, v = 32768, g = 49152;  // staging rows of one chunk
+    static constexpr int am = 81920;    // [Ktilde; s Qtilde] bf16, MN-major 128 x 128
+    static constexpr int bm = 114688;   // column versions bf16, MN-major 160 x 128
+    static constexpr int lt = 155648;   // L^T (later W^T) bf16, K-major [channel][token]
+    static constexpr int vt = 172032;   // V^T (later U^T)
+    static constexpr int qb = 188416;   // s Qbar fp32 [channel][token], 16-byte chunks swizzled
+    static constexpr int beta = 221184; // 64 floats
+    static constexpr int refs = 221440; // fp32 [5][128]: G at tokens 7, 23, 39, 55, 63
+    static constexpr int tot = 224000;  // fp32 [128]: G at token 31
+    static constexpr int bar = 224512;  // mbarriers: staging loaded, MMA done
+    static constexpr int tmem = 224528;
+    static constexpr int bytes = 224544;
+    // Reused once the first MMA has consumed am / bm:
+    static constexpr int As = am;                // fp32 [64][65]: A
+    static constexpr int Ts = am + 16640;        // fp32 [64][65]: T
+    static constexpr int Hs = am + 33280;        // bf16 K-major [i][j]: H (LBO 1024, SBO 128)
+    static constexpr int TBs = Hs + 8192;        // bf16 K-major [i][j]: T Diag(beta)
+    static constexpr int Xs = TBs + 8192;        // fp32 [3][16][16] scratch of the solve
+};
+static_assert(P1::Xs + 3072 <= P1::lt, "solve scratch overlaps L^T");
+static_assert(P1::bytes <= 232448, "phase-1 shared memory exceeds 227 KiB");
+constexpr int kAS = 65;  // row stride (floats) of A and T
 
 // (I, J) of column version v = I (I + 1) / 2 + J.
-__device__ __forceinline__ constexpr int ver_I(int v) { return v < 1 ? 0 : v < 3 ? 1 : v < 6 ? 2 : 3; }
-__device__ __forceinline__ constexpr int ver_J(int v) { return v - ver_I(v) * (ver_I(v) + 1) / 2; }
+__host__ __device__ constexpr int ver_I(int v) { return v < 1 ? 0 : v < 3 ? 1 : v < 6 ? 2 : 3; }
+__host__ __device__ constexpr int ver_J(int v) { return v - ver_I(v) * (ver_I(v) + 1) / 2; }
 
-__device__ __forceinline__ float ldbf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void st16(unsigned char *p, const float *x) {
+    *reinterpret_cast<uint4 *>(p) = pack8(x);
+}
 
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(kP1Threads, 1)
 tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
                const float *__restrict__ beta, float scale, const ChunkEntry *__restrict__ table,
                long long nslots, int H, unsigned char *__restrict__ ws, int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    // Heads vary fastest across the grid, so CTAs resident together read whole
-    // token rows ([token][head][channel]) rather than one head's slice of many.
-    const int h = blockIdx.x;
-    const long long slot = (long long)blockIdx.z * gridDim.y + blockIdx.y;
-    if (slot >= nslots) return;
-    const ChunkEntry ce = table[slot];
-    if (ce.seq < 0) return;
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int c = tid;  // key/value channel owned by this thread
-    unsigned char *R1 = sm + kP1R1;
-    unsigned char *R2 = sm + kP1R2;
-    float *Es = reinterpret_cast<float *>(sm + kP1E);
-    float *beta_s = reinterpret_cast<float *>(sm + kP1Beta);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + kP1Bar);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kP1Tmem);
-    unsigned char *reg = ws + ((size_t)slot * H + h) * TcRegion::bytes;
+    const int c = tid & 127, half = tid >> 7;
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + P1::bar);
+    uint64_t *bar_mma = bar_ld + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P1::tmem);
+    float *beta_s = reinterpret_cast<float *>(sm + P1::beta);
+    float *refs = reinterpret_cast<float *>(sm + P1::refs);
+    float *tot = reinterpret_cast<float *>(sm + P1::tot);
+    const long long nitems = nslots * H;
 
     if (warp == 0) tmem_alloc<256>(tslot);
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_mma, 1);
         mbar_fence_init();
     }
-
-    const int len = ce.len;
-    const size_t row0 = (size_t)ce.bos * H + h;  // token row of the chunk's first token
-    auto at = [&](int i) { return (row0 + (size_t)i * H) * D + c; };
-
-    // ---- cumulative log-decay, block references, E_i = exp(G_i - G_r(block i)).
-    float G[C];
-#pragma unroll
-    for (int i = 0; i < C; ++i) G[i] = i < len ? __ldg(g + at(i)) : 0.f;
-#pragma unroll
-    for (int i = 1; i < C; ++i) G[i] += G[i - 1];
-    const float Rf[4] = {G[7], G[23], G[39], G[55]};
-    const float Gend = G[C - 1];
-#pragma unroll
-    for (int i = 0; i < C; ++i) Es[i * D + c] = __expf(G[i] - Rf[i >> 4]);
-    float P[4], Y[4];
-#pragma unroll
-    for (int I = 0; I < 4; ++I) {
-        P[I] = __expf(Rf[I]);         // exp(G_r(I)) from the chunk start
-        Y[I] = __expf(Gend - Rf[I]);  // exp(G_n - G_r(I))
-    }
-    float X[4][4];  // exp(G_r(I) - G_r(J)), J <= I
-#pragma unroll
-    for (int I = 0; I < 4; ++I)
-#pragma unroll
-        for (int J = 0; J < 4; ++J) X[I][J] = J < I ? __expf(Rf[I] - Rf[J]) : 1.f;
-    if (tid < C) beta_s[tid] = tid < len ? beta[row0 + (size_t)tid * H] : 0.f;
-
-    // ---- operands of the gated K K^T / Q K^T product, and Kbar^T.
-    // A operand (MN-major, 128 rows x 128 channels): rows i = Ktilde_i, 64+i = s Qtilde_i.
-    // B operand (MN-major, 160 rows): row 16 v(I,J) + (j mod 16) = k_j exp(G_r(I) - G_j).
-#pragma unroll
-    for (int ig = 0; ig < 8; ++ig) {
-        float kk[8], qq[8], e[8], f[8], t8[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int i = ig * 8 + r;
-            kk[r] = i < len ? ldbf(k + at(i)) : 0.f;
-            qq[r] = i < len ? scale * ldbf(q + at(i)) : 0.f;
-            e[r] = Es[i * D + c];
-            f[r] = 1.f / e[r];
-        }
-        const uint32_t a_off = (uint32_t)ig * kA1Sbo + (uint32_t)(c >> 3) * 128u + (uint32_t)(c & 7) * 16u;
-#pragma unroll
-        for (int r = 0; r < 8; ++r) t8[r] = kk[r] * e[r];
-        *reinterpret_cast<uint4 *>(R1 + a_off) = pack8(t8);
-#pragma unroll
-        for (int r = 0; r < 8; ++r) t8[r] = qq[r] * e[r];
-        *reinterpret_cast<uint4 *>(R1 + a_off + 8 * kA1Sbo) = pack8(t8);
-        const int J = ig >> 1;
-#pragma unroll
-        for (int I = 0; I < 4; ++I) {
-            if (I < J) continue;
-            const int n0 = 16 * (I * (I + 1) / 2 + J) + (ig & 1) * 8;
-#pragma unroll
-            for (int r = 0; r < 8; ++r) t8[r] = kk[r] * f[r] * X[I][J];
-            *reinterpret_cast<uint4 *>(R2 + (uint32_t)(n0 >> 3) * kA1Sbo + (uint32_t)(c >> 3) * 128u +
-                                       (uint32_t)(c & 7) * 16u) = pack8(t8);
-        }
-        // Kbar^T row c, tokens 8 ig .. 8 ig + 7: k_j exp(G_n - G_j).
-#pragma unroll
-        for (int r = 0; r < 8; ++r) t8[r] = kk[r] * f[r] * Y[J];
-        *reinterpret_cast<uint4 *>(reg + TcRegion::A2 + kmaj(c, ig * 8, kA2Lbo, kA2Sbo)) = pack8(t8);
-    }
-    fence_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    if (tid == 0) {
-        const uint32_t id = idesc_bf16(128, 160, 1, 1);
-#pragma unroll
-        for (int s = 0; s < D / 16; ++s)
-            mma_bf16(tmem, desc(smem_u32(R1) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo),
-                     desc(smem_u32(R2) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo), id, s > 0);
-        commit(bar);
-    }
-    bool ok = __syncthreads_and(mbar_wait(bar, 0));
-    fence_after();
-    if (!ok) goto fail;
+    auto next_item = [&](long long w) {
+        while (w < nitems && table[w / H].seq < 0) w += gridDim.x;
+        return w;
+    };
+    auto issue = [&](long long w) {
+        const ChunkEntry e = table[w / H];
+        const int hh = (int)(w % H);
+        const int tsel = tid >> 6, i = tid & 63;
+        if (tid == 0) mbar_expect_tx(bar_ld, (uint32_t)e.len * (3u * 256u + 512u));
+        if (i < e.len) {
+            const size_t row = ((size_t)(e.bos + i) * H + hh) * D;
+            if (tsel == 0) bulk_g2s(sm + P1::q + i * 256, q + row, 256, bar_ld);
+            else if (tsel == 1) bulk_g2s(sm + P1::k + i * 256, k + row, 256, bar_ld);
+            else if (tsel == 2) bulk_g2s(sm + P1::v + i * 256, v + row, 256, bar_ld);
+            else bulk_g2s(sm + P1::g + i * 512, g + row, 512, bar_ld);
+        }
+    };
 
-    {
-        // ---- A (fp32, for the solve) and H (bf16 B operand, K-major [i][j]).
-        float *As = reinterpret_cast<float *>(R1);
-        float *Ts = reinterpret_cast<float *>(R1 + 16640);
-        unsigned char *Hs = R2;                  // K-major [N = i][K = j]: LBO 1024, SBO 128
-        unsigned char *TBs = R2 + 8192;          // same layout
-        float *Xs = reinterpret_cast<float *>(R2 + 16384);
-        const int i = tid & 63, Iblk = i >> 4;
-        const bool isH = tid >= 64;
-        const float bi = beta_s[i];
+    long long w = next_item(blockIdx.x);
+    if (w < nitems) issue(w);
+    uint32_t ld_phase = 0, mma_phase = 0;
+    bool ok = true;
+    while (w < nitems) {
+        const ChunkEntry ce = table[w / H];
+        const int h = (int)(w % H);
+        const int len = ce.len;
+        unsigned char *reg = ws + (size_t)w * TcRegion::bytes;  // w = slot * H + h
+        ok = __syncthreads_and(mbar_wait(bar_ld, ld_phase));
+        ld_phase ^= 1;
+        if (!ok) break;
+
+        // ================= elementwise pass (thread = channel c, 32 tokens)
+        {
+            const float *gs = reinterpret_cast<const float *>(sm + P1::g);
+            const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::q);
+            const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::k);
+            const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::v);
+            float G[32];
 #pragma unroll
-        for (int vv = 0; vv < 10; ++vv) {
-            const bool warp_uses = (warp & 1) ? vv >= 3 : vv < 3;  // warp-uniform
-            if (!warp_uses) continue;
-            float x[16];
-            tmem_ld16(tmem + lane_base + vv * 16, x);
-            tmem_wait_ld();
-            if (ver_I(vv) != Iblk) continue;
-            const int J = ver_J(vv);
-            if (!isH) {
+            for (int r = 0; r < 32; ++r) {
+                const int i = 32 * half + r;
+                G[r] = i < len ? gs[i * D + c] : 0.f;
+            }
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const int j = 16 * J + jj;
-                    As[i * kAS + j] = j < i ? -bi * x[jj] : 0.f;
+            for (int r = 1; r < 32; ++r) G[r] += G[r - 1];
+            if (half == 0) {
+                tot[c] = G[31];
+                refs[c] = G[7];
+                refs[128 + c] = G[23];
+            }
+            if (tid < C) beta_s[tid] = tid < len ? beta[(size_t)(ce.bos + tid) * H + h] : 0.f;
+            __syncthreads();
+            if (half == 1) {
+                const float o = tot[c];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) G[r] += o;
+                refs[256 + c] = G[7];
+                refs[384 + c] = G[23];
+                refs[512 + c] = G[31];
+            }
+            __syncthreads();
+            const float R0 = refs[c], R1 = refs[128 + c], R2 = refs[256 + c], R3 = refs[384 + c];
+            const float Gend = refs[512 + c];
+            // Per-channel block constants (see the header comment).
+            const float Rf[4] = {R0, R1, R2, R3};
+            float P[4], Y[4], X[4][4];
+#pragma unroll
+            for (int I = 0; I < 4; ++I) {
+                P[I] = __expf(Rf[I]);
+                Y[I] = __expf(Gend - Rf[I]);
+#pragma unroll
+                for (int J = 0; J < 4; ++J) X[I][J] = J < I ? __expf(Rf[I] - Rf[J]) : 1.f;
+            }
+            float *qbar = reinterpret_cast<float *>(sm + P1::qb) + c * C;
+#pragma unroll
+            for (int ig = 0; ig < 4; ++ig) {
+                const int jj = ig >> 1;               // block within this half
+                const int i0 = 32 * half + 8 * ig;    // first token of the group
+                const int Jr = 2 * half + jj;         // block index of these tokens
+                const float Rs = half ? Rf[2 + jj] : Rf[jj];
+                const float Ps = half ? P[2 + jj] : P[jj];
+                const float Ys = half ? Y[2 + jj] : Y[jj];
+                float kv[8], qv[8], vv[8], E[8], kF[8], t8[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int i = i0 + r;
+                    const bool in = i < len;
+                    kv[r] = in ? __bfloat162float(ks[i * D + c]) : 0.f;
+                    qv[r] = in ? scale * __bfloat162float(qs[i * D + c]) : 0.f;
+                    vv[r] = in ? __bfloat162float(vs[i * D + c]) : 0.f;
+                    const float x = G[8 * ig + r] - Rs;
+                    E[r] = __expf(x);
+                    kF[r] = kv[r] * __expf(-x);
                 }
-            } else {
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float t8[8];
+                for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r];
+                st16(sm + P1::am + mnmaj(i0, c, kA1Lbo, kA1Sbo), t8);
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) t8[r] = (16 * J + 8 * hf + r <= i) ? x[8 * hf + r] : 0.f;
-                    *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J + 8 * hf, 1024, 128)) = pack8(t8);
+                for (int r = 0; r < 8; ++r) t8[r] = qv[r] * E[r];
+                st16(sm + P1::am + mnmaj(64 + i0, c, kA1Lbo, kA1Sbo), t8);
+#pragma unroll
+                for (int I = 0; I < 4; ++I) {
+                    if (I < Jr) continue;
+                    const float Xs = half ? X[I][2 + jj] : X[I][jj];
+                    const int n0 = 16 * (I * (I + 1) / 2 + Jr) + 8 * (ig & 1);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) t8[r] = kF[r] * Xs;
+                    st16(sm + P1::bm + mnmaj(n0, c, kA1Lbo, kA1Sbo), t8);
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) t8[r] = kF[r] * Ys;
+                st16(reg + TcRegion::A2 + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
+#pragma unroll
+                for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r] * Ps;
+                st16(sm + P1::lt + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
+                st16(sm + P1::vt + kmaj(c, i0, kA2Lbo, kA2Sbo), vv);
+#pragma unroll
+                for (int h4 = 0; h4 < 2; ++h4) {
+                    const int chunk = (i0 >> 2) + h4;  // 4-token fp32 chunk of row c
+                    *reinterpret_cast<float4 *>(qbar + ((chunk ^ (c & 7)) << 2)) =
+                        make_float4(qv[4 * h4] * E[4 * h4] * Ps, qv[4 * h4 + 1] * E[4 * h4 + 1] * Ps,
+                                    qv[4 * h4 + 2] * E[4 * h4 + 2] * Ps, qv[4 * h4 + 3] * E[4 * h4 + 3] * Ps);
                 }
             }
+            if (half == 1) reinterpret_cast<float *>(reg + TcRegion::Gam)[c] = __expf(Gend);
         }
+        fence_async_smem();
+        fence_before();
+        __syncthreads();
+        fence_after();
+
+        // The staging rows are consumed: fetch the next item's while this one runs.
+        const long long wn = next_item(w + gridDim.x);
+        if (wn < nitems) issue(wn);
+
+        // ================= A / H = gated K K^T and Q K^T (M=128, N=160, K=128)
+        if (tid == 0) {
+            const uint32_t id = idesc_bf16(128, 160, 1, 1);
 #pragma unroll
-        for (int J = 0; J < 4; ++J) {
-            if (J <= Iblk) continue;
-            if (!isH) {
+            for (int s = 0; s < D / 16; ++s)
+                mma_bf16(tmem, desc(smem_u32(sm + P1::am) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo),
+                         desc(smem_u32(sm + P1::bm) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo), id, s > 0);
+            commit(bar_mma);
+        }
+        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
+        mma_phase ^= 1;
+        fence_after();
+        if (!ok) break;
+        {
+            float *As = reinterpret_cast<float *>(sm + P1::As);
+            unsigned char *Hs = sm + P1::Hs;
+            const int lr = tid & 127, i = lr & 63, Iblk = i >> 4;
+            const bool isH = lr >= 64;
+            const int side = warp >> 2;
+            const bool upper = (warp & 1) != 0;  // rows 32-63: blocks 2, 3
+            const float bi = beta_s[i];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) As[i * kAS + 16 * J + jj] = 0.f;
-            } else {
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J, 1024, 128)) = z;
-                *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J + 8, 1024, 128)) = z;
+            for (int vv = 0; vv < 10; ++vv) {
+                // Versions of this warp's rows, split between the two halves of the CTA.
+                const bool mine = upper ? (side ? vv >= 7 : (vv >= 3 && vv < 7))
+                                        : (side ? vv == 2 : vv < 2);
+                if (!mine) continue;  // warp-uniform
+                float x[16];
+                tmem_ld16(tmem + lane_base + vv * 16, x);
+                tmem_wait_ld();
+                if (ver_I(vv) != Iblk) continue;
+                const int J = ver_J(vv);
+                if (!isH) {
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const int j = 16 * J + jj;
+                        As[i * kAS + j] = j < i ? -bi * x[jj] : 0.f;
+                    }
+                } else {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float t8[8];
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) t8[r] = (16 * J + 8 * hf + r <= i) ? x[8 * hf + r] : 0.f;
+                        st16(Hs + kmaj(i, 16 * J + 8 * hf, 1024, 128), t8);
+                    }
+                }
+            }
+            if (side == 0) {
+#pragma unroll
+                for (int J = 0; J < 4; ++J) {
+                    if (J <= Iblk) continue;
+                    if (!isH) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) As[i * kAS + 16 * J + jj] = 0.f;
+                    } else {
+                        const uint4 z = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J, 1024, 128)) = z;
+                        *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J + 8, 1024, 128)) = z;
+                    }
+                }
             }
         }
         fence_before();
         __syncthreads();
 
-        // ---- T = (I - A)^{-1}. Diagonal 16x16 blocks by forward substitution
-        // (thread = column), then T_IJ = T_II sum_{K=J}^{I-1} A_IK T_KJ by levels.
-        if (tid < 64) {
-            const int I = tid >> 4, col = tid;
-            float x[16];
+        // ================= T = (I - A)^{-1}, then T Diag(beta) as a bf16 operand.
+        {
+            const float *As = reinterpret_cast<const float *>(sm + P1::As);
+            float *Ts = reinterpret_cast<float *>(sm + P1::Ts);
+            float *Xs = reinterpret_cast<float *>(sm + P1::Xs);
+            if (tid < 64) {
+                const int I = tid >> 4, col = tid;
+                float x[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int ii = 16 * I + r;
-                float acc = ii == col ? 1.f : 0.f;
+                for (int r = 0; r < 16; ++r) {
+                    const int ii = 16 * I + r;
+                    float acc = ii == col ? 1.f : 0.f;
 #pragma unroll
-                for (int rr = 0; rr < r; ++rr) acc += As[ii * kAS + 16 * I + rr] * x[rr];
-                x[r] = ii < col ? 0.f : acc;
-                Ts[ii * kAS + col] = x[r];
+                    for (int rr = 0; rr < r; ++rr) acc += As[ii * kAS + 16 * I + rr] * x[rr];
+                    x[r] = ii < col ? 0.f : acc;
+                    Ts[ii * kAS + col] = x[r];
+                }
             }
-        }
-        __syncthreads();
+            __syncthreads();
 #pragma unroll
-        for (int L = 1; L <= 3; ++L) {
-            const int npairs = 4 - L;
-            for (int o = tid; o < npairs * 256; o += 128) {
-                const int p = o >> 8, r = (o >> 4) & 15, cc = o & 15;
-                const int J = p, I = J + L;
-                float acc = 0.f;
-                for (int K = J; K < I; ++K)
+            for (int L = 1; L <= 3; ++L) {
+                const int npairs = 4 - L;
+                for (int o = tid; o < npairs * 256; o += kP1Threads) {
+                    const int p = o >> 8, r = (o >> 4) & 15, cc = o & 15;
+                    const int J = p, I = J + L;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int K = 0; K < L; ++K)
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk)
+                            acc += As[(16 * I + r) * kAS + 16 * (J + K) + kk] *
+                                   Ts[(16 * (J + K) + kk) * kAS + 16 * J + cc];
+                    Xs[p * 256 + r * 16 + cc] = acc;
+                }
+                __syncthreads();
+                for (int o = tid; o < npairs * 256; o += kP1Threads) {
+                    const int p = o >> 8, r = (o >> 4) & 15, cc = o & 15;
+                    const int J = p, I = J + L;
+                    float acc = 0.f;
 #pragma unroll
                     for (int kk = 0; kk < 16; ++kk)
-                        acc += As[(16 * I + r) * kAS + 16 * K + kk] * Ts[(16 * K + kk) * kAS + 16 * J + cc];
-                Xs[p * 256 + r * 16 + cc] = acc;
+                        acc += Ts[(16 * I + r) * kAS + 16 * I + kk] * Xs[p * 256 + kk * 16 + cc];
+                    Ts[(16 * I + r) * kAS + 16 * J + cc] = acc;
+                }
+                __syncthreads();
             }
-            __syncthreads();
-            for (int o = tid; o < npairs * 256; o += 128) {
-                const int p = o >> 8, r = (o >> 4) & 15, cc = o & 15;
-                const int J = p, I = J + L;
-                float acc = 0.f;
+            const int i = tid & 63, jq = tid >> 6;
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    acc += Ts[(16 * I + r) * kAS + 16 * I + kk] * Xs[p * 256 + kk * 16 + cc];
-                Ts[(16 * I + r) * kAS + 16 * J + cc] = acc;
-            }
-            __syncthreads();
-        }
-
-        // ---- T B (bf16 B operand, K-major [N = i][K = j]).
-        {
-            const int hf = tid >> 6;
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int jb = 32 * hf + 8 * q4;
+            for (int hf = 0; hf < 2; ++hf) {
+                const int jb = 16 * jq + 8 * hf;
                 float t8[8];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int j = jb + r;
                     t8[r] = j <= i ? Ts[i * kAS + j] * beta_s[j] : 0.f;
                 }
-                *reinterpret_cast<uint4 *>(TBs + kmaj(i, jb, 1024, 128)) = pack8(t8);
+                st16(sm + P1::TBs + kmaj(i, jb, 1024, 128), t8);
             }
-        }
-        __syncthreads();
-
-        // ---- L^T and V^T (A operands, K-major [M = channel][K = token]) into R1.
-#pragma unroll
-        for (int jg = 0; jg < 8; ++jg) {
-            float t8[8], u8[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int j = jg * 8 + r;
-                t8[r] = j < len ? ldbf(k + at(j)) * Es[j * D + c] * P[jg >> 1] : 0.f;
-                u8[r] = j < len ? ldbf(v + at(j)) : 0.f;
-            }
-            *reinterpret_cast<uint4 *>(R1 + kmaj(c, jg * 8, kA2Lbo, kA2Sbo)) = pack8(t8);
-            *reinterpret_cast<uint4 *>(R1 + 16384 + kmaj(c, jg * 8, kA2Lbo, kA2Sbo)) = pack8(u8);
         }
         fence_async_smem();
         fence_before();
         __syncthreads();
         fence_after();
+
+        // ================= W = (T B) L, U = (T B) V
         if (tid == 0) {
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
             for (int s = 0; s < C / 16; ++s) {
-                const uint64_t b = desc(smem_u32(TBs) + s * 2 * 1024, 1024, 128);
-                mma_bf16(tmem + 0, desc(smem_u32(R1) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
-                mma_bf16(tmem + 64, desc(smem_u32(R1 + 16384) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id,
-                         s > 0);
+                const uint64_t b = desc(smem_u32(sm + P1::TBs) + s * 2 * 1024, 1024, 128);
+                mma_bf16(tmem + 0, desc(smem_u32(sm + P1::lt) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
+                mma_bf16(tmem + 64, desc(smem_u32(sm + P1::vt) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
             }
-            commit(bar);
+            commit(bar_mma);
         }
-        ok = __syncthreads_and(mbar_wait(bar, 1));
+        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
+        mma_phase ^= 1;
         fence_after();
-        if (!ok) goto fail;
-
-        // ---- W, U: workspace copies for the state pass, and W^T, U^T operands.
-        float *Uw = reinterpret_cast<float *>(reg + TcRegion::U) + (size_t)(c / kTN) * C * kTN;
+        if (!ok) break;
+        {
+            const int side = tid >> 7;
+            float *slab = reinterpret_cast<float *>(reg + TcRegion::U) + (size_t)c * C;  // [c][i]
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            float w16[16], u16[16];
-            tmem_ld16(tmem + lane_base + 16 * part, w16);
-            tmem_ld16(tmem + lane_base + 64 + 16 * part, u16);
-            tmem_wait_ld();
+            for (int part = 0; part < 4; ++part) {
+                float x[16];
+                tmem_ld16(tmem + lane_base + 64 * side + 16 * part, x);
+                tmem_wait_ld();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int i0 = 16 * part + 8 * hf;
-                const uint4 wp = pack8(w16 + 8 * hf);
-                *reinterpret_cast<uint4 *>(reg + TcRegion::A1 + mnmaj(i0, c, kA1Lbo, kA1Sbo)) = wp;
-                *reinterpret_cast<uint4 *>(R1 + kmaj(c, i0, kA2Lbo, kA2Sbo)) = wp;
-                *reinterpret_cast<uint4 *>(R1 + 16384 + kmaj(c, i0, kA2Lbo, kA2Sbo)) = pack8(u16 + 8 * hf);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int i0 = 16 * part + 8 * hf;
+                    if (side == 0) {
+                        const uint4 wp = pack8(x + 8 * hf);
+                        *reinterpret_cast<uint4 *>(reg + TcRegion::A1 + mnmaj(i0, c, kA1Lbo, kA1Sbo)) = wp;
+                        *reinterpret_cast<uint4 *>(sm + P1::lt + kmaj(c, i0, kA2Lbo, kA2Sbo)) = wp;
+                    } else {
+                        st16(sm + P1::vt + kmaj(c, i0, kA2Lbo, kA2Sbo), x + 8 * hf);
+                    }
+                }
+                if (side == 1) {
+#pragma unroll
+                    for (int f = 0; f < 4; ++f)
+                        *reinterpret_cast<float4 *>(slab + 16 * part + 4 * f) =
+                            make_float4(x[4 * f], x[4 * f + 1], x[4 * f + 2], x[4 * f + 3]);
+                }
             }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Uw[slab_idx(16 * part + r, c % kTN)] = u16[r];
         }
         fence_async_smem();
         fence_before();
         __syncthreads();
         fence_after();
+
+        // ================= H W and H U
         if (tid == 0) {
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
             for (int s = 0; s < C / 16; ++s) {
-                const uint64_t b = desc(smem_u32(Hs) + s * 2 * 1024, 1024, 128);
-                mma_bf16(tmem + 128, desc(smem_u32(R1) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
-                mma_bf16(tmem + 192, desc(smem_u32(R1 + 16384) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id,
-                         s > 0);
+                const uint64_t b = desc(smem_u32(sm + P1::Hs) + s * 2 * 1024, 1024, 128);
+                mma_bf16(tmem + 128, desc(smem_u32(sm + P1::lt) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
+                mma_bf16(tmem + 192, desc(smem_u32(sm + P1::vt) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
             }
-            commit(bar);
+            commit(bar_mma);
         }
-        ok = __syncthreads_and(mbar_wait(bar, 0));
+        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
+        mma_phase ^= 1;
         fence_after();
-        if (!ok) goto fail;
-
-        // ---- Q' = Qbar - H W (rows 64..127 of A1) and Ou = H U.
-        float *Ow = reinterpret_cast<float *>(reg + TcRegion::Ou) + (size_t)(c / kTN) * C * kTN;
+        if (!ok) break;
+        {
+            const int side = tid >> 7;
+            const float *qbar = reinterpret_cast<const float *>(sm + P1::qb) + c * C;
+            float *slab = reinterpret_cast<float *>(reg + TcRegion::Ou) + (size_t)c * C;  // [c][i]
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-            float d16[16], o16[16], t16[16];
-            tmem_ld16(tmem + lane_base + 128 + 16 * part, d16);
-            tmem_ld16(tmem + lane_base + 192 + 16 * part, o16);
-            tmem_wait_ld();
+            for (int part = 0; part < 4; ++part) {
+                float x[16];
+                tmem_ld16(tmem + lane_base + 128 + 64 * side + 16 * part, x);
+                tmem_wait_ld();
+                if (side == 0) {
+                    float t16[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int ii = 16 * part + r;
-                const float qb = ii < len ? scale * ldbf(q + at(ii)) * Es[ii * D + c] * P[part] : 0.f;
-                t16[r] = qb - d16[r];
-                Ow[slab_idx(ii, c % kTN)] = o16[r];
+                    for (int f = 0; f < 4; ++f) {
+                        const int chunk = 4 * part + f;
+                        const float4 qb = *reinterpret_cast<const float4 *>(qbar + ((chunk ^ (c & 7)) << 2));
+                        t16[4 * f] = qb.x - x[4 * f];
+                        t16[4 * f + 1] = qb.y - x[4 * f + 1];
+                        t16[4 * f + 2] = qb.z - x[4 * f + 2];
+                        t16[4 * f + 3] = qb.w - x[4 * f + 3];
+                    }
+                    st16(reg + TcRegion::A1 + mnmaj(64 + 16 * part, c, kA1Lbo, kA1Sbo), t16);
+                    st16(reg + TcRegion::A1 + mnmaj(64 + 16 * part + 8, c, kA1Lbo, kA1Sbo), t16 + 8);
+                } else {
+#pragma unroll
+                    for (int f = 0; f < 4; ++f)
+                        *reinterpret_cast<float4 *>(slab + 16 * part + 4 * f) =
+                            make_float4(x[4 * f], x[4 * f + 1], x[4 * f + 2], x[4 * f + 3]);
+                }
             }
-            *reinterpret_cast<uint4 *>(reg + TcRegion::A1 + mnmaj(64 + 16 * part, c, kA1Lbo, kA1Sbo)) =
-                pack8(t16);
-            *reinterpret_cast<uint4 *>(reg + TcRegion::A1 + mnmaj(64 + 16 * part + 8, c, kA1Lbo, kA1Sbo)) =
-                pack8(t16 + 8);
         }
-        reinterpret_cast<float *>(reg + TcRegion::Gam)[c] = __expf(Gend);
+        fence_before();
+        __syncthreads();
+        fence_after();
+        w = wn;
+    }
+    if (!ok) {
+        if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
+        // Bounded waits for copies and MMAs that may still be in flight.
+        mbar_wait(bar_ld, ld_phase);
+        mbar_wait(bar_mma, mma_phase);
     }
     fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc<256>(tmem);
-    return;
-
-fail:
-    if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
-    mbar_wait(bar, 0);  // bounded: let any MMA still in flight finish before freeing TMEM
-    mbar_wait(bar, 1);
-    fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc<256>(*tslot);
 }
 
 // ---------------------------------------------------------------- phase 2
+// One CTA of 256 threads per (sequence, head, 32-column slab). Thread t owns
+// TMEM lane / state row t mod 128 and slab columns [16 s, 16 s + 16) with
+// s = t / 128. U and Ou arrive transposed ([column][token]) so that the thread
+// of token row i reads them without bank conflicts.
+constexpr int kP2Threads = 256;
 constexpr int kBufBytes = 66560;  // one chunk's A1, A2, U slab, Ou slab, gamma (65 KiB)
 constexpr int kBufA2 = 32768, kBufU = 49152, kBufOu = 57344, kBufGam = 65536;
 constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 512;
@@ -426,13 +523,14 @@ constexpr int kP2Smem = kP2Tmem + 8;
 constexpr uint32_t kB1Lbo = 128, kB1Sbo = 2048;
 constexpr uint32_t kB2Lbo = 128, kB2Sbo = 1024;
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kP2Threads, 1)
 tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
               const int32_t *__restrict__ cu_seqlens, int T_fixed, const float *init_state,
               __nv_bfloat16 *__restrict__ out, float *final_state, int H, int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int n = blockIdx.x, h = blockIdx.y, jt = blockIdx.z, j0 = jt * kTN;
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int lr = tid & 127, side = tid >> 7, js = 16 * side;  // lane / row, first slab column
     int bos, len;
     if (cu_seqlens) {
         bos = cu_seqlens[n];
@@ -449,24 +547,22 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     uint64_t *bar_mma = bar_load + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kP2Tmem);
 
-    // Thread c owns state row c of the slab, columns j0 .. j0 + 31.
-    const int c = tid;
-    const size_t st_off = (((size_t)n * H + h) * D + c) * D + j0;
-    float S[kTN];
+    const int c = lr;  // state row
+    const size_t st_off = (((size_t)n * H + h) * D + c) * D + j0 + js;
+    float S[16];
     if (init_state) {
 #pragma unroll
-        for (int j = 0; j < kTN; j += 4) {
+        for (int j = 0; j < 16; j += 4) {
             const float4 t = *reinterpret_cast<const float4 *>(init_state + st_off + j);
             S[j] = t.x; S[j + 1] = t.y; S[j + 2] = t.z; S[j + 3] = t.w;
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < kTN; ++j) S[j] = 0.f;
+        for (int j = 0; j < 16; ++j) S[j] = 0.f;
     }
-    auto put_state = [&]() {
-        // B1 rows n = j (hi) and 32 + j (lo), K-row = channel c.
+    auto put_state = [&]() {  // B1 rows js + j (hi) and 32 + js + j (lo), K-row c
 #pragma unroll
-        for (int jg = 0; jg < kTN / 8; ++jg) {
+        for (int jg = 0; jg < 2; ++jg) {
             float hi[8], lo[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
@@ -474,8 +570,8 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 hi[r] = __bfloat162float(__float2bfloat16_rn(x));
                 lo[r] = x - hi[r];
             }
-            *reinterpret_cast<uint4 *>(B1 + mnmaj(8 * jg, c, kB1Lbo, kB1Sbo)) = pack8(hi);
-            *reinterpret_cast<uint4 *>(B1 + mnmaj(kTN + 8 * jg, c, kB1Lbo, kB1Sbo)) = pack8(lo);
+            st16(B1 + mnmaj(js + 8 * jg, c, kB1Lbo, kB1Sbo), hi);
+            st16(B1 + mnmaj(kTN + js + 8 * jg, c, kB1Lbo, kB1Sbo), lo);
         }
     };
     put_state();
@@ -492,7 +588,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     auto issue_load = [&](int ch, int b) {
         const unsigned char *r = ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes;
@@ -500,8 +596,8 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         mbar_expect_tx(bar_load + b, kLoadBytes);
         bulk_g2s(dst, r + TcRegion::A1, 32768, bar_load + b);
         bulk_g2s(dst + kBufA2, r + TcRegion::A2, 16384, bar_load + b);
-        bulk_g2s(dst + kBufU, r + TcRegion::U + (size_t)jt * C * kTN * 4, C * kTN * 4, bar_load + b);
-        bulk_g2s(dst + kBufOu, r + TcRegion::Ou + (size_t)jt * C * kTN * 4, C * kTN * 4, bar_load + b);
+        bulk_g2s(dst + kBufU, r + TcRegion::U + (size_t)jt * kTN * C * 4, kTN * C * 4, bar_load + b);
+        bulk_g2s(dst + kBufOu, r + TcRegion::Ou + (size_t)jt * kTN * C * 4, kTN * C * 4, bar_load + b);
         bulk_g2s(dst + kBufGam, r + TcRegion::Gam, 512, bar_load + b);
     };
     if (tid == 0 && nchunks > 0) issue_load(0, 0);
@@ -529,41 +625,39 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         fence_after();
         if (!ok) break;
         {
-            float hi[16], lo[16], d[kTN];
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                tmem_ld16(tmem + lane_base + 16 * part, hi);
-                tmem_ld16(tmem + lane_base + kTN + 16 * part, lo);
-                tmem_wait_ld();
-#pragma unroll
-                for (int r = 0; r < 16; ++r) d[16 * part + r] = hi[r] + lo[r];
-            }
-            const int i = tid & 63;
-            if (tid < 64) {
+            float hi[16], lo[16];
+            tmem_ld16(tmem + lane_base + js, hi);
+            tmem_ld16(tmem + lane_base + kTN + js, lo);
+            tmem_wait_ld();
+            const int i = lr & 63;
+            if (lr < 64) {
                 const float *Us = reinterpret_cast<const float *>(buf + kBufU);
 #pragma unroll
-                for (int jg = 0; jg < kTN / 8; ++jg) {
+                for (int jg = 0; jg < 2; ++jg) {
                     float zh[8], zl[8];
 #pragma unroll
                     for (int r = 0; r < 8; ++r) {
-                        const int j = 8 * jg + r;
-                        const float z = Us[slab_idx(i, j)] - d[j];
+                        const int j = js + 8 * jg + r;
+                        const float z = Us[j * C + i] - (hi[8 * jg + r] + lo[8 * jg + r]);
                         zh[r] = __bfloat162float(__float2bfloat16_rn(z));
                         zl[r] = z - zh[r];
                     }
-                    *reinterpret_cast<uint4 *>(B2 + mnmaj(8 * jg, i, kB2Lbo, kB2Sbo)) = pack8(zh);
-                    *reinterpret_cast<uint4 *>(B2 + 4096 + mnmaj(8 * jg, i, kB2Lbo, kB2Sbo)) = pack8(zl);
+                    st16(B2 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zh);
+                    st16(B2 + 4096 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zl);
                 }
             } else {
                 const float *Os = reinterpret_cast<const float *>(buf + kBufOu);
                 const int clen = min(C, len - ch * C);
                 if (i < clen) {
-                    __nv_bfloat16 *dst = out + ((size_t)(bos + ch * C + i) * H + h) * D + j0;
+                    __nv_bfloat16 *dst = out + ((size_t)(bos + ch * C + i) * H + h) * D + j0 + js;
 #pragma unroll
-                    for (int jg = 0; jg < kTN / 8; ++jg) {
+                    for (int jg = 0; jg < 2; ++jg) {
                         float o8[8];
 #pragma unroll
-                        for (int r = 0; r < 8; ++r) o8[r] = Os[slab_idx(i, 8 * jg + r)] + d[8 * jg + r];
+                        for (int r = 0; r < 8; ++r) {
+                            const int j = js + 8 * jg + r;
+                            o8[r] = Os[j * C + i] + (hi[8 * jg + r] + lo[8 * jg + r]);
+                        }
                         *reinterpret_cast<uint4 *>(dst + 8 * jg) = pack8(o8);
                     }
                 }
@@ -592,13 +686,10 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         {
             const float gam = reinterpret_cast<const float *>(buf + kBufGam)[c];
             float d16[16];
+            tmem_ld16(tmem + lane_base + 2 * kTN + js, d16);
+            tmem_wait_ld();
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                tmem_ld16(tmem + lane_base + 2 * kTN + 16 * part, d16);
-                tmem_wait_ld();
-#pragma unroll
-                for (int r = 0; r < 16; ++r) S[16 * part + r] = gam * S[16 * part + r] + d16[r];
-            }
+            for (int r = 0; r < 16; ++r) S[r] = gam * S[r] + d16[r];
             put_state();
         }
         fence_async_smem();
@@ -607,13 +698,12 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     }
     if (!ok) {
         if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
-        // Bounded waits for the copies and MMAs that may still be in flight.
         mbar_wait(bar_load, 0);
         mbar_wait(bar_load + 1, 0);
         mbar_wait(bar_mma, mma_phase);
     } else if (final_state) {
 #pragma unroll
-        for (int j = 0; j < kTN; j += 4)
+        for (int j = 0; j < 16; j += 4)
             *reinterpret_cast<float4 *>(final_state + st_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     fence_before();
@@ -632,21 +722,38 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, cudaStream_t stream,
                               cudaEvent_t *events) {
-    cudaError_t err = cudaFuncSetAttribute(tc_intra_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           kP1Smem);
+    // Per device, once: the SM count (phase 1 runs one persistent CTA per SM)
+    // and the dynamic shared-memory opt-ins. Repeating this is idempotent.
+    static int sm_counts[64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(tc_state_pass, cudaFuncAttributeMaxDynamicSharedMemorySize, kP2Smem);
-    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (sm_counts[dev] == 0) {
+        int n = 0;
+        if ((err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return err;
+        if ((err = cudaFuncSetAttribute(tc_intra_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        P1::bytes)) != cudaSuccess)
+            return err;
+        if ((err = cudaFuncSetAttribute(tc_state_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kP2Smem)) != cudaSuccess)
+            return err;
+        sm_counts[dev] = n;
+    }
+    const int sm_count = sm_counts[dev];
     if ((err = mark(events, 1, stream)) != cudaSuccess) return err;
     if (slots > 0) {
-        tc_intra_chunk<<<head_slot_grid(H, slots), 128, kP1Smem, stream>>>(
+        const long long items = slots * H;
+        const unsigned grid = (unsigned)(items < sm_count ? items : sm_count);
+        tc_intra_chunk<<<grid, kP1Threads, P1::bytes, stream>>>(
             static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
             static_cast<const __nv_bfloat16 *>(v), g, beta, scale, table, slots, H, region, status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if ((err = mark(events, 2, stream)) != cudaSuccess) return err;
     if (num_seqs > 0) {
-        tc_state_pass<<<dim3(num_seqs, H, D / kTN), 128, kP2Smem, stream>>>(
+        tc_state_pass<<<dim3(num_seqs, H, D / kTN), kP2Threads, kP2Smem, stream>>>(
             region, seq_first_slot, cu_seqlens, T_fixed, init_state,
             static_cast<__nv_bfloat16 *>(out), final_state, H, status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
