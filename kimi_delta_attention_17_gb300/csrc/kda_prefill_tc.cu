@@ -87,15 +87,15 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int tmem = 224528;
     static constexpr int bytes = 224544;
     // Reused once the first MMA has consumed am / bm:
-    static constexpr int As = am;                // fp32 [64][65]: A
-    static constexpr int Ts = am + 16640;        // fp32 [64][65]: T
-    static constexpr int Hs = am + 33280;        // bf16 K-major [i][j]: H (LBO 1024, SBO 128)
+    static constexpr int As = am;                // fp32 [64][68]: A
+    static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
+    static constexpr int Hs = am + 34816;        // bf16 K-major [i][j]: H (LBO 1024, SBO 128)
     static constexpr int TBs = Hs + 8192;        // bf16 K-major [i][j]: T Diag(beta)
     static constexpr int Xs = TBs + 8192;        // fp32 [3][16][16] scratch of the solve
 };
 static_assert(P1::Xs + 3072 <= P1::lt, "solve scratch overlaps L^T");
 static_assert(P1::bytes <= 232448, "phase-1 shared memory exceeds 227 KiB");
-constexpr int kAS = 65;  // row stride (floats) of A and T
+constexpr int kAS = 68;  // row stride (floats) of A and T: 16-byte rows, 8 rows hit 8 bank groups
 
 // (I, J) of column version v = I (I + 1) / 2 + J.
 __host__ __device__ constexpr int ver_I(int v) { return v < 1 ? 0 : v < 3 ? 1 : v < 6 ? 2 : 3; }
@@ -137,8 +137,7 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         while (w < nitems && table[w / H].seq < 0) w += gridDim.x;
         return w;
     };
-    auto issue = [&](long long w) {
-        const ChunkEntry e = table[w / H];
+    auto issue = [&](long long w, const ChunkEntry e) {
         const int hh = (int)(w % H);
         const int tsel = tid >> 6, i = tid & 63;
         if (tid == 0) mbar_expect_tx(bar_ld, (uint32_t)e.len * (3u * 256u + 512u));
@@ -152,12 +151,17 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     };
 
     long long w = next_item(blockIdx.x);
-    if (w < nitems) issue(w);
+    if (w < nitems) issue(w, table[w / H]);
     uint32_t ld_phase = 0, mma_phase = 0;
     bool ok = true;
     while (w < nitems) {
         const ChunkEntry ce = table[w / H];
         const int h = (int)(w % H);
+        // The next item and its table entry, read now so that the prefetch
+        // below does not wait on global memory.
+        const long long wn = next_item(w + gridDim.x);
+        ChunkEntry en = ce;
+        if (wn < nitems) en = table[wn / H];
         const int len = ce.len;
         unsigned char *reg = ws + (size_t)w * TcRegion::bytes;  // w = slot * H + h
         ok = __syncthreads_and(mbar_wait(bar_ld, ld_phase));
@@ -264,10 +268,6 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         __syncthreads();
         fence_after();
 
-        // The staging rows are consumed: fetch the next item's while this one runs.
-        const long long wn = next_item(w + gridDim.x);
-        if (wn < nitems) issue(wn);
-
         // ================= A / H = gated K K^T and Q K^T (M=128, N=160, K=128)
         if (tid == 0) {
             const uint32_t id = idesc_bf16(128, 160, 1, 1);
@@ -277,6 +277,8 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                          desc(smem_u32(sm + P1::bm) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo), id, s > 0);
             commit(bar_mma);
         }
+        // The staging rows are consumed: fetch the next item's while this one runs.
+        if (wn < nitems) issue(wn, en);
         ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
         mma_phase ^= 1;
         fence_after();
@@ -302,9 +304,15 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 const int J = ver_J(vv);
                 if (!isH) {
 #pragma unroll
-                    for (int jj = 0; jj < 16; ++jj) {
-                        const int j = 16 * J + jj;
-                        As[i * kAS + j] = j < i ? -bi * x[jj] : 0.f;
+                    for (int f = 0; f < 4; ++f) {
+                        float a4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 16 * J + 4 * f + e;
+                            a4[e] = j < i ? -bi * x[4 * f + e] : 0.f;
+                        }
+                        *reinterpret_cast<float4 *>(As + i * kAS + 16 * J + 4 * f) =
+                            make_float4(a4[0], a4[1], a4[2], a4[3]);
                     }
                 } else {
 #pragma unroll
@@ -322,7 +330,9 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                     if (J <= Iblk) continue;
                     if (!isH) {
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) As[i * kAS + 16 * J + jj] = 0.f;
+                        for (int f = 0; f < 4; ++f)
+                            *reinterpret_cast<float4 *>(As + i * kAS + 16 * J + 4 * f) =
+                                make_float4(0.f, 0.f, 0.f, 0.f);
                     } else {
                         const uint4 z = make_uint4(0, 0, 0, 0);
                         *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J, 1024, 128)) = z;
@@ -340,43 +350,65 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
             float *Ts = reinterpret_cast<float *>(sm + P1::Ts);
             float *Xs = reinterpret_cast<float *>(sm + P1::Xs);
             if (tid < 64) {
-                const int I = tid >> 4, col = tid;
+                // Column `col` of T_II by column-oriented substitution: once x_r is
+                // final it is pushed into every later row, so the dependent chain
+                // is one FMA per row instead of a growing dot product.
+                const int I = tid >> 4, col = tid, cl = tid & 15;
                 float x[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const int ii = 16 * I + r;
-                    float acc = ii == col ? 1.f : 0.f;
+                for (int r = 0; r < 16; ++r) x[r] = r == cl ? 1.f : 0.f;
 #pragma unroll
-                    for (int rr = 0; rr < r; ++rr) acc += As[ii * kAS + 16 * I + rr] * x[rr];
-                    x[r] = ii < col ? 0.f : acc;
-                    Ts[ii * kAS + col] = x[r];
+                for (int r = 0; r < 15; ++r) {
+                    const float xr = r < cl ? 0.f : x[r];
+#pragma unroll
+                    for (int rr = r + 1; rr < 16; ++rr) x[rr] += As[(16 * I + rr) * kAS + 16 * I + r] * xr;
                 }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) Ts[(16 * I + r) * kAS + col] = r < cl ? 0.f : x[r];
             }
             __syncthreads();
+            // Off-diagonal blocks by levels L = I - J; each thread computes a
+            // 1 x 4 strip (row r, columns 4 cg .. 4 cg + 3) of X_IJ and then of
+            // T_IJ = T_II X_IJ, reading 16-byte runs of A, T and X.
 #pragma unroll
             for (int L = 1; L <= 3; ++L) {
                 const int npairs = 4 - L;
-                for (int o = tid; o < npairs * 256; o += kP1Threads) {
-                    const int p = o >> 8, r = (o >> 4) & 15, cc = o & 15;
-                    const int J = p, I = J + L;
-                    float acc = 0.f;
+                const int p = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
+                const int J = p, I = J + L;
+                if (tid < npairs * 64) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int K = 0; K < L; ++K)
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk)
-                            acc += As[(16 * I + r) * kAS + 16 * (J + K) + kk] *
-                                   Ts[(16 * (J + K) + kk) * kAS + 16 * J + cc];
-                    Xs[p * 256 + r * 16 + cc] = acc;
+                        for (int kk = 0; kk < 16; kk += 4) {
+                            const float4 a = *reinterpret_cast<const float4 *>(
+                                As + (16 * I + r) * kAS + 16 * (J + K) + kk);
+                            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 t = *reinterpret_cast<const float4 *>(
+                                    Ts + (16 * (J + K) + kk + e) * kAS + 16 * J + 4 * cg);
+                                acc.x += av[e] * t.x; acc.y += av[e] * t.y;
+                                acc.z += av[e] * t.z; acc.w += av[e] * t.w;
+                            }
+                        }
+                    *reinterpret_cast<float4 *>(Xs + p * 256 + r * 16 + 4 * cg) = acc;
                 }
                 __syncthreads();
-                for (int o = tid; o < npairs * 256; o += kP1Threads) {
-                    const int p = o >> 8, r = (o >> 4) & 15, cc = o & 15;
-                    const int J = p, I = J + L;
-                    float acc = 0.f;
+                if (tid < npairs * 64) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        acc += Ts[(16 * I + r) * kAS + 16 * I + kk] * Xs[p * 256 + kk * 16 + cc];
-                    Ts[(16 * I + r) * kAS + 16 * J + cc] = acc;
+                    for (int kk = 0; kk < 16; kk += 4) {
+                        const float4 a = *reinterpret_cast<const float4 *>(Ts + (16 * I + r) * kAS + 16 * I + kk);
+                        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 xv = *reinterpret_cast<const float4 *>(Xs + p * 256 + (kk + e) * 16 + 4 * cg);
+                            acc.x += av[e] * xv.x; acc.y += av[e] * xv.y;
+                            acc.z += av[e] * xv.z; acc.w += av[e] * xv.w;
+                        }
+                    }
+                    *reinterpret_cast<float4 *>(Ts + (16 * I + r) * kAS + 16 * J + 4 * cg) = acc;
                 }
                 __syncthreads();
             }
@@ -386,9 +418,14 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 const int jb = 16 * jq + 8 * hf;
                 float t8[8];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int j = jb + r;
-                    t8[r] = j <= i ? Ts[i * kAS + j] * beta_s[j] : 0.f;
+                for (int f = 0; f < 2; ++f) {
+                    const float4 t = *reinterpret_cast<const float4 *>(Ts + i * kAS + jb + 4 * f);
+                    const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = jb + 4 * f + e;
+                        t8[4 * f + e] = j <= i ? tv[e] * beta_s[j] : 0.f;
+                    }
                 }
                 st16(sm + P1::TBs + kmaj(i, jb, 1024, 128), t8);
             }

@@ -141,18 +141,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
-// Packs 8 floats as 8 bf16 (round to nearest even) into one 16-byte vector.
-__device__ __forceinline__ uint4 pack8(const float *x) {
-    uint4 r;
-    r.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[0])) |
-          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[1])) << 16);
-    r.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[2])) |
-          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[3])) << 16);
-    r.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[4])) |
-          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[5])) << 16);
-    r.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[6])) |
-          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x[7])) << 16);
+// Packs 8 floats as 8 bf16 (round to nearest even), two per instruction,
+// into one 16-byte vector (element 0 in the lowest half-word).
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
 }
 
 }  // namespace tc
