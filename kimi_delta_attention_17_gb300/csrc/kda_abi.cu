@@ -168,7 +168,7 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if (err != cudaSuccess) return KDA_ERR_CUDA;
     if (use_tc(dk, dtype))
         err = launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
-                                T_fixed, H, num_seqs, slots, table, seq_first_slot,
+                                T_fixed, (long long)B * T, H, num_seqs, slots, table, seq_first_slot,
                                 reinterpret_cast<unsigned char *>(region), status, stream, events);
     else
         err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out,

@@ -80,7 +80,7 @@ size_t tc_region_bytes();
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
                               const float *beta, float scale, const float *init_state,
                               const int32_t *cu_seqlens, void *out, float *final_state,
-                              int T_fixed, int H, int num_seqs, long long slots,
+                              int T_fixed, long long tokens, int H, int num_seqs, long long slots,
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, cudaStream_t stream,
                               cudaEvent_t *events);

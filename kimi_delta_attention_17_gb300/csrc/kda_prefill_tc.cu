@@ -39,6 +39,8 @@
 // thread per key channel writes 16-byte runs along the token axis (MN-major
 // tiles when the contraction runs over channels, K-major when it runs over
 // tokens). Accumulators are read back with tcgen05.ld (thread t = TMEM lane t).
+#include <cuda.h>  // CUtensorMap (the encoder is fetched at run time; no libcuda link)
+
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -53,13 +55,20 @@ constexpr int kTN = 32;  // state columns per phase-2 CTA
 
 // Workspace region of one (chunk slot, head), byte offsets.
 struct TcRegion {
-    static constexpr size_t A1 = 0;        // [W; Q'] bf16, MN-major, 128 tokens x 128 ch
+    static constexpr size_t A1 = 0;        // [s Qbar; W] bf16, MN-major, 128 tokens x 128 ch
     static constexpr size_t A2 = 32768;    // Kbar^T bf16, K-major, 128 ch x 64 tokens
-    static constexpr size_t U = 49152;     // fp32 [128 columns][64 tokens] (transposed)
-    static constexpr size_t Ou = 81920;    // same layout as U
-    static constexpr size_t Gam = 114688;  // fp32 [128] exp(G_n)
-    static constexpr size_t bytes = 115200;
+    static constexpr size_t Hm = 49152;    // H bf16, K-major [token i][token j] (LBO 1024, SBO 128)
+    static constexpr size_t U = 57344;     // fp32 [4 slabs][64 tokens][32 columns], rows swizzled
+    static constexpr size_t Gam = 90112;   // fp32 [128] exp(G_n)
+    static constexpr size_t bytes = 90624;
 };
+// Element (token i, column j of a 32-column slab) of a U slab: the float4
+// groups of a row are XOR-swizzled by (i & 7), so the phase-2 thread that owns
+// row i reads it without bank conflicts, while phase 1 (one thread per column)
+// still writes each row with one coalesced 128-byte store per warp.
+__host__ __device__ constexpr int slab_idx(int i, int j) {
+    return i * 32 + ((((j >> 2) ^ (i & 7))) << 2) + (j & 3);
+}
 // Descriptor strides of the workspace tiles (and of their shared-memory copies).
 constexpr uint32_t kA1Lbo = 128, kA1Sbo = 2048;  // MN-major: channel cores adjacent
 constexpr uint32_t kA2Lbo = 2048, kA2Sbo = 128;  // K-major: channel groups adjacent
@@ -77,20 +86,18 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int q = 0, k = 16384, v = 32768, g = 49152;  // staging rows of one chunk
     static constexpr int am = 81920;    // [Ktilde; s Qtilde] bf16, MN-major 128 x 128
     static constexpr int bm = 114688;   // column versions bf16, MN-major 160 x 128
-    static constexpr int lt = 155648;   // L^T (later W^T) bf16, K-major [channel][token]
-    static constexpr int vt = 172032;   // V^T (later U^T)
-    static constexpr int qb = 188416;   // s Qbar fp32 [channel][token], 16-byte chunks swizzled
-    static constexpr int beta = 221184; // 64 floats
-    static constexpr int refs = 221440; // fp32 [5][128]: G at tokens 7, 23, 39, 55, 63
-    static constexpr int tot = 224000;  // fp32 [128]: G at token 31
-    static constexpr int bar = 224512;  // mbarriers: staging loaded, MMA done
-    static constexpr int tmem = 224528;
-    static constexpr int bytes = 224544;
+    static constexpr int lt = 155648;   // L^T bf16, K-major [channel][token]
+    static constexpr int vt = 172032;   // V^T bf16, K-major [channel][token]
+    static constexpr int beta = 188416; // 64 floats
+    static constexpr int refs = 188672; // fp32 [5][128]: G at tokens 7, 23, 39, 55, 63
+    static constexpr int tot = 191232;  // fp32 [128]: G at token 31
+    static constexpr int bar = 191744;  // mbarriers: staging loaded, MMA done
+    static constexpr int tmem = 191760;
+    static constexpr int bytes = 191776;
     // Reused once the first MMA has consumed am / bm:
     static constexpr int As = am;                // fp32 [64][68]: A
     static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
-    static constexpr int Hs = am + 34816;        // bf16 K-major [i][j]: H (LBO 1024, SBO 128)
-    static constexpr int TBs = Hs + 8192;        // bf16 K-major [i][j]: T Diag(beta)
+    static constexpr int TBs = am + 34816;       // bf16 K-major [i][j]: T Diag(beta)
     static constexpr int Xs = TBs + 8192;        // fp32 [3][16][16] scratch of the solve
 };
 static_assert(P1::Xs + 3072 <= P1::lt, "solve scratch overlaps L^T");
@@ -106,8 +113,8 @@ __device__ __forceinline__ void st16(unsigned char *p, const float *x) {
 }
 
 __global__ void __launch_bounds__(kP1Threads, 1)
-tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-               const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
+tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                const float *__restrict__ beta, float scale, const ChunkEntry *__restrict__ table,
                long long nslots, int H, unsigned char *__restrict__ ws, int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -137,17 +144,17 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         while (w < nitems && table[w / H].seq < 0) w += gridDim.x;
         return w;
     };
+    // One thread fetches an item: four 3-D TMA tiles (128 channels x 1 head x
+    // 64 tokens) land as dense [token][channel] rows. Tokens past the end of
+    // the tensor read as zeros; tokens of the next sequence are masked by len.
     auto issue = [&](long long w, const ChunkEntry e) {
+        if (tid != 0) return;
         const int hh = (int)(w % H);
-        const int tsel = tid >> 6, i = tid & 63;
-        if (tid == 0) mbar_expect_tx(bar_ld, (uint32_t)e.len * (3u * 256u + 512u));
-        if (i < e.len) {
-            const size_t row = ((size_t)(e.bos + i) * H + hh) * D;
-            if (tsel == 0) bulk_g2s(sm + P1::q + i * 256, q + row, 256, bar_ld);
-            else if (tsel == 1) bulk_g2s(sm + P1::k + i * 256, k + row, 256, bar_ld);
-            else if (tsel == 2) bulk_g2s(sm + P1::v + i * 256, v + row, 256, bar_ld);
-            else bulk_g2s(sm + P1::g + i * 512, g + row, 512, bar_ld);
-        }
+        mbar_expect_tx(bar_ld, 64u * (3u * 256u + 512u));
+        tma_load_3d(sm + P1::q, &tm_q, 0, hh, e.bos, bar_ld);
+        tma_load_3d(sm + P1::k, &tm_k, 0, hh, e.bos, bar_ld);
+        tma_load_3d(sm + P1::v, &tm_v, 0, hh, e.bos, bar_ld);
+        tma_load_3d(sm + P1::g, &tm_g, 0, hh, e.bos, bar_ld);
     };
 
     long long w = next_item(blockIdx.x);
@@ -157,16 +164,16 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
     while (w < nitems) {
         const ChunkEntry ce = table[w / H];
         const int h = (int)(w % H);
-        // The next item and its table entry, read now so that the prefetch
-        // below does not wait on global memory.
-        const long long wn = next_item(w + gridDim.x);
-        ChunkEntry en = ce;
-        if (wn < nitems) en = table[wn / H];
         const int len = ce.len;
         unsigned char *reg = ws + (size_t)w * TcRegion::bytes;  // w = slot * H + h
         ok = __syncthreads_and(mbar_wait(bar_ld, ld_phase));
         ld_phase ^= 1;
         if (!ok) break;
+        // The next item and its table entry, read now so that the prefetch
+        // below does not wait on global memory.
+        const long long wn = next_item(w + gridDim.x);
+        ChunkEntry en = ce;
+        if (wn < nitems) en = table[wn / H];
 
         // ================= elementwise pass (thread = channel c, 32 tokens)
         {
@@ -210,7 +217,6 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
 #pragma unroll
                 for (int J = 0; J < 4; ++J) X[I][J] = J < I ? __expf(Rf[I] - Rf[J]) : 1.f;
             }
-            float *qbar = reinterpret_cast<float *>(sm + P1::qb) + c * C;
 #pragma unroll
             for (int ig = 0; ig < 4; ++ig) {
                 const int jj = ig >> 1;               // block within this half
@@ -253,13 +259,10 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
                 for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r] * Ps;
                 st16(sm + P1::lt + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
                 st16(sm + P1::vt + kmaj(c, i0, kA2Lbo, kA2Sbo), vv);
+                // s Qbar, rows 0-63 of the state-pass operand [s Qbar; W].
 #pragma unroll
-                for (int h4 = 0; h4 < 2; ++h4) {
-                    const int chunk = (i0 >> 2) + h4;  // 4-token fp32 chunk of row c
-                    *reinterpret_cast<float4 *>(qbar + ((chunk ^ (c & 7)) << 2)) =
-                        make_float4(qv[4 * h4] * E[4 * h4] * Ps, qv[4 * h4 + 1] * E[4 * h4 + 1] * Ps,
-                                    qv[4 * h4 + 2] * E[4 * h4 + 2] * Ps, qv[4 * h4 + 3] * E[4 * h4 + 3] * Ps);
-                }
+                for (int r = 0; r < 8; ++r) t8[r] = qv[r] * E[r] * Ps;
+                st16(reg + TcRegion::A1 + mnmaj(i0, c, kA1Lbo, kA1Sbo), t8);
             }
             if (half == 1) reinterpret_cast<float *>(reg + TcRegion::Gam)[c] = __expf(Gend);
         }
@@ -285,7 +288,7 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         if (!ok) break;
         {
             float *As = reinterpret_cast<float *>(sm + P1::As);
-            unsigned char *Hs = sm + P1::Hs;
+            unsigned char *Hs = reg + TcRegion::Hm;  // H goes straight to the workspace
             const int lr = tid & 127, i = lr & 63, Iblk = i >> 4;
             const bool isH = lr >= 64;
             const int side = warp >> 2;
@@ -451,79 +454,20 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
         fence_after();
         if (!ok) break;
         {
+            // W -> rows 64-127 of [s Qbar; W] (side 0); U -> its slab (side 1).
             const int side = tid >> 7;
-            float *slab = reinterpret_cast<float *>(reg + TcRegion::U) + (size_t)c * C;  // [c][i]
+            float *slab = reinterpret_cast<float *>(reg + TcRegion::U) + (size_t)(c >> 5) * (C * 32);
 #pragma unroll
             for (int part = 0; part < 4; ++part) {
                 float x[16];
                 tmem_ld16(tmem + lane_base + 64 * side + 16 * part, x);
                 tmem_wait_ld();
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int i0 = 16 * part + 8 * hf;
-                    if (side == 0) {
-                        const uint4 wp = pack8(x + 8 * hf);
-                        *reinterpret_cast<uint4 *>(reg + TcRegion::A1 + mnmaj(i0, c, kA1Lbo, kA1Sbo)) = wp;
-                        *reinterpret_cast<uint4 *>(sm + P1::lt + kmaj(c, i0, kA2Lbo, kA2Sbo)) = wp;
-                    } else {
-                        st16(sm + P1::vt + kmaj(c, i0, kA2Lbo, kA2Sbo), x + 8 * hf);
-                    }
-                }
-                if (side == 1) {
-#pragma unroll
-                    for (int f = 0; f < 4; ++f)
-                        *reinterpret_cast<float4 *>(slab + 16 * part + 4 * f) =
-                            make_float4(x[4 * f], x[4 * f + 1], x[4 * f + 2], x[4 * f + 3]);
-                }
-            }
-        }
-        fence_async_smem();
-        fence_before();
-        __syncthreads();
-        fence_after();
-
-        // ================= H W and H U
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-            for (int s = 0; s < C / 16; ++s) {
-                const uint64_t b = desc(smem_u32(sm + P1::Hs) + s * 2 * 1024, 1024, 128);
-                mma_bf16(tmem + 128, desc(smem_u32(sm + P1::lt) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
-                mma_bf16(tmem + 192, desc(smem_u32(sm + P1::vt) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
-            }
-            commit(bar_mma);
-        }
-        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
-        mma_phase ^= 1;
-        fence_after();
-        if (!ok) break;
-        {
-            const int side = tid >> 7;
-            const float *qbar = reinterpret_cast<const float *>(sm + P1::qb) + c * C;
-            float *slab = reinterpret_cast<float *>(reg + TcRegion::Ou) + (size_t)c * C;  // [c][i]
-#pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                float x[16];
-                tmem_ld16(tmem + lane_base + 128 + 64 * side + 16 * part, x);
-                tmem_wait_ld();
                 if (side == 0) {
-                    float t16[16];
-#pragma unroll
-                    for (int f = 0; f < 4; ++f) {
-                        const int chunk = 4 * part + f;
-                        const float4 qb = *reinterpret_cast<const float4 *>(qbar + ((chunk ^ (c & 7)) << 2));
-                        t16[4 * f] = qb.x - x[4 * f];
-                        t16[4 * f + 1] = qb.y - x[4 * f + 1];
-                        t16[4 * f + 2] = qb.z - x[4 * f + 2];
-                        t16[4 * f + 3] = qb.w - x[4 * f + 3];
-                    }
-                    st16(reg + TcRegion::A1 + mnmaj(64 + 16 * part, c, kA1Lbo, kA1Sbo), t16);
-                    st16(reg + TcRegion::A1 + mnmaj(64 + 16 * part + 8, c, kA1Lbo, kA1Sbo), t16 + 8);
+                    st16(reg + TcRegion::A1 + mnmaj(64 + 16 * part, c, kA1Lbo, kA1Sbo), x);
+                    st16(reg + TcRegion::A1 + mnmaj(64 + 16 * part + 8, c, kA1Lbo, kA1Sbo), x + 8);
                 } else {
 #pragma unroll
-                    for (int f = 0; f < 4; ++f)
-                        *reinterpret_cast<float4 *>(slab + 16 * part + 4 * f) =
-                            make_float4(x[4 * f], x[4 * f + 1], x[4 * f + 2], x[4 * f + 3]);
+                    for (int r = 0; r < 16; ++r) slab[slab_idx(16 * part + r, c & 31)] = x[r];
                 }
             }
         }
@@ -546,11 +490,16 @@ tc_intra_chunk(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restr
 // ---------------------------------------------------------------- phase 2
 // One CTA of 256 threads per (sequence, head, 32-column slab). Thread t owns
 // TMEM lane / state row t mod 128 and slab columns [16 s, 16 s + 16) with
-// s = t / 128. U and Ou arrive transposed ([column][token]) so that the thread
-// of token row i reads them without bank conflicts.
+// s = t / 128. Per chunk, with S the state entering it:
+//   round trip 1:  D1 = [s Qbar; W] S          (rows 0-63: Qbar S, 64-127: W S)
+//                  Z  = U - W S                 (lanes 64-127)
+//   round trip 2:  D2 = Kbar^T Z,  D1[0:64] += H Z
+//                  S <- Diag(exp G_n) S + D2,  O = D1[0:64] = s Qbar S + H Z
+// ("Understanding Kimi Delta Attention", "The token outputs" and "One state
+// crosses the chunk boundary"). S and Z enter the MMAs as bf16 hi + lo pairs.
 constexpr int kP2Threads = 256;
-constexpr int kBufBytes = 66560;  // one chunk's A1, A2, U slab, Ou slab, gamma (65 KiB)
-constexpr int kBufA2 = 32768, kBufU = 49152, kBufOu = 57344, kBufGam = 65536;
+constexpr int kBufBytes = 66560;  // one chunk's A1, A2, H, U slab, gamma (65 KiB)
+constexpr int kBufA2 = 32768, kBufH = 49152, kBufU = 57344, kBufGam = 65536;
 constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 512;
 constexpr int kP2B1 = 2 * kBufBytes;            // S (hi | lo) bf16, MN-major [K = ch][N = 64]
 constexpr int kP2B2 = kP2B1 + 16384;            // Z hi, Z lo bf16, MN-major [K = token][N = 32]
@@ -633,8 +582,8 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         mbar_expect_tx(bar_load + b, kLoadBytes);
         bulk_g2s(dst, r + TcRegion::A1, 32768, bar_load + b);
         bulk_g2s(dst + kBufA2, r + TcRegion::A2, 16384, bar_load + b);
+        bulk_g2s(dst + kBufH, r + TcRegion::Hm, 8192, bar_load + b);
         bulk_g2s(dst + kBufU, r + TcRegion::U + (size_t)jt * kTN * C * 4, kTN * C * 4, bar_load + b);
-        bulk_g2s(dst + kBufOu, r + TcRegion::Ou + (size_t)jt * kTN * C * 4, kTN * C * 4, bar_load + b);
         bulk_g2s(dst + kBufGam, r + TcRegion::Gam, 512, bar_load + b);
     };
     if (tid == 0 && nchunks > 0) issue_load(0, 0);
@@ -661,43 +610,31 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         mma_phase ^= 1;
         fence_after();
         if (!ok) break;
-        {
+        if (lr >= 64) {
+            // Z = U - W S for token row i, slab columns js .. js + 15.
             float hi[16], lo[16];
             tmem_ld16(tmem + lane_base + js, hi);
             tmem_ld16(tmem + lane_base + kTN + js, lo);
             tmem_wait_ld();
-            const int i = lr & 63;
-            if (lr < 64) {
-                const float *Us = reinterpret_cast<const float *>(buf + kBufU);
+            const int i = lr - 64;
+            const float *Us = reinterpret_cast<const float *>(buf + kBufU);
 #pragma unroll
-                for (int jg = 0; jg < 2; ++jg) {
-                    float zh[8], zl[8];
+            for (int jg = 0; jg < 2; ++jg) {
+                float zh[8], zl[8];
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const int j = js + 8 * jg + r;
-                        const float z = Us[j * C + i] - (hi[8 * jg + r] + lo[8 * jg + r]);
+                for (int r4 = 0; r4 < 2; ++r4) {
+                    const float4 u = *reinterpret_cast<const float4 *>(Us + slab_idx(i, js + 8 * jg + 4 * r4));
+                    const float uv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 4 * r4 + e;
+                        const float z = uv[e] - (hi[8 * jg + r] + lo[8 * jg + r]);
                         zh[r] = __bfloat162float(__float2bfloat16_rn(z));
                         zl[r] = z - zh[r];
                     }
-                    st16(B2 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zh);
-                    st16(B2 + 4096 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zl);
                 }
-            } else {
-                const float *Os = reinterpret_cast<const float *>(buf + kBufOu);
-                const int clen = min(C, len - ch * C);
-                if (i < clen) {
-                    __nv_bfloat16 *dst = out + ((size_t)(bos + ch * C + i) * H + h) * D + j0 + js;
-#pragma unroll
-                    for (int jg = 0; jg < 2; ++jg) {
-                        float o8[8];
-#pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            const int j = js + 8 * jg + r;
-                            o8[r] = Os[j * C + i] + (hi[8 * jg + r] + lo[8 * jg + r]);
-                        }
-                        *reinterpret_cast<uint4 *>(dst + 8 * jg) = pack8(o8);
-                    }
-                }
+                st16(B2 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zh);
+                st16(B2 + 4096 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zl);
             }
         }
         fence_async_smem();
@@ -705,15 +642,19 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         __syncthreads();
         if (tid == 0) {
             fence_after();
+            // D2 = Kbar^T (Z_hi + Z_lo); D1 rows 0-63 += H Z (rows 64-127 receive
+            // products of whatever follows H in shared memory: W S is consumed).
             const uint32_t id = idesc_bf16(128, kTN, 0, 1);
 #pragma unroll
             for (int part = 0; part < 2; ++part)
 #pragma unroll
-                for (int s = 0; s < C / 16; ++s)
-                    mma_bf16(tmem + 2 * kTN,
-                             desc(smem_u32(buf + kBufA2) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo),
-                             desc(smem_u32(B2 + part * 4096) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id,
-                             part > 0 || s > 0);
+                for (int s = 0; s < C / 16; ++s) {
+                    const uint64_t bz = desc(smem_u32(B2 + part * 4096) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo);
+                    mma_bf16(tmem + 2 * kTN, desc(smem_u32(buf + kBufA2) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo),
+                             bz, id, part > 0 || s > 0);
+                    mma_bf16(tmem + part * kTN, desc(smem_u32(buf + kBufH) + s * 2 * 1024, 1024, 128), bz,
+                             id, 1);
+                }
             commit(bar_mma);
         }
         ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
@@ -728,6 +669,24 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
 #pragma unroll
             for (int r = 0; r < 16; ++r) S[r] = gam * S[r] + d16[r];
             put_state();
+        }
+        if (lr < 64) {
+            // O = s Qbar S + H Z for token row i, slab columns js .. js + 15.
+            const int i = lr, clen = min(C, len - ch * C);
+            float hi[16], lo[16];
+            tmem_ld16(tmem + lane_base + js, hi);
+            tmem_ld16(tmem + lane_base + kTN + js, lo);
+            tmem_wait_ld();
+            if (i < clen) {
+                __nv_bfloat16 *dst = out + ((size_t)(bos + ch * C + i) * H + h) * D + j0 + js;
+#pragma unroll
+                for (int jg = 0; jg < 2; ++jg) {
+                    float o8[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) o8[r] = hi[8 * jg + r] + lo[8 * jg + r];
+                    *reinterpret_cast<uint4 *>(dst + 8 * jg) = pack8(o8);
+                }
+            }
         }
         fence_async_smem();
         fence_before();
@@ -752,10 +711,50 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
 
 size_t tc_region_bytes() { return TcRegion::bytes; }
 
+namespace {
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time so that the
+// library does not link libcuda.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// A [tokens][H][128] tensor seen as 3-D (channel, head, token) with boxes of
+// 128 channels x 1 head x 64 tokens; out-of-range tokens read as zeros.
+cudaError_t token_rows_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int esize, int H,
+                           long long tokens) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize};
+    const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)C};
+    const cuuint32_t unit[3] = {1u, 1u, 1u};
+    const CUresult r = enc(m, dt, 3, const_cast<void *>(base), dims, strides, box, unit,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
                               const float *beta, float scale, const float *init_state,
                               const int32_t *cu_seqlens, void *out, float *final_state,
-                              int T_fixed, int H, int num_seqs, long long slots,
+                              int T_fixed, long long tokens, int H, int num_seqs, long long slots,
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, cudaStream_t stream,
                               cudaEvent_t *events) {
@@ -780,12 +779,17 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     }
     const int sm_count = sm_counts[dev];
     if ((err = mark(events, 1, stream)) != cudaSuccess) return err;
-    if (slots > 0) {
+    if (slots > 0 && tokens > 0) {
+        CUtensorMap tq, tk, tv, tg;
+        if ((err = token_rows_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
+            (err = token_rows_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
+            (err = token_rows_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
+            (err = token_rows_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tokens)) != cudaSuccess)
+            return err;
         const long long items = slots * H;
         const unsigned grid = (unsigned)(items < sm_count ? items : sm_count);
-        tc_intra_chunk<<<grid, kP1Threads, P1::bytes, stream>>>(
-            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-            static_cast<const __nv_bfloat16 *>(v), g, beta, scale, table, slots, H, region, status);
+        tc_intra_chunk<<<grid, kP1Threads, P1::bytes, stream>>>(tq, tk, tv, tg, beta, scale, table,
+                                                                 slots, H, region, status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if ((err = mark(events, 2, stream)) != cudaSuccess) return err;

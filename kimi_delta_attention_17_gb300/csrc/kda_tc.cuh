@@ -141,6 +141,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 3-D tiled TMA load of one box of `map` at element coordinates (x, y, z)
+// into shared memory, completing its bytes on mbar. `map` is the address of a
+// __grid_constant__ CUtensorMap kernel parameter.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *map, int x, int y, int z,
+                                            uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(mbar))
+        : "memory");
+}
+
 // Packs 8 floats as 8 bf16 (round to nearest even), two per instruction,
 // into one 16-byte vector (element 0 in the lowest half-word).
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
