@@ -89,11 +89,9 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int lt = 155648;   // L^T bf16, K-major [channel][token]
     static constexpr int vt = 172032;   // V^T bf16, K-major [channel][token]
     static constexpr int beta = 188416; // 64 floats
-    static constexpr int refs = 188672; // fp32 [5][128]: G at tokens 7, 23, 39, 55, 63
-    static constexpr int tot = 191232;  // fp32 [128]: G at token 31
-    static constexpr int bar = 191744;  // mbarriers: staging loaded, MMA done
-    static constexpr int tmem = 191760;
-    static constexpr int bytes = 191776;
+    static constexpr int bar = 188672;  // mbarriers: staging loaded, MMA done
+    static constexpr int tmem = 188688;
+    static constexpr int bytes = 188704;
     // Reused once the first MMA has consumed am / bm:
     static constexpr int As = am;                // fp32 [64][68]: A
     static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
@@ -124,8 +122,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint64_t *bar_mma = bar_ld + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P1::tmem);
     float *beta_s = reinterpret_cast<float *>(sm + P1::beta);
-    float *refs = reinterpret_cast<float *>(sm + P1::refs);
-    float *tot = reinterpret_cast<float *>(sm + P1::tot);
     const long long nitems = nslots * H;
 
     if (warp == 0) tmem_alloc<256>(tslot);
@@ -181,32 +177,46 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::q);
             const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::k);
             const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::v);
+            // Cumulative log-decay of channel c. Each thread sums all 64 tokens
+            // (no exchange between the two halves) but keeps only the prefixes of
+            // its own 32; the block references r(I) = 7, 23, 39, 55 and the chunk
+            // end come out of the same pass.
             float G[32];
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const int i = 32 * half + r;
-                G[r] = i < len ? gs[i * D + c] : 0.f;
-            }
-#pragma unroll
-            for (int r = 1; r < 32; ++r) G[r] += G[r - 1];
+            float R0, R1, R2, R3, Gend;
             if (half == 0) {
-                tot[c] = G[31];
-                refs[c] = G[7];
-                refs[128 + c] = G[23];
+                float acc = 0.f;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    acc += r < len ? gs[r * D + c] : 0.f;
+                    G[r] = acc;
+                }
+                R0 = G[7];
+                R1 = G[23];
+#pragma unroll
+                for (int r = 32; r < 64; ++r) {
+                    acc += r < len ? gs[r * D + c] : 0.f;
+                    if (r == 39) R2 = acc;
+                    if (r == 55) R3 = acc;
+                }
+                Gend = acc;
+            } else {
+                float acc = 0.f;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    acc += r < len ? gs[r * D + c] : 0.f;
+                    if (r == 7) R0 = acc;
+                    if (r == 23) R1 = acc;
+                }
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    acc += 32 + r < len ? gs[(32 + r) * D + c] : 0.f;
+                    G[r] = acc;
+                }
+                R2 = G[7];
+                R3 = G[23];
+                Gend = G[31];
             }
             if (tid < C) beta_s[tid] = tid < len ? beta[(size_t)(ce.bos + tid) * H + h] : 0.f;
-            __syncthreads();
-            if (half == 1) {
-                const float o = tot[c];
-#pragma unroll
-                for (int r = 0; r < 32; ++r) G[r] += o;
-                refs[256 + c] = G[7];
-                refs[384 + c] = G[23];
-                refs[512 + c] = G[31];
-            }
-            __syncthreads();
-            const float R0 = refs[c], R1 = refs[128 + c], R2 = refs[256 + c], R3 = refs[384 + c];
-            const float Gend = refs[512 + c];
             // Per-channel block constants (see the header comment).
             const float Rf[4] = {R0, R1, R2, R3};
             float P[4], Y[4], X[4][4];
@@ -500,14 +510,22 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 constexpr int kP2Threads = 256;
 constexpr int kBufBytes = 66560;  // one chunk's A1, A2, H, U slab, gamma (65 KiB)
 constexpr int kBufA2 = 32768, kBufH = 49152, kBufU = 57344, kBufGam = 65536;
-constexpr uint32_t kLoadBytes = 32768 + 16384 + 8192 + 8192 + 512;
+// Each buffer fills in two parts: A = [s Qbar; W], U slab, gamma (free once the
+// chunk two back has finished its first product and state update); B =
+// Kbar^T, H (free only once that chunk's H Z product has completed).
+constexpr uint32_t kLoadBytesA = 32768 + 8192 + 512;
+constexpr uint32_t kLoadBytesB = 16384 + 8192;
 constexpr int kP2B1 = 2 * kBufBytes;            // S (hi | lo) bf16, MN-major [K = ch][N = 64]
-constexpr int kP2B2 = kP2B1 + 16384;            // Z hi, Z lo bf16, MN-major [K = token][N = 32]
-constexpr int kP2Bar = kP2B2 + 8192;            // 3 mbarriers
-constexpr int kP2Tmem = kP2Bar + 24;
+constexpr int kP2B2 = kP2B1 + 16384;            // [Z_hi | Z_lo] bf16, MN-major [K = token][N = 64]
+constexpr int kP2Bar = kP2B2 + 8192;            // 5 mbarriers: load A[2], load B[2], MMA
+constexpr int kP2Tmem = kP2Bar + 40;
 constexpr int kP2Smem = kP2Tmem + 8;
 constexpr uint32_t kB1Lbo = 128, kB1Sbo = 2048;
 constexpr uint32_t kB2Lbo = 128, kB2Sbo = 1024;
+// TMEM columns: D1 alternates between [0, 64) and [64, 128) from chunk to
+// chunk (the token outputs of chunk n are read while chunk n + 1's first
+// product runs); D2 = Kbar^T Z at [128, 192).
+constexpr int kD2Col = 128;
 
 __global__ void __launch_bounds__(kP2Threads, 1)
 tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
@@ -529,8 +547,9 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     const int slot0 = seq_first_slot[n];
     unsigned char *B1 = sm + kP2B1;
     unsigned char *B2 = sm + kP2B2;
-    uint64_t *bar_load = reinterpret_cast<uint64_t *>(sm + kP2Bar);  // [2]
-    uint64_t *bar_mma = bar_load + 2;
+    uint64_t *bar_la = reinterpret_cast<uint64_t *>(sm + kP2Bar);  // [2]
+    uint64_t *bar_lb = bar_la + 2;                                  // [2]
+    uint64_t *bar_mma = bar_la + 4;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kP2Tmem);
 
     const int c = lr;  // state row
@@ -562,10 +581,12 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     };
     put_state();
 
-    if (warp == 0) tmem_alloc<128>(tslot);
+    if (warp == 0) tmem_alloc<256>(tslot);
     if (tid == 0) {
-        mbar_init(bar_load, 1);
-        mbar_init(bar_load + 1, 1);
+        mbar_init(bar_la, 1);
+        mbar_init(bar_la + 1, 1);
+        mbar_init(bar_lb, 1);
+        mbar_init(bar_lb + 1, 1);
         mbar_init(bar_mma, 1);
         mbar_fence_init();
     }
@@ -576,45 +597,78 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     const uint32_t tmem = *tslot;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    auto issue_load = [&](int ch, int b) {
-        const unsigned char *r = ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes;
+    auto region_of = [&](int ch) { return ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes; };
+    auto issue_a = [&](int ch, int b) {
+        const unsigned char *r = region_of(ch);
         unsigned char *dst = sm + b * kBufBytes;
-        mbar_expect_tx(bar_load + b, kLoadBytes);
-        bulk_g2s(dst, r + TcRegion::A1, 32768, bar_load + b);
-        bulk_g2s(dst + kBufA2, r + TcRegion::A2, 16384, bar_load + b);
-        bulk_g2s(dst + kBufH, r + TcRegion::Hm, 8192, bar_load + b);
-        bulk_g2s(dst + kBufU, r + TcRegion::U + (size_t)jt * kTN * C * 4, kTN * C * 4, bar_load + b);
-        bulk_g2s(dst + kBufGam, r + TcRegion::Gam, 512, bar_load + b);
+        mbar_expect_tx(bar_la + b, kLoadBytesA);
+        bulk_g2s(dst, r + TcRegion::A1, 32768, bar_la + b);
+        bulk_g2s(dst + kBufU, r + TcRegion::U + (size_t)jt * kTN * C * 4, kTN * C * 4, bar_la + b);
+        bulk_g2s(dst + kBufGam, r + TcRegion::Gam, 512, bar_la + b);
     };
-    if (tid == 0 && nchunks > 0) issue_load(0, 0);
+    auto issue_b = [&](int ch, int b) {
+        const unsigned char *r = region_of(ch);
+        unsigned char *dst = sm + b * kBufBytes;
+        mbar_expect_tx(bar_lb + b, kLoadBytesB);
+        bulk_g2s(dst + kBufA2, r + TcRegion::A2, 16384, bar_lb + b);
+        bulk_g2s(dst + kBufH, r + TcRegion::Hm, 8192, bar_lb + b);
+    };
+    if (tid == 0 && nchunks > 0) {
+        issue_a(0, 0);
+        issue_b(0, 0);
+    }
 
     uint32_t mma_phase = 0;
     bool ok = true;
+    // Token outputs of chunk `ch` (rows 0-63 of its D1): s Qbar S + H Z.
+    auto put_outputs = [&](int ch) {
+        const int i = lr, clen = min(C, len - ch * C);
+        const uint32_t d1 = tmem + lane_base + 64 * (ch & 1);
+        float hi[16], lo[16];
+        tmem_ld16(d1 + js, hi);
+        tmem_ld16(d1 + kTN + js, lo);
+        tmem_wait_ld();
+        if (i < clen) {
+            __nv_bfloat16 *dst = out + ((size_t)(bos + ch * C + i) * H + h) * D + j0 + js;
+#pragma unroll
+            for (int jg = 0; jg < 2; ++jg) {
+                float o8[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) o8[r] = hi[8 * jg + r] + lo[8 * jg + r];
+                *reinterpret_cast<uint4 *>(dst + 8 * jg) = pack8(o8);
+            }
+        }
+    };
     for (int ch = 0; ch < nchunks; ++ch) {
         const int b = ch & 1;
         unsigned char *buf = sm + b * kBufBytes;
-        if (tid == 0 && ch + 1 < nchunks) issue_load(ch + 1, b ^ 1);
-        ok = __syncthreads_and(mbar_wait(bar_load + b, (ch >> 1) & 1));
-        if (!ok) break;
-        // [W S; Q' S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
+        const uint32_t d1 = tmem + 64 * b;
+        const uint32_t lp = (ch >> 1) & 1;  // load parity of this buffer
+        if (tid == 0 && ch + 1 < nchunks) issue_a(ch + 1, b ^ 1);
+        // Each thread waits for this chunk's tiles itself (no CTA barrier).
+        bool mine = mbar_wait(bar_la + b, lp);
+        // [s Qbar S; W S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
         if (tid == 0) {
             fence_after();
             const uint32_t id = idesc_bf16(128, 2 * kTN, 1, 1);
 #pragma unroll
             for (int s = 0; s < D / 16; ++s)
-                mma_bf16(tmem, desc(smem_u32(buf) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo),
+                mma_bf16(d1, desc(smem_u32(buf) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo),
                          desc(smem_u32(B1) + s * 2 * kB1Lbo, kB1Lbo, kB1Sbo), id, s > 0);
-            commit(bar_mma);
+            commit(bar_mma);  // also covers the previous chunk's H Z product
         }
-        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
+        mine = mine && mbar_wait(bar_mma, mma_phase);
         mma_phase ^= 1;
+        ok = __syncthreads_and(mine);
         fence_after();
         if (!ok) break;
+        // The previous chunk's H Z product has completed: its buffer's B part is free.
+        if (tid == 0 && ch + 1 < nchunks) issue_b(ch + 1, b ^ 1);
         if (lr >= 64) {
             // Z = U - W S for token row i, slab columns js .. js + 15.
             float hi[16], lo[16];
-            tmem_ld16(tmem + lane_base + js, hi);
-            tmem_ld16(tmem + lane_base + kTN + js, lo);
+            tmem_ld16(d1 + lane_base + js, hi);
+            tmem_ld16(d1 + lane_base + kTN + js, lo);
             tmem_wait_ld();
             const int i = lr - 64;
             const float *Us = reinterpret_cast<const float *>(buf + kBufU);
@@ -634,28 +688,33 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                     }
                 }
                 st16(B2 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zh);
-                st16(B2 + 4096 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zl);
+                st16(B2 + mnmaj(kTN + js + 8 * jg, i, kB2Lbo, kB2Sbo), zl);
             }
+        } else if (ch > 0) {
+            put_outputs(ch - 1);  // overlaps this chunk's Z
         }
         fence_async_smem();
         fence_before();
         __syncthreads();
+        bool lb_ok = true;
         if (tid == 0) {
+            lb_ok = mbar_wait(bar_lb + b, lp);
             fence_after();
-            // D2 = Kbar^T (Z_hi + Z_lo); D1 rows 0-63 += H Z (rows 64-127 receive
-            // products of whatever follows H in shared memory: W S is consumed).
-            const uint32_t id = idesc_bf16(128, kTN, 0, 1);
+        }
+        if (tid == 0 && lb_ok) {
+            // D2 = Kbar^T [Z_hi | Z_lo] (N = 64); then D1 += H [Z_hi | Z_lo], which
+            // adds H Z to the s Qbar S rows 0-63 (rows 64-127 take products of
+            // whatever follows H in shared memory; W S there is consumed).
+            const uint32_t id = idesc_bf16(128, 2 * kTN, 0, 1);
 #pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int s = 0; s < C / 16; ++s) {
-                    const uint64_t bz = desc(smem_u32(B2 + part * 4096) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo);
-                    mma_bf16(tmem + 2 * kTN, desc(smem_u32(buf + kBufA2) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo),
-                             bz, id, part > 0 || s > 0);
-                    mma_bf16(tmem + part * kTN, desc(smem_u32(buf + kBufH) + s * 2 * 1024, 1024, 128), bz,
-                             id, 1);
-                }
+            for (int s = 0; s < C / 16; ++s)
+                mma_bf16(tmem + kD2Col, desc(smem_u32(buf + kBufA2) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo),
+                         desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, s > 0);
             commit(bar_mma);
+#pragma unroll
+            for (int s = 0; s < C / 16; ++s)
+                mma_bf16(d1, desc(smem_u32(buf + kBufH) + s * 2 * 1024, 1024, 128),
+                         desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, 1);
         }
         ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
         mma_phase ^= 1;
@@ -663,39 +722,36 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         if (!ok) break;
         {
             const float gam = reinterpret_cast<const float *>(buf + kBufGam)[c];
-            float d16[16];
-            tmem_ld16(tmem + lane_base + 2 * kTN + js, d16);
-            tmem_wait_ld();
-#pragma unroll
-            for (int r = 0; r < 16; ++r) S[r] = gam * S[r] + d16[r];
-            put_state();
-        }
-        if (lr < 64) {
-            // O = s Qbar S + H Z for token row i, slab columns js .. js + 15.
-            const int i = lr, clen = min(C, len - ch * C);
             float hi[16], lo[16];
-            tmem_ld16(tmem + lane_base + js, hi);
-            tmem_ld16(tmem + lane_base + kTN + js, lo);
+            tmem_ld16(tmem + lane_base + kD2Col + js, hi);
+            tmem_ld16(tmem + lane_base + kD2Col + kTN + js, lo);
             tmem_wait_ld();
-            if (i < clen) {
-                __nv_bfloat16 *dst = out + ((size_t)(bos + ch * C + i) * H + h) * D + j0 + js;
 #pragma unroll
-                for (int jg = 0; jg < 2; ++jg) {
-                    float o8[8];
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) o8[r] = hi[8 * jg + r] + lo[8 * jg + r];
-                    *reinterpret_cast<uint4 *>(dst + 8 * jg) = pack8(o8);
-                }
-            }
+            for (int r = 0; r < 16; ++r) S[r] = gam * S[r] + (hi[r] + lo[r]);
+            put_state();
         }
         fence_async_smem();
         fence_before();
         __syncthreads();
     }
+    if (ok && nchunks > 0) {
+        // The last chunk's H Z product: one more commit covers it.
+        if (tid == 0) {
+            fence_after();
+            commit(bar_mma);
+        }
+        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
+        mma_phase ^= 1;
+        fence_after();
+        if (ok && lr < 64) put_outputs(nchunks - 1);
+    }
     if (!ok) {
         if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
-        mbar_wait(bar_load, 0);
-        mbar_wait(bar_load + 1, 0);
+        // Bounded waits for copies and MMAs that may still be in flight.
+        for (int bb = 0; bb < 2; ++bb) {
+            mbar_wait(bar_la + bb, 0);
+            mbar_wait(bar_lb + bb, 0);
+        }
         mbar_wait(bar_mma, mma_phase);
     } else if (final_state) {
 #pragma unroll
@@ -704,7 +760,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     }
     fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc<128>(tmem);
+    if (warp == 0) tmem_dealloc<256>(tmem);
 }
 
 }  // namespace
