@@ -165,6 +165,29 @@ def measured_peaks():
             "source": "fallback"}
 
 
+def kernel_sources_sha256():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kimi_delta_attention_17_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic(key):
+    """DRAM bytes per launch from the committed ncu capture (profiles/ncu_traffic.json),
+    or None when the kernel sources have changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    t = json.load(open(path))
+    if t.get("kernel_sources_sha256") != kernel_sources_sha256() or key not in t:
+        return None
+    return t[key]["bytes_per_launch"]
+
+
 # ------------------------------------------------------------------ the oracle on the host cores
 
 def oracle_prefill_sample(inp, spec, target_s=10.0, max_tokens=None):
@@ -378,7 +401,9 @@ def bench_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32",
+            # bf16 storage at d = 128 runs the tensor-core path (bf16 operands,
+            # fp32 accumulation and state); everything else the fp32 path.
+            "dtype": "bf16" if (spec.dtype == "bf16" and d == 128) else "f32",
             "data": "synthetic",
             "config": {"workload": spec.name, "B": B, "T": T, "H": H, "d_k": d, "d_v": d,
                        "chunk": 64, "storage": spec.dtype, "num_seqs": N,
@@ -386,7 +411,9 @@ def bench_ours(args):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "kernel": "kda_chunk_fwd (all phases)",
                          "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved_gbs / peaks["hbm_gbs"],
+                         "traffic": (measured_traffic("prefill_long_t131072")
+                                     if spec == kin.LONG_128K else None),
                          "algorithmic_bytes_per_launch": pbytes,
                          "peak_source": peaks["source"],
                          "phases_ms": phase_ms, "dominant_phase": dominant,
@@ -403,7 +430,8 @@ def bench_ours(args):
                 "value": dec_steps_s, "unit": "steps/s", "ms_per_step": dec_ms_launch,
                 "roofline": {"bound": "hbm", "kernel": "decode_step_kernel",
                              "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                             "frac": dec_gbs / peaks["hbm_gbs"], "traffic": None,
+                             "frac": dec_gbs / peaks["hbm_gbs"],
+                             "traffic": measured_traffic("decode_256x32"),
                              "algorithmic_bytes_per_launch": dbytes},
                 "e2e": {"value": world * dspec.steps / (de_ms / 1e3), "unit": "steps/s",
                         "h2d_bytes_per_step": d_h2d, "d2h_bytes_per_step": d_d2h},

@@ -48,8 +48,10 @@ def test_prefill_workload(spec, heads):
     fin_s = f64(fin[:, sel])
     del out, fin
     ref_out, ref_fin = oracle_prefill(inp, heads=heads)
-    assert_parity(out_s, ref_out, spec.dtype, "O")
-    assert_parity(fin_s, ref_fin, spec.dtype, "final state")
+    eo = assert_parity(out_s, ref_out, spec.dtype, "O")
+    es = assert_parity(fin_s, ref_fin, spec.dtype, "final state")
+    print("\n%s: O max|err| %.3g rel %.3g; final state max|err| %.3g rel %.3g"
+          % (spec.name, eo[0], eo[1], es[0], es[1]))
 
 
 def test_decode_workload():
@@ -69,4 +71,5 @@ def test_decode_workload():
         ref_out, ref_state = oracle.decode_step(*(f64(inp[n][t][seqs]) for n in ("q", "k", "v", "g", "beta")),
                                                 inp["scale"], ref_state)
         assert_parity(f64(outs[t]), ref_out, spec.dtype, "decode O step %d" % t)
-    assert_parity(f64(state[seqs]), ref_state, spec.dtype, "decode state after %d steps" % spec.steps)
+    es = assert_parity(f64(state[seqs]), ref_state, spec.dtype, "decode state after %d steps" % spec.steps)
+    print("\n%s: state after %d steps max|err| %.3g rel %.3g" % (spec.name, spec.steps, es[0], es[1]))
