@@ -1,23 +1,21 @@
 // Tensor-core chunkwise prefill for bf16 q/k/v with d_k = d_v = 128 (sm_103a:
-// tcgen05.mma with TMEM accumulators, 1-D bulk copies for the state pass).
+// tcgen05.mma with TMEM accumulators, tensor-map and 1-D bulk copies).
 //
 // The algebra is the chunkwise form of "Understanding Kimi Delta Attention"
-// (sections "The triangular system" and "Putting the chunks together"), with
-// the output regrouped as O = (Qbar - H W) S0 + H U = Q' S0 + Ou so that the
-// serial state pass only multiplies by the state:
+// (sections "The triangular system" and "Putting the chunks together"):
 //
-//   phase 1 (every chunk and head in parallel, one CTA each):
+//   phase 1 (every chunk and head in parallel; persistent, one CTA per SM):
 //     G      in-chunk cumulative log-decay (registers, one thread per channel)
 //     A, H   decay-gated K K^T and Q K^T, from ONE tcgen05.mma (below)
 //     T      (I - A)^{-1}: blocked forward substitution in fp32 shared memory
-//     W = (T B) L,  U = (T B) V                 two MMAs, B = Diag(beta)
-//     Q' = Qbar - H W,  Ou = H U                two MMAs
-//     Kbar^T, exp(G_n)                          elementwise
+//     W = (T B) L,  U = (T B) V                 one MMA pair, B = Diag(beta)
+//     s Qbar, Kbar^T, exp(G_n)                  elementwise
 //   phase 2 (one CTA per sequence, head and 32-column slab of the state,
-//   chunks in order, state in registers):
-//     [W S; Q' S] = [W; Q'] S                   one MMA, M = 128
-//     Z = U - W S,  O = Ou + Q' S
+//   chunks in order, state in registers, warp-specialised):
+//     [s Qbar S; W S] = [s Qbar; W] S           one MMA, M = 128
+//     Z = U - W S                               elementwise
 //     S <- Diag(exp(G_n)) S + Kbar^T Z          one MMA
+//     O = s Qbar S + H Z                        one MMA into the first one's rows
 //
 // Decay absorption with secondary chunking ("Kimi Delta Attention: a half-life
 // per channel", section "What changes in the kernel"): the per-channel pair
@@ -53,15 +51,20 @@ constexpr int D = 128;   // d_k = d_v on this path
 constexpr int C = kChunk;
 constexpr int kTN = 32;  // state columns per phase-2 CTA
 
-// Workspace region of one (chunk slot, head), byte offsets.
+// Workspace region of one (chunk slot, head), byte offsets. Everything every
+// state-pass CTA of the head needs comes first, contiguous, so that it moves
+// in one bulk copy; each CTA's U slab follows. (An SM completes about one bulk
+// copy per 900 cycles whatever its size, up to 64 KiB: copies must be few and large.)
 struct TcRegion {
     static constexpr size_t A1 = 0;        // [s Qbar; W] bf16, MN-major, 128 tokens x 128 ch
     static constexpr size_t A2 = 32768;    // Kbar^T bf16, K-major, 128 ch x 64 tokens
     static constexpr size_t Hm = 49152;    // H bf16, K-major [token i][token j] (LBO 1024, SBO 128)
-    static constexpr size_t U = 57344;     // fp32 [4 slabs][64 tokens][32 columns], rows swizzled
-    static constexpr size_t Gam = 90112;   // fp32 [128] exp(G_n)
+    static constexpr size_t Gam = 57344;   // fp32 [128] exp(G_n)
+    static constexpr size_t shared = 57856;  // bytes of the part above
+    static constexpr size_t U = 57856;     // fp32 [4 slabs][64 tokens][32 columns], rows swizzled
     static constexpr size_t bytes = 90624;
 };
+static_assert(TcRegion::U + 4 * 64 * 32 * 4 == TcRegion::bytes, "region layout");
 // Element (token i, column j of a 32-column slab) of a U slab: the float4
 // groups of a row are XOR-swizzled by (i & 7), so the phase-2 thread that owns
 // row i reads it without bank conflicts, while phase 1 (one thread per column)
@@ -74,14 +77,13 @@ constexpr uint32_t kA1Lbo = 128, kA1Sbo = 2048;  // MN-major: channel cores adja
 constexpr uint32_t kA2Lbo = 2048, kA2Sbo = 128;  // K-major: channel groups adjacent
 
 // ---------------------------------------------------------------- phase 1
-// Persistent: one CTA per SM walks the (chunk slot, head) items, heads
-// fastest. The raw rows of the next item (q, k, v bf16 and g fp32, one 1-D
-// bulk copy per token row and tensor, issued by 256 threads at once) stream
-// into the staging area while the current item runs its MMAs, solve and
-// stores. Thread (c, half) owns key/value channel c and tokens
-// [32 half, 32 half + 32) in the elementwise pass; for TMEM read-back thread
-// t owns lane t mod 128, the two halves of the CTA splitting the columns.
-constexpr int kP1Threads = 256;
+// Persistent: one CTA of 16 warps per SM walks the (chunk slot, head) items,
+// heads fastest. The raw rows of the next item (q, k, v bf16 and g fp32: four
+// tensor-map tiles) stream into the staging area while the current item runs
+// its MMAs, solve and stores. Thread (c, blk) owns key/value channel c and the
+// 16-token block blk in the elementwise pass; for TMEM read-back thread t owns
+// lane t mod 128, the four warps of a lane quadrant splitting the columns.
+constexpr int kP1Threads = 512;
 struct P1 {  // shared-memory offsets, bytes
     static constexpr int q = 0, k = 16384, v = 32768, g = 49152;  // staging rows of one chunk
     static constexpr int am = 81920;    // [Ktilde; s Qtilde] bf16, MN-major 128 x 128
@@ -91,7 +93,8 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int beta = 188416; // 64 floats
     static constexpr int bar = 188672;  // mbarriers: staging loaded, MMA done
     static constexpr int tmem = 188688;
-    static constexpr int bytes = 188704;
+    static constexpr int exch = 188704; // fp32 [2][4][128]: block totals and local references of G
+    static constexpr int bytes = 192800;
     // Reused once the first MMA has consumed am / bm:
     static constexpr int As = am;                // fp32 [64][68]: A
     static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
@@ -114,15 +117,29 @@ __global__ void __launch_bounds__(kP1Threads, 1)
 tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                const float *__restrict__ beta, float scale, const ChunkEntry *__restrict__ table,
-               long long nslots, int H, unsigned char *__restrict__ ws, int *__restrict__ status) {
+               const int *__restrict__ used_slots, long long nslots, int H,
+               unsigned char *__restrict__ ws, int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int c = tid & 127, half = tid >> 7;
+    const int c = tid & 127, blk = tid >> 7;  // channel; 16-token block / column group
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + P1::bar);
     uint64_t *bar_mma = bar_ld + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P1::tmem);
     float *beta_s = reinterpret_cast<float *>(sm + P1::beta);
-    const long long nitems = nslots * H;
+    // Slots [0, used) of the table hold every chunk, in order; the rest are empty.
+    const int used = (int)min((long long)*used_slots, nslots);
+    // Items are (slot, head) pairs, heads fastest; CTA b takes items b, b + grid,
+    // ...: stepping by the grid in (slot, head) form keeps 64-bit divisions off
+    // the item path.
+    const int step_s = (int)(gridDim.x / H), step_h = (int)(gridDim.x % H);
+    auto advance = [&](int &sl, int &hh) {
+        sl += step_s;
+        hh += step_h;
+        if (hh >= H) {
+            hh -= H;
+            ++sl;
+        }
+    };
 
     if (warp == 0) tmem_alloc<256>(tslot);
     if (tid == 0) {
@@ -136,16 +153,11 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t tmem = *tslot;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    auto next_item = [&](long long w) {
-        while (w < nitems && table[w / H].seq < 0) w += gridDim.x;
-        return w;
-    };
     // One thread fetches an item: four 3-D TMA tiles (128 channels x 1 head x
     // 64 tokens) land as dense [token][channel] rows. Tokens past the end of
     // the tensor read as zeros; tokens of the next sequence are masked by len.
-    auto issue = [&](long long w, const ChunkEntry e) {
+    auto issue = [&](int hh, const ChunkEntry e) {
         if (tid != 0) return;
-        const int hh = (int)(w % H);
         mbar_expect_tx(bar_ld, 64u * (3u * 256u + 512u));
         tma_load_3d(sm + P1::q, &tm_q, 0, hh, e.bos, bar_ld);
         tma_load_3d(sm + P1::k, &tm_k, 0, hh, e.bos, bar_ld);
@@ -153,99 +165,104 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tma_load_3d(sm + P1::g, &tm_g, 0, hh, e.bos, bar_ld);
     };
 
-    long long w = next_item(blockIdx.x);
-    if (w < nitems) issue(w, table[w / H]);
+    // Each item's table entry and beta values are read one item ahead, so
+    // that no global load latency sits on the item's path.
+    auto beta_of = [&](int hh, const ChunkEntry &e) {
+        return tid < C && tid < e.len ? beta[(size_t)(e.bos + tid) * H + hh] : 0.f;
+    };
+    int sl = (int)(blockIdx.x / H), hc = (int)(blockIdx.x % H);  // this item
+    ChunkEntry ce{};
+    float bcur = 0.f;
+    if (sl < used) {
+        ce = table[sl];
+        issue(hc, ce);
+        bcur = beta_of(hc, ce);
+    }
+    int sn = sl, hn = hc;  // the next item
+    advance(sn, hn);
+    ChunkEntry en = sn < used ? table[sn] : ce;
     uint32_t ld_phase = 0, mma_phase = 0;
     bool ok = true;
-    while (w < nitems) {
-        const ChunkEntry ce = table[w / H];
-        const int h = (int)(w % H);
+    while (sl < used) {
         const int len = ce.len;
-        unsigned char *reg = ws + (size_t)w * TcRegion::bytes;  // w = slot * H + h
+        int snn = sn, hnn = hn;  // the item after next
+        ChunkEntry enn;
+        float bn;
+        unsigned char *reg = ws + ((size_t)sl * H + hc) * TcRegion::bytes;
         ok = __syncthreads_and(mbar_wait(bar_ld, ld_phase));
         ld_phase ^= 1;
         if (!ok) break;
-        // The next item and its table entry, read now so that the prefetch
-        // below does not wait on global memory.
-        const long long wn = next_item(w + gridDim.x);
-        ChunkEntry en = ce;
-        if (wn < nitems) en = table[wn / H];
 
-        // ================= elementwise pass (thread = channel c, 32 tokens)
+        // ================= elementwise pass (thread = channel c, block blk of 16 tokens)
         {
             const float *gs = reinterpret_cast<const float *>(sm + P1::g);
             const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::q);
             const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::k);
             const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::v);
-            // Cumulative log-decay of channel c. Each thread sums all 64 tokens
-            // (no exchange between the two halves) but keeps only the prefixes of
-            // its own 32; the block references r(I) = 7, 23, 39, 55 and the chunk
-            // end come out of the same pass.
-            float G[32];
-            float R0, R1, R2, R3, Gend;
-            if (half == 0) {
-                float acc = 0.f;
+            // Cumulative log-decay of channel c: each thread sums its own block,
+            // keeping the 16 in-block prefixes; block totals and in-block
+            // references (token 7 of each block) are exchanged so that every
+            // thread has the absolute references R_I = G_{16 I + 7} and the chunk
+            // total. In-block factors need only the local prefixes (the block's
+            // offset cancels in G_i - G_r).
+            float G[16];
+            float acc = 0.f;
 #pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    acc += r < len ? gs[r * D + c] : 0.f;
-                    G[r] = acc;
-                }
-                R0 = G[7];
-                R1 = G[23];
-#pragma unroll
-                for (int r = 32; r < 64; ++r) {
-                    acc += r < len ? gs[r * D + c] : 0.f;
-                    if (r == 39) R2 = acc;
-                    if (r == 55) R3 = acc;
-                }
-                Gend = acc;
-            } else {
-                float acc = 0.f;
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    acc += r < len ? gs[r * D + c] : 0.f;
-                    if (r == 7) R0 = acc;
-                    if (r == 23) R1 = acc;
-                }
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    acc += 32 + r < len ? gs[(32 + r) * D + c] : 0.f;
-                    G[r] = acc;
-                }
-                R2 = G[7];
-                R3 = G[23];
-                Gend = G[31];
+            for (int t = 0; t < 16; ++t) {
+                const int tok = 16 * blk + t;
+                acc += tok < len ? gs[tok * D + c] : 0.f;
+                G[t] = acc;
             }
-            if (tid < C) beta_s[tid] = tid < len ? beta[(size_t)(ce.bos + tid) * H + h] : 0.f;
-            // Per-channel block constants (see the header comment).
-            const float Rf[4] = {R0, R1, R2, R3};
-            float P[4], Y[4], X[4][4];
+            float *tot_s = reinterpret_cast<float *>(sm + P1::exch);
+            float *ref_s = tot_s + 4 * D;
+            tot_s[blk * D + c] = acc;
+            ref_s[blk * D + c] = G[7];
+            if (tid < C) beta_s[tid] = bcur;
+            __syncthreads();
+            // The table entry of the item after next and the next item's beta,
+            // read here: a CTA barrier waits for its threads' loads, and the next
+            // one is the whole elementwise pass away.
+            advance(snn, hnn);
+            enn = snn < used ? table[snn] : en;
+            bn = sn < used ? beta_of(hn, en) : 0.f;
+            float R[4], off = 0.f;
 #pragma unroll
             for (int I = 0; I < 4; ++I) {
-                P[I] = __expf(Rf[I]);
-                Y[I] = __expf(Gend - Rf[I]);
-#pragma unroll
-                for (int J = 0; J < 4; ++J) X[I][J] = J < I ? __expf(Rf[I] - Rf[J]) : 1.f;
+                R[I] = off + ref_s[I * D + c];
+                off += tot_s[I * D + c];
             }
+            const float Gend = off;
+            // Per-channel block constants (see the header comment): the own
+            // block's reference, exp of it from the chunk start and to the chunk
+            // end, and the factors exp(R_I - R_blk) of the later blocks' versions.
+            const float Rs = blk == 0 ? R[0] : blk == 1 ? R[1] : blk == 2 ? R[2] : R[3];
+            const float Rl = G[7];  // the same reference, relative to the block start
+            const float Ps = __expf(Rs), Ys = __expf(Gend - Rs);
+            float Xv[4];
 #pragma unroll
-            for (int ig = 0; ig < 4; ++ig) {
-                const int jj = ig >> 1;               // block within this half
-                const int i0 = 32 * half + 8 * ig;    // first token of the group
-                const int Jr = 2 * half + jj;         // block index of these tokens
-                const float Rs = half ? Rf[2 + jj] : Rf[jj];
-                const float Ps = half ? P[2 + jj] : P[jj];
-                const float Ys = half ? Y[2 + jj] : Y[jj];
-                float kv[8], qv[8], vv[8], E[8], kF[8], t8[8];
+            for (int I = 0; I < 4; ++I) Xv[I] = I > blk ? __expf(R[I] - Rs) : 1.f;
+#pragma unroll
+            for (int ig = 0; ig < 2; ++ig) {
+                const int i0 = 16 * blk + 8 * ig;  // first token of the group
+                float kv[8], qv[8], E[8], kF[8], t8[8];
+                uint32_t vraw[4];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int i = i0 + r;
                     const bool in = i < len;
                     kv[r] = in ? __bfloat162float(ks[i * D + c]) : 0.f;
                     qv[r] = in ? scale * __bfloat162float(qs[i * D + c]) : 0.f;
-                    vv[r] = in ? __bfloat162float(vs[i * D + c]) : 0.f;
-                    const float x = G[8 * ig + r] - Rs;
+                    const float x = G[8 * ig + r] - Rl;
                     E[r] = __expf(x);
                     kF[r] = kv[r] * __expf(-x);
+                }
+                // V^T needs no arithmetic: move the bf16 bits (zero past the end).
+                const unsigned short *vb = reinterpret_cast<const unsigned short *>(vs);
+#pragma unroll
+                for (int r = 0; r < 8; r += 2) {
+                    const uint32_t lo = i0 + r < len ? vb[(i0 + r) * D + c] : 0u;
+                    const uint32_t hi = i0 + r + 1 < len ? vb[(i0 + r + 1) * D + c] : 0u;
+                    vraw[r >> 1] = lo | (hi << 16);
                 }
 #pragma unroll
                 for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r];
@@ -255,11 +272,10 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 st16(sm + P1::am + mnmaj(64 + i0, c, kA1Lbo, kA1Sbo), t8);
 #pragma unroll
                 for (int I = 0; I < 4; ++I) {
-                    if (I < Jr) continue;
-                    const float Xs = half ? X[I][2 + jj] : X[I][jj];
-                    const int n0 = 16 * (I * (I + 1) / 2 + Jr) + 8 * (ig & 1);
+                    if (I < blk) continue;
+                    const int n0 = 16 * (I * (I + 1) / 2 + blk) + 8 * ig;
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) t8[r] = kF[r] * Xs;
+                    for (int r = 0; r < 8; ++r) t8[r] = kF[r] * Xv[I];
                     st16(sm + P1::bm + mnmaj(n0, c, kA1Lbo, kA1Sbo), t8);
                 }
 #pragma unroll
@@ -268,13 +284,14 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r] * Ps;
                 st16(sm + P1::lt + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
-                st16(sm + P1::vt + kmaj(c, i0, kA2Lbo, kA2Sbo), vv);
+                *reinterpret_cast<uint4 *>(sm + P1::vt + kmaj(c, i0, kA2Lbo, kA2Sbo)) =
+                    make_uint4(vraw[0], vraw[1], vraw[2], vraw[3]);
                 // s Qbar, rows 0-63 of the state-pass operand [s Qbar; W].
 #pragma unroll
                 for (int r = 0; r < 8; ++r) t8[r] = qv[r] * E[r] * Ps;
                 st16(reg + TcRegion::A1 + mnmaj(i0, c, kA1Lbo, kA1Sbo), t8);
             }
-            if (half == 1) reinterpret_cast<float *>(reg + TcRegion::Gam)[c] = __expf(Gend);
+            if (blk == 3) reinterpret_cast<float *>(reg + TcRegion::Gam)[c] = __expf(Gend);
         }
         fence_async_smem();
         fence_before();
@@ -291,7 +308,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             commit(bar_mma);
         }
         // The staging rows are consumed: fetch the next item's while this one runs.
-        if (wn < nitems) issue(wn, en);
+        if (sn < used) issue(hn, en);
         ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
         mma_phase ^= 1;
         fence_after();
@@ -301,14 +318,14 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             unsigned char *Hs = reg + TcRegion::Hm;  // H goes straight to the workspace
             const int lr = tid & 127, i = lr & 63, Iblk = i >> 4;
             const bool isH = lr >= 64;
-            const int side = warp >> 2;
+            const int grp = warp >> 2;           // which of the quadrant's four warps
             const bool upper = (warp & 1) != 0;  // rows 32-63: blocks 2, 3
             const float bi = beta_s[i];
 #pragma unroll
             for (int vv = 0; vv < 10; ++vv) {
-                // Versions of this warp's rows, split between the two halves of the CTA.
-                const bool mine = upper ? (side ? vv >= 7 : (vv >= 3 && vv < 7))
-                                        : (side ? vv == 2 : vv < 2);
+                // Versions of this warp's rows (blocks 0-1: versions 0-2; blocks
+                // 2-3: versions 3-9), split among the quadrant's four warps.
+                const bool mine = upper ? (vv >= 3 && ((vv - 3) >> 1) == grp) : vv == grp;
                 if (!mine) continue;  // warp-uniform
                 float x[16];
                 tmem_ld16(tmem + lane_base + vv * 16, x);
@@ -337,7 +354,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
             }
-            if (side == 0) {
+            if (grp == 3) {
 #pragma unroll
                 for (int J = 0; J < 4; ++J) {
                     if (J <= Iblk) continue;
@@ -425,10 +442,9 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
                 __syncthreads();
             }
-            const int i = tid & 63, jq = tid >> 6;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int jb = 16 * jq + 8 * hf;
+            {
+                // Row i, columns jb .. jb + 7 of T Diag(beta): one 16-byte run per thread.
+                const int i = tid & 63, jb = 8 * (tid >> 6);
                 float t8[8];
 #pragma unroll
                 for (int f = 0; f < 2; ++f) {
@@ -464,11 +480,13 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         fence_after();
         if (!ok) break;
         {
-            // W -> rows 64-127 of [s Qbar; W] (side 0); U -> its slab (side 1).
-            const int side = tid >> 7;
+            // W -> rows 64-127 of [s Qbar; W] (column groups 0, 1); U -> its slab
+            // (groups 2, 3); each thread reads two 16-token parts of its lane.
+            const int side = blk >> 1;
             float *slab = reinterpret_cast<float *>(reg + TcRegion::U) + (size_t)(c >> 5) * (C * 32);
 #pragma unroll
-            for (int part = 0; part < 4; ++part) {
+            for (int pp = 0; pp < 2; ++pp) {
+                const int part = 2 * (blk & 1) + pp;
                 float x[16];
                 tmem_ld16(tmem + lane_base + 64 * side + 16 * part, x);
                 tmem_wait_ld();
@@ -484,7 +502,13 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         fence_before();
         __syncthreads();
         fence_after();
-        w = wn;
+        sl = sn;
+        hc = hn;
+        ce = en;
+        sn = snn;
+        hn = hnn;
+        en = enn;
+        bcur = bn;
     }
     if (!ok) {
         if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
@@ -507,19 +531,37 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 //                  S <- Diag(exp G_n) S + D2,  O = D1[0:64] = s Qbar S + H Z
 // ("Understanding Kimi Delta Attention", "The token outputs" and "One state
 // crosses the chunk boundary"). S and Z enter the MMAs as bf16 hi + lo pairs.
-constexpr int kP2Threads = 256;
-constexpr int kBufBytes = 66560;  // one chunk's A1, A2, H, U slab, gamma (65 KiB)
-constexpr int kBufA2 = 32768, kBufH = 49152, kBufU = 57344, kBufGam = 65536;
-// Each buffer fills in two parts: A = [s Qbar; W], U slab, gamma (free once the
-// chunk two back has finished its first product and state update); B =
-// Kbar^T, H (free only once that chunk's H Z product has completed).
-constexpr uint32_t kLoadBytesA = 32768 + 8192 + 512;
-constexpr uint32_t kLoadBytesB = 16384 + 8192;
-constexpr int kP2B1 = 2 * kBufBytes;            // S (hi | lo) bf16, MN-major [K = ch][N = 64]
+// Warp roles: warps 0-15 compute (warp w reads TMEM lanes 32 (w % 4) ..
+// + 31 and owns state columns 8 (w / 4) .. + 7 of the slab); warp 16 issues
+// the MMAs; warp 17's lane 0 issues every bulk copy of the chunk tiles (a
+// copy's issue can hold its thread for a hundred cycles or more).
+constexpr int kP2Compute = 512;
+constexpr int kP2MmaWarp = kP2Compute / 32;
+constexpr int kP2ProdWarp = kP2MmaWarp + 1;
+constexpr int kP2Threads = kP2Compute + 64;
+constexpr int kP2Sync = kP2Compute + 32;  // compute warps + MMA warp
+constexpr int kBarZ = 1, kBarS = 2;       // named barriers: Z written, state written
+constexpr int kP2Bufs = 3;        // chunk buffers: loads run ahead of use
+// One chunk's buffer: the region's shared part (A1, A2, H, gamma) at the same
+// offsets as in the workspace, then this CTA's U slab. Two bulk copies fill it;
+// it is free again once the chunk that last used it has finished its H Z product.
+constexpr int kBufA2 = (int)TcRegion::A2, kBufH = (int)TcRegion::Hm, kBufGam = (int)TcRegion::Gam;
+constexpr int kBufU = (int)TcRegion::shared;
+constexpr int kBufBytes = 66560;  // 65 KiB
+constexpr uint32_t kSlabBytes = kTN * C * 4;
+constexpr uint32_t kLoadBytes = (uint32_t)TcRegion::shared + kSlabBytes;
+static_assert(kBufU + (int)kSlabBytes <= kBufBytes, "chunk buffer too small");
+constexpr int kP2B1 = kP2Bufs * kBufBytes;      // S (hi | lo) bf16, MN-major [K = ch][N = 64]
 constexpr int kP2B2 = kP2B1 + 16384;            // [Z_hi | Z_lo] bf16, MN-major [K = token][N = 64]
-constexpr int kP2Bar = kP2B2 + 8192;            // 5 mbarriers: load A[2], load B[2], MMA
-constexpr int kP2Tmem = kP2Bar + 40;
-constexpr int kP2Smem = kP2Tmem + 8;
+// mbarriers: loaded[3], free[3], first product, second product; then the
+// TMEM base and the error flag.
+constexpr int kP2Bar = kP2B2 + 8192;
+constexpr int kP2NBar = 2 * kP2Bufs + 2;
+constexpr int kP2Tmem = kP2Bar + 8 * kP2NBar;
+constexpr int kP2Err = kP2Tmem + 4;
+constexpr int kP2Smem = kP2Err + 4;
+static_assert(kBufBytes % 1024 == 0 && kP2B1 % 1024 == 0, "operand tiles must stay 1 KiB aligned");
+static_assert(kP2Smem <= 232448, "phase-2 shared memory exceeds 227 KiB");
 constexpr uint32_t kB1Lbo = 128, kB1Sbo = 2048;
 constexpr uint32_t kB2Lbo = 128, kB2Sbo = 1024;
 // TMEM columns: D1 alternates between [0, 64) and [64, 128) from chunk to
@@ -533,8 +575,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
               __nv_bfloat16 *__restrict__ out, float *final_state, int H, int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int n = blockIdx.x, h = blockIdx.y, jt = blockIdx.z, j0 = jt * kTN;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int lr = tid & 127, side = tid >> 7, js = 16 * side;  // lane / row, first slab column
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int bos, len;
     if (cu_seqlens) {
         bos = cu_seqlens[n];
@@ -547,47 +588,48 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     const int slot0 = seq_first_slot[n];
     unsigned char *B1 = sm + kP2B1;
     unsigned char *B2 = sm + kP2B2;
-    uint64_t *bar_la = reinterpret_cast<uint64_t *>(sm + kP2Bar);  // [2]
-    uint64_t *bar_lb = bar_la + 2;                                  // [2]
-    uint64_t *bar_mma = bar_la + 4;
+    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kP2Bar);  // [kP2Bufs] tiles landed
+    uint64_t *bar_fr = bar_ld + kP2Bufs;                            // [kP2Bufs] tiles consumed
+    uint64_t *bar_m1 = bar_fr + kP2Bufs;                            // first product done
+    uint64_t *bar_m2 = bar_m1 + 1;                                  // second product done
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kP2Tmem);
-
-    const int c = lr;  // state row
-    const size_t st_off = (((size_t)n * H + h) * D + c) * D + j0 + js;
-    float S[16];
-    if (init_state) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-            const float4 t = *reinterpret_cast<const float4 *>(init_state + st_off + j);
-            S[j] = t.x; S[j + 1] = t.y; S[j + 2] = t.z; S[j + 3] = t.w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) S[j] = 0.f;
-    }
-    auto put_state = [&]() {  // B1 rows js + j (hi) and 32 + js + j (lo), K-row c
-#pragma unroll
-        for (int jg = 0; jg < 2; ++jg) {
-            float hi[8], lo[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const float x = S[8 * jg + r];
-                hi[r] = __bfloat162float(__float2bfloat16_rn(x));
-                lo[r] = x - hi[r];
-            }
-            st16(B1 + mnmaj(js + 8 * jg, c, kB1Lbo, kB1Sbo), hi);
-            st16(B1 + mnmaj(kTN + js + 8 * jg, c, kB1Lbo, kB1Sbo), lo);
+    volatile int *err = reinterpret_cast<volatile int *>(sm + kP2Err);
+    // A bounded wait that is skipped once any warp has given up; a timeout
+    // raises the CTA's error flag and the call's status.
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        if (*err) return;
+        if (!mbar_wait(bar, parity)) {
+            *err = 1;
+            atomicExch(status, (int)KDA_ERR_TIMEOUT);
         }
     };
-    put_state();
 
+    // Compute-thread coordinates: TMEM lane / state row r, slab columns js .. js + 7.
+    const int r = 32 * (warp & 3) + lane, js = 8 * ((warp >> 2) & 3);
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const size_t st_off = (((size_t)n * H + h) * D + r) * D + j0 + js;
+    float S[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) S[j] = 0.f;
+    auto put_state = [&]() {  // B1 rows js + j (hi) and 32 + js + j (lo), K-row r
+        uint4 hi, lo;
+        split8(S, hi, lo);
+        *reinterpret_cast<uint4 *>(B1 + mnmaj(js, r, kB1Lbo, kB1Sbo)) = hi;
+        *reinterpret_cast<uint4 *>(B1 + mnmaj(kTN + js, r, kB1Lbo, kB1Sbo)) = lo;
+    };
+    if (warp < kP2MmaWarp) {
+        if (init_state) {
+            const float4 t0 = *reinterpret_cast<const float4 *>(init_state + st_off);
+            const float4 t1 = *reinterpret_cast<const float4 *>(init_state + st_off + 4);
+            S[0] = t0.x; S[1] = t0.y; S[2] = t0.z; S[3] = t0.w;
+            S[4] = t1.x; S[5] = t1.y; S[6] = t1.z; S[7] = t1.w;
+        }
+        put_state();
+    }
     if (warp == 0) tmem_alloc<256>(tslot);
     if (tid == 0) {
-        mbar_init(bar_la, 1);
-        mbar_init(bar_la + 1, 1);
-        mbar_init(bar_lb, 1);
-        mbar_init(bar_lb + 1, 1);
-        mbar_init(bar_mma, 1);
+        for (int i = 0; i < kP2NBar; ++i) mbar_init(bar_ld + i, 1);
+        *err = 0;
         mbar_fence_init();
     }
     fence_async_smem();
@@ -595,168 +637,164 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    auto region_of = [&](int ch) { return ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes; };
-    auto issue_a = [&](int ch, int b) {
-        const unsigned char *r = region_of(ch);
-        unsigned char *dst = sm + b * kBufBytes;
-        mbar_expect_tx(bar_la + b, kLoadBytesA);
-        bulk_g2s(dst, r + TcRegion::A1, 32768, bar_la + b);
-        bulk_g2s(dst + kBufU, r + TcRegion::U + (size_t)jt * kTN * C * 4, kTN * C * 4, bar_la + b);
-        bulk_g2s(dst + kBufGam, r + TcRegion::Gam, 512, bar_la + b);
-    };
-    auto issue_b = [&](int ch, int b) {
-        const unsigned char *r = region_of(ch);
-        unsigned char *dst = sm + b * kBufBytes;
-        mbar_expect_tx(bar_lb + b, kLoadBytesB);
-        bulk_g2s(dst + kBufA2, r + TcRegion::A2, 16384, bar_lb + b);
-        bulk_g2s(dst + kBufH, r + TcRegion::Hm, 8192, bar_lb + b);
-    };
-    if (tid == 0 && nchunks > 0) {
-        issue_a(0, 0);
-        issue_b(0, 0);
-    }
-
-    uint32_t mma_phase = 0;
-    bool ok = true;
-    // Token outputs of chunk `ch` (rows 0-63 of its D1): s Qbar S + H Z.
-    auto put_outputs = [&](int ch) {
-        const int i = lr, clen = min(C, len - ch * C);
-        const uint32_t d1 = tmem + lane_base + 64 * (ch & 1);
-        float hi[16], lo[16];
-        tmem_ld16(d1 + js, hi);
-        tmem_ld16(d1 + kTN + js, lo);
-        tmem_wait_ld();
-        if (i < clen) {
-            __nv_bfloat16 *dst = out + ((size_t)(bos + ch * C + i) * H + h) * D + j0 + js;
+    // Chunk ch lives in buffer ch % 3 and is that buffer's (ch / 3)-th use: its
+    // loads complete the phase of parity (ch / 3) & 1 of the buffer's "landed"
+    // barrier, and its release the phase of the same parity of the "free" one.
+    if (warp == kP2ProdWarp) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int ch = 0; ch < nchunks && !*err; ++ch) {
+                const int b = ch % kP2Bufs;
+                if (ch >= kP2Bufs) wait(bar_fr + b, (uint32_t)(ch / kP2Bufs - 1) & 1);
+                if (*err) break;
+                const unsigned char *rg = ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes;
+                unsigned char *dst = sm + b * kBufBytes;
+                mbar_expect_tx(bar_ld + b, kLoadBytes);
+                bulk_g2s(dst, rg, (uint32_t)TcRegion::shared, bar_ld + b);
+                bulk_g2s(dst + kBufU, rg + TcRegion::U + (size_t)jt * kSlabBytes, kSlabBytes, bar_ld + b);
+                issued = ch + 1;
+            }
+            // Every copy lands before the CTA exits (bounded waits; a buffer's
+            // last use is the newest phase of its barrier).
+            for (int cc = issued > kP2Bufs ? issued - kP2Bufs : 0; cc < issued; ++cc)
+                mbar_wait(bar_ld + cc % kP2Bufs, (uint32_t)(cc / kP2Bufs) & 1);
+        }
+        __syncwarp();
+    } else if (warp == kP2MmaWarp) {
+        // One lane issues; the whole warp keeps the named-barrier protocol, so
+        // the compute warps never wait on a barrier that cannot complete.
+        for (int ch = 0; ch < nchunks; ++ch) {
+            const int b = ch % kP2Bufs;
+            unsigned char *buf = sm + b * kBufBytes;
+            const uint32_t d1 = tmem + 64 * (ch & 1);
+            const uint32_t lp = (uint32_t)(ch / kP2Bufs) & 1;
+            if (lane == 0) {
+                wait(bar_ld + b, lp);
+                if (!*err) {
+                    // [s Qbar S; W S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
+                    fence_after();
+                    const uint32_t id = idesc_bf16(128, 2 * kTN, 1, 1);
 #pragma unroll
-            for (int jg = 0; jg < 2; ++jg) {
+                    for (int s = 0; s < D / 16; ++s)
+                        mma_bf16(d1, desc(smem_u32(buf) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo),
+                                 desc(smem_u32(B1) + s * 2 * kB1Lbo, kB1Lbo, kB1Sbo), id, s > 0);
+                    commit(bar_m1);  // also covers the previous chunk's H Z product
+                }
+            }
+            __syncwarp();
+            bar_sync(kBarZ, kP2Sync);  // Z of this chunk is in B2
+            fence_after();
+            if (lane == 0) {
+                // The compute warps saw the first product complete, and with it the
+                // previous chunk's H Z product: that chunk's buffer is free.
+                if (ch > 0) mbar_arrive(bar_fr + (ch - 1) % kP2Bufs);
+                if (!*err) {
+                    // D2 = Kbar^T [Z_hi | Z_lo] (N = 64); then D1 += H [Z_hi | Z_lo], which
+                    // adds H Z to the s Qbar S rows 0-63 (rows 64-127 take products of
+                    // whatever follows H in shared memory; W S there is consumed).
+                    fence_after();
+                    const uint32_t id = idesc_bf16(128, 2 * kTN, 0, 1);
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        mma_bf16(tmem + kD2Col, desc(smem_u32(buf + kBufA2) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo),
+                                 desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, s > 0);
+                    commit(bar_m2);
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        mma_bf16(d1, desc(smem_u32(buf + kBufH) + s * 2 * 1024, 1024, 128),
+                                 desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, 1);
+                }
+            }
+            __syncwarp();
+            bar_sync(kBarS, kP2Sync);  // the new state is in B1
+            fence_after();
+        }
+        // The last chunk's H Z product: one more commit covers it.
+        if (lane == 0 && nchunks > 0 && !*err) commit(bar_m1);
+        __syncwarp();
+    } else {
+        uint32_t p1 = 0, p2 = 0;  // phases of the two product barriers
+        const bool zrow = r >= 64;
+        // Token outputs of chunk `ch` (rows 0-63 of its D1): s Qbar S + H Z.
+        auto put_outputs = [&](int ch) {
+            const int clen = min(C, len - ch * C);
+            const uint32_t d1 = tmem + lane_base + 64 * (ch & 1);
+            float hi[8], lo[8];
+            tmem_ld8(d1 + js, hi);
+            tmem_ld8(d1 + kTN + js, lo);
+            tmem_wait_ld();
+            if (r < clen) {
                 float o8[8];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) o8[r] = hi[8 * jg + r] + lo[8 * jg + r];
-                *reinterpret_cast<uint4 *>(dst + 8 * jg) = pack8(o8);
+                for (int j = 0; j < 8; ++j) o8[j] = hi[j] + lo[j];
+                *reinterpret_cast<uint4 *>(out + ((size_t)(bos + ch * C + r) * H + h) * D + j0 + js) = pack8(o8);
             }
-        }
-    };
-    for (int ch = 0; ch < nchunks; ++ch) {
-        const int b = ch & 1;
-        unsigned char *buf = sm + b * kBufBytes;
-        const uint32_t d1 = tmem + 64 * b;
-        const uint32_t lp = (ch >> 1) & 1;  // load parity of this buffer
-        if (tid == 0 && ch + 1 < nchunks) issue_a(ch + 1, b ^ 1);
-        // Each thread waits for this chunk's tiles itself (no CTA barrier).
-        bool mine = mbar_wait(bar_la + b, lp);
-        // [s Qbar S; W S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
-        if (tid == 0) {
+        };
+        for (int ch = 0; ch < nchunks; ++ch) {
+            const int b = ch % kP2Bufs;
+            unsigned char *buf = sm + b * kBufBytes;
+            const uint32_t d1 = tmem + 64 * (ch & 1);
+            // The tiles landed long ago (the first product used them); this
+            // thread's own wait makes the copied U and gamma visible to it.
+            wait(bar_ld + b, (uint32_t)(ch / kP2Bufs) & 1);
+            wait(bar_m1, p1);
+            p1 ^= 1;
             fence_after();
-            const uint32_t id = idesc_bf16(128, 2 * kTN, 1, 1);
+            if (zrow) {
+                // Z = U - W S for token row i, slab columns js .. js + 7.
+                const int i = r - 64;
+                float hi[8], lo[8];
+                tmem_ld8(d1 + lane_base + js, hi);
+                tmem_ld8(d1 + lane_base + kTN + js, lo);
+                const float *Us = reinterpret_cast<const float *>(buf + kBufU);
+                const float4 u0 = *reinterpret_cast<const float4 *>(Us + slab_idx(i, js));
+                const float4 u1 = *reinterpret_cast<const float4 *>(Us + slab_idx(i, js + 4));
+                tmem_wait_ld();
+                const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                float z[8];
 #pragma unroll
-            for (int s = 0; s < D / 16; ++s)
-                mma_bf16(d1, desc(smem_u32(buf) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo),
-                         desc(smem_u32(B1) + s * 2 * kB1Lbo, kB1Lbo, kB1Sbo), id, s > 0);
-            commit(bar_mma);  // also covers the previous chunk's H Z product
-        }
-        mine = mine && mbar_wait(bar_mma, mma_phase);
-        mma_phase ^= 1;
-        ok = __syncthreads_and(mine);
-        fence_after();
-        if (!ok) break;
-        // The previous chunk's H Z product has completed: its buffer's B part is free.
-        if (tid == 0 && ch + 1 < nchunks) issue_b(ch + 1, b ^ 1);
-        if (lr >= 64) {
-            // Z = U - W S for token row i, slab columns js .. js + 15.
-            float hi[16], lo[16];
-            tmem_ld16(d1 + lane_base + js, hi);
-            tmem_ld16(d1 + lane_base + kTN + js, lo);
-            tmem_wait_ld();
-            const int i = lr - 64;
-            const float *Us = reinterpret_cast<const float *>(buf + kBufU);
-#pragma unroll
-            for (int jg = 0; jg < 2; ++jg) {
-                float zh[8], zl[8];
-#pragma unroll
-                for (int r4 = 0; r4 < 2; ++r4) {
-                    const float4 u = *reinterpret_cast<const float4 *>(Us + slab_idx(i, js + 8 * jg + 4 * r4));
-                    const float uv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = 4 * r4 + e;
-                        const float z = uv[e] - (hi[8 * jg + r] + lo[8 * jg + r]);
-                        zh[r] = __bfloat162float(__float2bfloat16_rn(z));
-                        zl[r] = z - zh[r];
-                    }
-                }
-                st16(B2 + mnmaj(js + 8 * jg, i, kB2Lbo, kB2Sbo), zh);
-                st16(B2 + mnmaj(kTN + js + 8 * jg, i, kB2Lbo, kB2Sbo), zl);
+                for (int j = 0; j < 8; ++j) z[j] = uv[j] - (hi[j] + lo[j]);
+                uint4 zh, zl;
+                split8(z, zh, zl);
+                *reinterpret_cast<uint4 *>(B2 + mnmaj(js, i, kB2Lbo, kB2Sbo)) = zh;
+                *reinterpret_cast<uint4 *>(B2 + mnmaj(kTN + js, i, kB2Lbo, kB2Sbo)) = zl;
+            } else if (ch > 0) {
+                put_outputs(ch - 1);  // overlaps this chunk's Z
             }
-        } else if (ch > 0) {
-            put_outputs(ch - 1);  // overlaps this chunk's Z
-        }
-        fence_async_smem();
-        fence_before();
-        __syncthreads();
-        bool lb_ok = true;
-        if (tid == 0) {
-            lb_ok = mbar_wait(bar_lb + b, lp);
+            fence_async_smem();
+            fence_before();
+            bar_arrive(kBarZ, kP2Sync);
+            const float gam = reinterpret_cast<const float *>(buf + kBufGam)[r];
+            wait(bar_m2, p2);
+            p2 ^= 1;
             fence_after();
-        }
-        if (tid == 0 && lb_ok) {
-            // D2 = Kbar^T [Z_hi | Z_lo] (N = 64); then D1 += H [Z_hi | Z_lo], which
-            // adds H Z to the s Qbar S rows 0-63 (rows 64-127 take products of
-            // whatever follows H in shared memory; W S there is consumed).
-            const uint32_t id = idesc_bf16(128, 2 * kTN, 0, 1);
+            {
+                float hi[8], lo[8];
+                tmem_ld8(tmem + lane_base + kD2Col + js, hi);
+                tmem_ld8(tmem + lane_base + kD2Col + kTN + js, lo);
+                tmem_wait_ld();
 #pragma unroll
-            for (int s = 0; s < C / 16; ++s)
-                mma_bf16(tmem + kD2Col, desc(smem_u32(buf + kBufA2) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo),
-                         desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, s > 0);
-            commit(bar_mma);
-#pragma unroll
-            for (int s = 0; s < C / 16; ++s)
-                mma_bf16(d1, desc(smem_u32(buf + kBufH) + s * 2 * 1024, 1024, 128),
-                         desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, 1);
+                for (int j = 0; j < 8; ++j) S[j] = gam * S[j] + (hi[j] + lo[j]);
+                put_state();
+            }
+            fence_async_smem();
+            fence_before();
+            // A full barrier here (an arrive would do on the normal path, where
+            // the product barriers pace the compute warps) keeps every warp
+            // within one phase of the named barriers even when a timeout has
+            // made the product waits fall through.
+            bar_sync(kBarS, kP2Sync);
         }
-        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
-        mma_phase ^= 1;
-        fence_after();
-        if (!ok) break;
-        {
-            const float gam = reinterpret_cast<const float *>(buf + kBufGam)[c];
-            float hi[16], lo[16];
-            tmem_ld16(tmem + lane_base + kD2Col + js, hi);
-            tmem_ld16(tmem + lane_base + kD2Col + kTN + js, lo);
-            tmem_wait_ld();
-#pragma unroll
-            for (int r = 0; r < 16; ++r) S[r] = gam * S[r] + (hi[r] + lo[r]);
-            put_state();
-        }
-        fence_async_smem();
-        fence_before();
-        __syncthreads();
-    }
-    if (ok && nchunks > 0) {
-        // The last chunk's H Z product: one more commit covers it.
-        if (tid == 0) {
+        if (nchunks > 0) {
+            wait(bar_m1, p1);
             fence_after();
-            commit(bar_mma);
+            if (!zrow) put_outputs(nchunks - 1);
         }
-        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
-        mma_phase ^= 1;
-        fence_after();
-        if (ok && lr < 64) put_outputs(nchunks - 1);
-    }
-    if (!ok) {
-        if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
-        // Bounded waits for copies and MMAs that may still be in flight.
-        for (int bb = 0; bb < 2; ++bb) {
-            mbar_wait(bar_la + bb, 0);
-            mbar_wait(bar_lb + bb, 0);
+        if (final_state && !*err) {
+            *reinterpret_cast<float4 *>(final_state + st_off) = make_float4(S[0], S[1], S[2], S[3]);
+            *reinterpret_cast<float4 *>(final_state + st_off + 4) = make_float4(S[4], S[5], S[6], S[7]);
         }
-        mbar_wait(bar_mma, mma_phase);
-    } else if (final_state) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<float4 *>(final_state + st_off + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     fence_before();
     __syncthreads();
@@ -844,8 +882,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             return err;
         const long long items = slots * H;
         const unsigned grid = (unsigned)(items < sm_count ? items : sm_count);
-        tc_intra_chunk<<<grid, kP1Threads, P1::bytes, stream>>>(tq, tk, tv, tg, beta, scale, table,
-                                                                 slots, H, region, status);
+        tc_intra_chunk<<<grid, kP1Threads, P1::bytes, stream>>>(
+            tq, tk, tv, tg, beta, scale, table, seq_first_slot + num_seqs, slots, H, region, status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if ((err = mark(events, 2, stream)) != cudaSuccess) return err;

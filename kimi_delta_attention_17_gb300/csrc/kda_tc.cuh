@@ -98,6 +98,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 8 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -113,10 +123,45 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
                  "r"(bytes)
                  : "memory");
 }
+// Arrives once on mbar (no transaction bytes).
+__device__ __forceinline__ void mbar_arrive(uint64_t *mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mbar)) : "memory");
+}
+// Named barrier `id` of `nthreads` threads (whole warps): arrive without
+// waiting, or arrive and wait for the others.
+__device__ __forceinline__ void bar_arrive(int id, int nthreads) {
+    asm volatile("barrier.cta.arrive.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void bar_sync(int id, int nthreads) {
+    asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Barrier `id` over `nthreads` threads of the CTA (whole warps),
+// returning whether `pred` held in every one of them.
+__device__ __forceinline__ bool bar_and(bool pred, int id, int nthreads) {
+    uint32_t r;
+    asm volatile(
+        "{.reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.cta.red.and.aligned.pred q, %2, %3, p; "
+        "selp.u32 %0, 1, 0, q;}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 // Bounded wait for the phase with the given parity to complete. Returns false
-// if it gave up (after roughly a second or more of polling).
+// if it gave up (after roughly a second or more of polling). A phase that has
+// already completed is seen by the first, non-blocking test.
 __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
     const uint32_t a = smem_u32(mbar);
+    {
+        uint32_t done;
+        asm volatile(
+            "{.reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, "
+            "0, p;}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
     for (uint32_t it = 0; it < (1u << 22); ++it) {
         uint32_t ok;
         asm volatile(
@@ -162,6 +207,22 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 __device__ __forceinline__ uint4 pack8(const float *x) {
     return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
+}
+// Splits x0, x1 into bf16 pairs with x ~ hi + lo: hi keeps the upper 16 bits
+// of each float (truncation, one byte permute for the pair), lo = x - hi is
+// exact in fp32 and rounds once to bf16, so hi + lo carries 16 significant
+// bits (|x - hi - lo| <= 2^-16 |x|).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
+    hi = __byte_perm(u0, u1, 0x7632);
+    lo = pack2(x0 - __uint_as_float(u0 & 0xFFFF0000u), x1 - __uint_as_float(u1 & 0xFFFF0000u));
+}
+// split2 over 8 values: two 16-byte vectors (hi, lo).
+__device__ __forceinline__ void split8(const float *x, uint4 &hi, uint4 &lo) {
+    split2(x[0], x[1], hi.x, lo.x);
+    split2(x[2], x[3], hi.y, lo.y);
+    split2(x[4], x[5], hi.z, lo.z);
+    split2(x[6], x[7], hi.w, lo.w);
 }
 
 }  // namespace tc
