@@ -99,9 +99,11 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int As = am;                // fp32 [64][68]: A
     static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
     static constexpr int TBs = am + 34816;       // bf16 K-major [i][j]: T Diag(beta)
-    static constexpr int Xs = TBs + 8192;        // fp32 [3][16][16] scratch of the solve
+    static constexpr int Ms = TBs + 8192;        // fp32 [6][16][kMS]: M_IK = T_II A_IK
+    static constexpr int Rs = Ms + 6 * 16 * 20 * 4;  // fp32 [3][16][kMS]: partial sums of T_IJ
 };
-static_assert(P1::Xs + 3072 <= P1::lt, "solve scratch overlaps L^T");
+constexpr int kMS = 20;  // row stride (floats) of the M / R blocks: 8 rows hit 8 bank groups
+static_assert(P1::Rs + 3 * 16 * kMS * 4 <= P1::lt, "solve scratch overlaps L^T");
 static_assert(P1::bytes <= 232448, "phase-1 shared memory exceeds 227 KiB");
 constexpr int kAS = 68;  // row stride (floats) of A and T: 16-byte rows, 8 rows hit 8 bank groups
 
@@ -241,18 +243,22 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float Xv[4];
 #pragma unroll
             for (int I = 0; I < 4; ++I) Xv[I] = I > blk ? __expf(R[I] - Rs) : 1.f;
-#pragma unroll
+            // A runtime loop over the two 8-token groups (one copy of the body
+            // keeps the kernel within the instruction cache).
+#pragma unroll 1
             for (int ig = 0; ig < 2; ++ig) {
                 const int i0 = 16 * blk + 8 * ig;  // first token of the group
-                float kv[8], qv[8], E[8], kF[8], t8[8];
+                float kv[8], qv[8], E[8], kF[8], t8[8], Gi[8];
                 uint32_t vraw[4];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) Gi[r] = ig ? G[8 + r] : G[r];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int i = i0 + r;
                     const bool in = i < len;
                     kv[r] = in ? __bfloat162float(ks[i * D + c]) : 0.f;
                     qv[r] = in ? scale * __bfloat162float(qs[i * D + c]) : 0.f;
-                    const float x = G[8 * ig + r] - Rl;
+                    const float x = Gi[r] - Rl;
                     E[r] = __expf(x);
                     kF[r] = kv[r] * __expf(-x);
                 }
@@ -321,12 +327,14 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int grp = warp >> 2;           // which of the quadrant's four warps
             const bool upper = (warp & 1) != 0;  // rows 32-63: blocks 2, 3
             const float bi = beta_s[i];
-#pragma unroll
-            for (int vv = 0; vv < 10; ++vv) {
-                // Versions of this warp's rows (blocks 0-1: versions 0-2; blocks
-                // 2-3: versions 3-9), split among the quadrant's four warps.
-                const bool mine = upper ? (vv >= 3 && ((vv - 3) >> 1) == grp) : vv == grp;
-                if (!mine) continue;  // warp-uniform
+            // Versions of this warp's rows (blocks 0-1: versions 0-2; blocks 2-3:
+            // versions 3-9), split among the quadrant's four warps; a runtime
+            // loop keeps the code small enough for the instruction cache.
+            const int v0 = upper ? 3 + 2 * grp : grp;
+            const int nv = upper ? (grp < 3 ? 2 : 1) : (grp < 3 ? 1 : 0);
+#pragma unroll 1
+            for (int k = 0; k < nv; ++k) {
+                const int vv = v0 + k;  // warp-uniform
                 float x[16];
                 tmem_ld16(tmem + lane_base + vv * 16, x);
                 tmem_wait_ld();
@@ -378,67 +386,124 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         {
             const float *As = reinterpret_cast<const float *>(sm + P1::As);
             float *Ts = reinterpret_cast<float *>(sm + P1::Ts);
-            float *Xs = reinterpret_cast<float *>(sm + P1::Xs);
-            if (tid < 64) {
-                // Column `col` of T_II by column-oriented substitution: once x_r is
-                // final it is pushed into every later row, so the dependent chain
-                // is one FMA per row instead of a growing dot product.
-                const int I = tid >> 4, col = tid, cl = tid & 15;
-                float x[16];
+            float *Ms = reinterpret_cast<float *>(sm + P1::Ms);
+            float *Rs = reinterpret_cast<float *>(sm + P1::Rs);
+            // Diagonal blocks T_II = (I - A_II)^{-1}, column by column: four
+            // threads share a column, each owning rows sub, sub + 4, sub + 8,
+            // sub + 12. Once x_r is final its owner broadcasts it (one shuffle)
+            // and every thread pushes it into its later rows, so the dependent
+            // chain is one shuffle and one FMA per row.
+            if (tid < 256) {
+                const int I = tid >> 6, col = (tid >> 2) & 15, sub = tid & 3;
+                const float *Ab = As + 16 * I * kAS + 16 * I;
+                // This thread's rows of A_II, loaded before the dependent chain
+                // (a[q][r] = A_II[4 q + sub][r], r < 4 q + sub; the rest unused).
+                float a[4][16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) x[r] = r == cl ? 1.f : 0.f;
+                for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int r = 0; r < 15; ++r) {
-                    const float xr = r < cl ? 0.f : x[r];
-#pragma unroll
-                    for (int rr = r + 1; rr < 16; ++rr) x[rr] += As[(16 * I + rr) * kAS + 16 * I + r] * xr;
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Ts[(16 * I + r) * kAS + col] = r < cl ? 0.f : x[r];
-            }
-            __syncthreads();
-            // Off-diagonal blocks by levels L = I - J; each thread computes a
-            // 1 x 4 strip (row r, columns 4 cg .. 4 cg + 3) of X_IJ and then of
-            // T_IJ = T_II X_IJ, reading 16-byte runs of A, T and X.
-#pragma unroll
-            for (int L = 1; L <= 3; ++L) {
-                const int npairs = 4 - L;
-                const int p = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
-                const int J = p, I = J + L;
-                if (tid < npairs * 64) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int K = 0; K < L; ++K)
-#pragma unroll
-                        for (int kk = 0; kk < 16; kk += 4) {
-                            const float4 a = *reinterpret_cast<const float4 *>(
-                                As + (16 * I + r) * kAS + 16 * (J + K) + kk);
-                            const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float4 t = *reinterpret_cast<const float4 *>(
-                                    Ts + (16 * (J + K) + kk + e) * kAS + 16 * J + 4 * cg);
-                                acc.x += av[e] * t.x; acc.y += av[e] * t.y;
-                                acc.z += av[e] * t.z; acc.w += av[e] * t.w;
-                            }
-                        }
-                    *reinterpret_cast<float4 *>(Xs + p * 256 + r * 16 + 4 * cg) = acc;
-                }
-                __syncthreads();
-                if (tid < npairs * 64) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int kk = 0; kk < 16; kk += 4) {
-                        const float4 a = *reinterpret_cast<const float4 *>(Ts + (16 * I + r) * kAS + 16 * I + kk);
-                        const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 xv = *reinterpret_cast<const float4 *>(Xs + p * 256 + (kk + e) * 16 + 4 * cg);
-                            acc.x += av[e] * xv.x; acc.y += av[e] * xv.y;
-                            acc.z += av[e] * xv.z; acc.w += av[e] * xv.w;
+                    for (int r4 = 0; r4 < 16; r4 += 4) {
+                        if (r4 < 4 * q + 3) {
+                            const float4 t = *reinterpret_cast<const float4 *>(Ab + (4 * q + sub) * kAS + r4);
+                            a[q][r4] = t.x; a[q][r4 + 1] = t.y; a[q][r4 + 2] = t.z; a[q][r4 + 3] = t.w;
                         }
                     }
-                    *reinterpret_cast<float4 *>(Ts + (16 * I + r) * kAS + 16 * J + 4 * cg) = acc;
+                float x[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) x[q] = 4 * q + sub == col ? 1.f : 0.f;
+#pragma unroll
+                for (int r = 0; r < 15; ++r) {
+                    const float xr = __shfl_sync(0xffffffffu, x[r >> 2], (tid & 31 & ~3) | (r & 3));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (4 * q + 3 > r && 4 * q + sub > r) x[q] += a[q][r] * xr;
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) Ts[(16 * I + 4 * q + sub) * kAS + 16 * I + col] = x[q];
+            }
+            __syncthreads();
+            // Off-diagonal blocks: with M_IK = T_II A_IK (K < I), block row I of
+            // (I - A) T = I gives T_IJ = sum_{K = J}^{I - 1} M_IK T_KJ. Stage 1
+            // forms the six M blocks; stage 2 the first subdiagonal and the terms
+            // of the lower blocks that need only T_JJ; stages 3 and 4 finish the
+            // second and third subdiagonals. Each thread computes a 1 x 4 strip
+            // (row r, columns 4 cg .. 4 cg + 3) of one 16 x 16 product.
+            auto mi = [](int I, int K) { return I * (I - 1) / 2 + K; };  // M block index, K < I
+            // acc += P (16 x 16, row stride ps) row r  x  Q (16 x 16, row stride qs) columns 4 cg ..
+            auto prod = [](float4 acc, const float *P, int ps, const float *Q, int qs, int r, int cg) {
+#pragma unroll
+                for (int h8 = 0; h8 < 16; h8 += 8) {
+                    // Eight rows of Q and the matching eight entries of P's row,
+                    // all loaded before the FMAs that consume them.
+                    float pm[8];
+                    float4 qv[8];
+#pragma unroll
+                    for (int m0 = 0; m0 < 8; m0 += 4) {
+                        const float4 pv = *reinterpret_cast<const float4 *>(P + r * ps + h8 + m0);
+                        pm[m0] = pv.x; pm[m0 + 1] = pv.y; pm[m0 + 2] = pv.z; pm[m0 + 3] = pv.w;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        qv[e] = *reinterpret_cast<const float4 *>(Q + (h8 + e) * qs + 4 * cg);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        acc.x += pm[e] * qv[e].x; acc.y += pm[e] * qv[e].y;
+                        acc.z += pm[e] * qv[e].z; acc.w += pm[e] * qv[e].w;
+                    }
+                }
+                return acc;
+            };
+            const int pr = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;  // product index, strip
+            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            auto Tb = [&](int I, int J) { return Ts + 16 * I * kAS + 16 * J; };
+            auto Mb = [&](int I, int K) { return Ms + mi(I, K) * 16 * kMS; };
+            auto put = [](float *B, int stride, int r, int cg, float4 v) {
+                *reinterpret_cast<float4 *>(B + r * stride + 4 * cg) = v;
+            };
+            // Stage 1: M_IK for (I, K) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).
+            // Stage 2: T_10, T_21, T_32 = M_{J+1,J} T_JJ; R_20 = M_20 T_00,
+            //          R_31 = M_31 T_11, R_30 = M_30 T_00.
+            // Stage 3: T_20 = R_20 + M_21 T_10, T_31 = R_31 + M_32 T_21; R_30 += M_31 T_10.
+            // Stage 4: T_30 = R_30 + M_32 T_20.
+            // One runtime loop picks each stage's operands and expands a single
+            // product (the kernel must stay within the instruction cache).
+#pragma unroll 1
+            for (int stg = 0; stg < 4; ++stg) {
+                const int nprod = stg < 2 ? 6 : stg == 2 ? 3 : 1;
+                if (pr < nprod) {
+                    const float *P, *Q;
+                    float *dst;
+                    int ps, qs = kAS, ds;
+                    const float *init = nullptr;  // partial sum to start from (R block)
+                    if (stg == 0) {
+                        const int I = pr < 1 ? 1 : pr < 3 ? 2 : 3, K = pr - I * (I - 1) / 2;
+                        P = Tb(I, I); ps = kAS;
+                        Q = As + 16 * I * kAS + 16 * K;
+                        dst = Mb(I, K); ds = kMS;
+                    } else if (stg == 1) {
+                        const int J = pr < 3 ? pr : pr < 5 ? pr - 3 : 0;
+                        const int I = pr < 3 ? J + 1 : pr < 5 ? J + 2 : 3;
+                        P = Mb(I, J); ps = kMS;
+                        Q = Tb(J, J);
+                        dst = pr < 3 ? Tb(I, J) : Rs + (pr - 3) * 16 * kMS;
+                        ds = pr < 3 ? kAS : kMS;
+                    } else if (stg == 2) {
+                        const int J = pr < 2 ? pr : 0;
+                        const int I = pr < 2 ? J + 2 : 3, K = pr < 2 ? J + 1 : 1;
+                        P = Mb(I, K); ps = kMS;
+                        Q = Tb(K, J);
+                        init = Rs + pr * 16 * kMS;
+                        dst = pr < 2 ? Tb(I, J) : Rs + pr * 16 * kMS;
+                        ds = pr < 2 ? kAS : kMS;
+                    } else {
+                        P = Mb(3, 2); ps = kMS;
+                        Q = Tb(2, 0);
+                        init = Rs + 2 * 16 * kMS;
+                        dst = Tb(3, 0); ds = kAS;
+                    }
+                    const float4 a0 = init ? *reinterpret_cast<const float4 *>(init + r * kMS + 4 * cg) : z4;
+                    put(dst, ds, r, cg, prod(a0, P, ps, Q, qs, r, cg));
                 }
                 __syncthreads();
             }
