@@ -71,6 +71,52 @@ typedef enum {
     KDA_DTYPE_BF16 = 1 /* q, k, v, out are bf16 */
 } kda_dtype;
 
+/*
+ * The decay family, i.e. the layout of g (the pages trace it as DeltaNet ->
+ * Gated DeltaNet -> KDA: "Kimi Delta Attention: How It Works, Step by Step",
+ * section 6; "Kimi Delta Attention: a half-life per channel", "Promote the
+ * scalar to a diagonal"). A scalar decay is the per-channel one with every
+ * channel equal; no decay is a = 1.
+ */
+typedef enum {
+    KDA_DECAY_CHANNEL = 0, /* g [tokens][H][dk]: one decay per key channel (KDA) */
+    KDA_DECAY_SCALAR = 1,  /* g [tokens][H]: one decay per token and head (Gated DeltaNet) */
+    KDA_DECAY_NONE = 2     /* a_t = 1; g is not read and may be NULL (DeltaNet) */
+} kda_decay;
+
+/*
+ * How the values in g become the log-decay log a_t ("Kimi Delta Attention: a
+ * half-life per channel": a_t = sigmoid(x_t W_a); "Understanding Kimi Delta
+ * Attention", closing remarks: a negative log-decay bounded below through a
+ * sigmoid).
+ */
+typedef enum {
+    KDA_GATE_LOG = 0,        /* g holds log a_t itself (<= 0) */
+    KDA_GATE_LOGSIGMOID = 1, /* g holds logits z: a_t = sigmoid(z), log a_t = -log(1 + e^-z) */
+    KDA_GATE_BOUNDED = 2     /* g holds logits z: log a_t = gate_lower * sigmoid(z) */
+} kda_gate;
+
+/*
+ * Options of kda_chunk_fwd_opt and kda_decode_step_opt. A NULL pointer means
+ * {KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0, 0}, the behaviour of kda_chunk_fwd and
+ * kda_decode_step.
+ *  decay       layout of g (above)
+ *  gate        meaning of g's values (above); ignored with KDA_DECAY_NONE
+ *  gate_lower  KDA_GATE_BOUNDED only: the lower bound of log a_t, finite and
+ *              in [-10, 0) (log a_t then lies in (gate_lower, 0))
+ *  l2norm_qk   nonzero: q and k are L2-normalised per token and head inside
+ *              the kernel, x / sqrt(sum_c x_c^2 + 1e-6), before anything else
+ *              uses them ("Kimi Delta Attention: How It Works, Step by Step",
+ *              section 16: the key and query are normalised); the query
+ *              scale still applies after it
+ */
+typedef struct {
+    kda_decay decay;
+    kda_gate gate;
+    float gate_lower;
+    int l2norm_qk;
+} kda_options;
+
 /* Human-readable name of a status code (static storage; never NULL). */
 const char *kda_status_string(kda_status status);
 
@@ -136,6 +182,21 @@ kda_status kda_chunk_fwd_timed(const void *q, const void *k, const void *v, cons
                                cudaEvent_t *events);
 
 /*
+ * kda_chunk_fwd with options (decay family, gate transform, in-kernel q/k
+ * normalisation; see kda_options) and optional phase events (as in
+ * kda_chunk_fwd_timed; `events` may be NULL). With KDA_DECAY_SCALAR, g is
+ * [tokens][H] fp32 and 4-byte aligned; with KDA_DECAY_NONE it is not read.
+ * The workspace is the same as kda_chunk_fwd's. Invalid option values return
+ * KDA_ERR_INVALID_ARGUMENT before any CUDA call.
+ */
+kda_status kda_chunk_fwd_opt(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, float scale, const float *init_state,
+                             const int32_t *cu_seqlens, void *out, float *final_state, int B,
+                             int T, int H, int dk, int dv, int num_seqs, kda_dtype dtype,
+                             const kda_options *options, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream, cudaEvent_t *events);
+
+/*
  * Capacity, in bytes, of the scratch array kda_chunk_fwd_noalloc uses: 64 MiB.
  * A problem fits when kda_chunk_fwd_workspace_size(...) for its sizes is at
  * most this value.
@@ -186,6 +247,15 @@ kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, co
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
                            const float *beta, float scale, float *state, void *out, int N, int H,
                            int dk, int dv, kda_dtype dtype, cudaStream_t stream);
+
+/*
+ * kda_decode_step with options (see kda_options). With KDA_DECAY_SCALAR, g is
+ * [N][H] fp32 and 4-byte aligned; with KDA_DECAY_NONE it is not read.
+ */
+kda_status kda_decode_step_opt(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, float scale, float *state, void *out, int N,
+                               int H, int dk, int dv, kda_dtype dtype, const kda_options *options,
+                               cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -14,6 +14,15 @@ STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARGUMENT", 2: "KDA_ERR_UNSUPPOR
                 3: "KDA_ERR_WORKSPACE", 4: "KDA_ERR_CUDA", 5: "KDA_ERR_TIMEOUT"}
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+DECAY = {"channel": 0, "scalar": 1, "none": 2}           # kda_decay
+GATE = {"log": 0, "logsigmoid": 1, "bounded": 2}          # kda_gate
+
+
+class Options(ctypes.Structure):
+    """kda_options of include/kda.h."""
+    _fields_ = [("decay", ctypes.c_int), ("gate", ctypes.c_int), ("gate_lower", ctypes.c_float),
+                ("l2norm_qk", ctypes.c_int)]
+
 
 _vp = ctypes.c_void_p
 _SIGNATURES = {
@@ -27,6 +36,10 @@ _SIGNATURES = {
                               + [ctypes.c_int] * 7 + [_vp], ctypes.c_int),
     "kda_decode_step": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]
                         + [ctypes.c_int] * 5 + [_vp], ctypes.c_int),
+    "kda_chunk_fwd_opt": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
+                          + [ctypes.c_int] * 7 + [_vp, _vp, ctypes.c_size_t, _vp, _vp], ctypes.c_int),
+    "kda_decode_step_opt": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]
+                            + [ctypes.c_int] * 5 + [_vp, _vp], ctypes.c_int),
 }
 
 _lib = None

@@ -126,11 +126,38 @@ extern "C" size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int 
 
 namespace {
 
+// Checks kda_options and turns them into the kernels' Prologue (NULL: the
+// defaults of kda_chunk_fwd / kda_decode_step).
+bool make_prologue(const kda_options *o, Prologue *p) {
+    *p = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0.f, 0};
+    if (!o) return true;
+    if (o->decay != KDA_DECAY_CHANNEL && o->decay != KDA_DECAY_SCALAR && o->decay != KDA_DECAY_NONE)
+        return false;
+    if (o->gate != KDA_GATE_LOG && o->gate != KDA_GATE_LOGSIGMOID && o->gate != KDA_GATE_BOUNDED)
+        return false;
+    if (o->gate == KDA_GATE_BOUNDED && !(o->gate_lower >= -10.f && o->gate_lower < 0.f)) return false;
+    *p = Prologue{(int)o->decay, (int)o->gate, o->gate == KDA_GATE_BOUNDED ? o->gate_lower : 0.f,
+                  o->l2norm_qk ? 1 : 0};
+    return true;
+}
+
+// g is required unless there is no decay; per-channel g is 16-byte aligned,
+// per-head g 4-byte aligned.
+bool g_ok(const float *g, const Prologue &p, bool required) {
+    if (p.decay == KDA_DECAY_NONE) return true;
+    if (required && !g) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(g);
+    return (a & (p.decay == KDA_DECAY_CHANNEL ? 15u : 3u)) == 0;
+}
+
 kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float scale, const float *init_state,
                           const int32_t *cu_seqlens, void *out, float *final_state, int B, int T,
-                          int H, int dk, int dv, int num_seqs, kda_dtype dtype, void *workspace,
-                          size_t workspace_bytes, cudaStream_t stream, cudaEvent_t *events) {
+                          int H, int dk, int dv, int num_seqs, kda_dtype dtype,
+                          const kda_options *options, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream, cudaEvent_t *events) {
+    Prologue pro;
+    if (!make_prologue(options, &pro)) return KDA_ERR_INVALID_ARGUMENT;
     if (dtype != KDA_DTYPE_F32 && dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARGUMENT;
     if (B <= 0 || T < 0 || H <= 0 || dk <= 0 || dv <= 0 || num_seqs <= 0)
         return KDA_ERR_INVALID_ARGUMENT;
@@ -139,8 +166,9 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if ((long long)B * T * H * (dk > dv ? dk : dv) >= (1LL << 40)) return KDA_ERR_INVALID_ARGUMENT;
     if ((long long)B * T >= (1LL << 31) - kChunk) return KDA_ERR_INVALID_ARGUMENT;
     const bool have_tokens = (long long)B * T > 0;
-    if (have_tokens && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(out) ||
+    if (have_tokens && (!q || !k || !v || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!g_ok(g, pro, have_tokens)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
         !aligned16(init_state) || !aligned16(final_state))
         return KDA_ERR_INVALID_ARGUMENT;
     if ((reinterpret_cast<uintptr_t>(beta) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
@@ -169,11 +197,12 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if (use_tc(dk, dtype))
         err = launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
                                 T_fixed, (long long)B * T, H, num_seqs, slots, table, seq_first_slot,
-                                reinterpret_cast<unsigned char *>(region), status, stream, events);
+                                reinterpret_cast<unsigned char *>(region), status, pro, stream,
+                                events);
     else
         err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
                                   final_state, T_fixed, H, dk, num_seqs, dtype, slots, table,
-                                  seq_first_slot, reinterpret_cast<float *>(region), stream,
+                                  seq_first_slot, reinterpret_cast<float *>(region), pro, stream,
                                   events);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -187,7 +216,8 @@ extern "C" kda_status kda_chunk_fwd(const void *q, const void *k, const void *v,
                                     kda_dtype dtype, void *workspace, size_t workspace_bytes,
                                     cudaStream_t stream) {
     return chunk_fwd_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B, T,
-                          H, dk, dv, num_seqs, dtype, workspace, workspace_bytes, stream, nullptr);
+                          H, dk, dv, num_seqs, dtype, nullptr, workspace, workspace_bytes, stream,
+                          nullptr);
 }
 
 extern "C" kda_status kda_chunk_fwd_timed(const void *q, const void *k, const void *v,
@@ -198,23 +228,59 @@ extern "C" kda_status kda_chunk_fwd_timed(const void *q, const void *k, const vo
                                           void *workspace, size_t workspace_bytes,
                                           cudaStream_t stream, cudaEvent_t *events) {
     return chunk_fwd_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B, T,
-                          H, dk, dv, num_seqs, dtype, workspace, workspace_bytes, stream, events);
+                          H, dk, dv, num_seqs, dtype, nullptr, workspace, workspace_bytes, stream,
+                          events);
 }
+
+extern "C" kda_status kda_chunk_fwd_opt(const void *q, const void *k, const void *v,
+                                        const float *g, const float *beta, float scale,
+                                        const float *init_state, const int32_t *cu_seqlens,
+                                        void *out, float *final_state, int B, int T, int H, int dk,
+                                        int dv, int num_seqs, kda_dtype dtype,
+                                        const kda_options *options, void *workspace,
+                                        size_t workspace_bytes, cudaStream_t stream,
+                                        cudaEvent_t *events) {
+    return chunk_fwd_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B, T,
+                          H, dk, dv, num_seqs, dtype, options, workspace, workspace_bytes, stream,
+                          events);
+}
+
+namespace {
+
+kda_status decode_impl(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, float scale, float *state, void *out, int N, int H,
+                       int dk, int dv, kda_dtype dtype, const kda_options *options,
+                       cudaStream_t stream) {
+    Prologue pro;
+    if (!make_prologue(options, &pro)) return KDA_ERR_INVALID_ARGUMENT;
+    if (dtype != KDA_DTYPE_F32 && dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!isfinite(scale)) return KDA_ERR_INVALID_ARGUMENT;
+    if ((long long)N * H >= (1LL << 31)) return KDA_ERR_INVALID_ARGUMENT;
+    if (N > 0 && (!q || !k || !v || !beta || !state || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!g_ok(g, pro, N > 0)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(state) || !aligned16(out))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(beta) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (!dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    const cudaError_t err =
+        launch_decode(q, k, v, g, beta, scale, state, out, N, H, dk, dtype, pro, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
 
 extern "C" kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
                                       const float *beta, float scale, float *state, void *out,
                                       int N, int H, int dk, int dv, kda_dtype dtype,
                                       cudaStream_t stream) {
-    if (dtype != KDA_DTYPE_F32 && dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARGUMENT;
-    if (N < 0 || H <= 0 || dk <= 0 || dv <= 0) return KDA_ERR_INVALID_ARGUMENT;
-    if (!isfinite(scale)) return KDA_ERR_INVALID_ARGUMENT;
-    if ((long long)N * H >= (1LL << 31)) return KDA_ERR_INVALID_ARGUMENT;
-    if (N > 0 && (!q || !k || !v || !g || !beta || !state || !out)) return KDA_ERR_INVALID_ARGUMENT;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(state) ||
-        !aligned16(out))
-        return KDA_ERR_INVALID_ARGUMENT;
-    if ((reinterpret_cast<uintptr_t>(beta) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
-    if (!dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
-    const cudaError_t err = launch_decode(q, k, v, g, beta, scale, state, out, N, H, dk, dtype, stream);
-    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return decode_impl(q, k, v, g, beta, scale, state, out, N, H, dk, dv, dtype, nullptr, stream);
+}
+
+extern "C" kda_status kda_decode_step_opt(const void *q, const void *k, const void *v,
+                                          const float *g, const float *beta, float scale,
+                                          float *state, void *out, int N, int H, int dk, int dv,
+                                          kda_dtype dtype, const kda_options *options,
+                                          cudaStream_t stream) {
+    return decode_impl(q, k, v, g, beta, scale, state, out, N, H, dk, dv, dtype, options, stream);
 }

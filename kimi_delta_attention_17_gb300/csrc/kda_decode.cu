@@ -21,11 +21,13 @@ namespace {
 constexpr int kDecodeThreads = 128;
 constexpr int kSlab = 32;  // state columns per CTA
 
-template <int D, typename InT>
+// kOpts = false is the plain step (per-channel log-decay in g, no
+// normalisation), compiled without the option branches.
+template <int D, typename InT, bool kOpts>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_step_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT *__restrict__ v,
                    const float *__restrict__ g, const float *__restrict__ beta, float scale,
-                   float *__restrict__ state, InT *__restrict__ out) {
+                   float *__restrict__ state, InT *__restrict__ out, Prologue pro) {
     constexpr int R = D / 16;  // rows per thread
     const int nh = blockIdx.x;           // (sequence, head) flattened
     const int col0 = blockIdx.y * kSlab;  // first state column of this slab
@@ -40,19 +42,29 @@ decode_step_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const I
         s[m] = *reinterpret_cast<const float4 *>(S + (size_t)(rg + 16 * m) * D);
 
     const size_t tok = (size_t)nh * D;
+    // Decay of this head: per channel, one per head, or none (log a = 0).
+    const float gh = kOpts && pro.decay == KDA_DECAY_SCALAR ? log_decay(g[nh], pro) : 0.f;
     float av[R], ak[R], aq[R], kr[R];
-    float qk = 0.f;
+    float qk = 0.f, kss = 0.f, qss = 0.f;  // q.k and the squared norms of raw k and q
 #pragma unroll
     for (int m = 0; m < R; ++m) {
         const int r = rg + 16 * m;
-        const float a = expf(g[tok + r]);
+        const float a = !kOpts ? expf(g[tok + r])
+                        : pro.decay == KDA_DECAY_CHANNEL ? expf(log_decay(g[tok + r], pro))
+                        : pro.decay == KDA_DECAY_SCALAR  ? expf(gh)
+                                                         : 1.f;
         const float kk = to_f32(k[tok + r]);
-        const float qq = scale * to_f32(q[tok + r]);
+        const float q0 = to_f32(q[tok + r]);
+        const float qq = scale * q0;
         av[m] = a;
         kr[m] = kk;
         ak[m] = a * kk;
         aq[m] = a * qq;
         qk += qq * kk;
+        if (kOpts) {
+            kss += kk * kk;
+            qss += q0 * q0;
+        }
     }
     float4 vh = make_float4(0.f, 0.f, 0.f, 0.f), po = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -72,20 +84,42 @@ decode_step_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const I
         po.z += __shfl_xor_sync(0xffffffffu, po.z, off);
         po.w += __shfl_xor_sync(0xffffffffu, po.w, off);
         qk += __shfl_xor_sync(0xffffffffu, qk, off);
+        if (kOpts) {
+            kss += __shfl_xor_sync(0xffffffffu, kss, off);
+            qss += __shfl_xor_sync(0xffffffffu, qss, off);
+        }
     }
     // ... then over the 4 warps.
-    __shared__ float red[4][8][9];
+    constexpr int NR = kOpts ? 11 : 9;  // reduced values per column quad
+    __shared__ float red[4][8][NR];
     const int warp = tid >> 5, lane = tid & 31;
     if (lane < 8) {
         float *r = red[warp][lane];
         r[0] = vh.x; r[1] = vh.y; r[2] = vh.z; r[3] = vh.w;
         r[4] = po.x; r[5] = po.y; r[6] = po.z; r[7] = po.w;
         r[8] = qk;
+        if (kOpts) {
+            r[NR - 2] = kss;
+            r[NR - 1] = qss;
+        }
     }
     __syncthreads();
-    float tot[9];
+    float tot[NR];
 #pragma unroll
-    for (int i = 0; i < 9; ++i) tot[i] = red[0][cq][i] + red[1][cq][i] + red[2][cq][i] + red[3][cq][i];
+    for (int i = 0; i < NR; ++i) tot[i] = red[0][cq][i] + red[1][cq][i] + red[2][cq][i] + red[3][cq][i];
+    if (kOpts && pro.l2norm) {
+        // The reads are linear in k and q: normalising afterwards scales vhat by
+        // 1/|k|, the decayed query read by 1/|q|, q.k by both, and the write by 1/|k|.
+        const float rk = rsqrtf(tot[NR - 2] + kL2Eps), rq = rsqrtf(tot[NR - 1] + kL2Eps);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            tot[i] *= rk;
+            tot[4 + i] *= rq;
+        }
+        tot[8] *= rk * rq;
+#pragma unroll
+        for (int m = 0; m < R; ++m) kr[m] *= rk;
+    }
 
     const float b = beta[nh];
     const size_t vo = (size_t)nh * D + col0 + 4 * cq;
@@ -114,11 +148,17 @@ decode_step_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const I
 template <int D, typename InT>
 cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const float *g,
                             const float *beta, float scale, float *state, void *out, int N, int H,
-                            cudaStream_t stream) {
+                            const Prologue &pro, cudaStream_t stream) {
     dim3 grid((unsigned)(N * H), D / kSlab);
-    decode_step_kernel<D, InT><<<grid, kDecodeThreads, 0, stream>>>(
-        static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g,
-        beta, scale, state, static_cast<InT *>(out));
+    const bool plain = pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOG && !pro.l2norm;
+    if (plain)
+        decode_step_kernel<D, InT, false><<<grid, kDecodeThreads, 0, stream>>>(
+            static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g,
+            beta, scale, state, static_cast<InT *>(out), pro);
+    else
+        decode_step_kernel<D, InT, true><<<grid, kDecodeThreads, 0, stream>>>(
+            static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g,
+            beta, scale, state, static_cast<InT *>(out), pro);
     return cudaGetLastError();
 }
 
@@ -126,14 +166,14 @@ cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const f
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float scale, float *state, void *out, int N, int H,
-                          int d, kda_dtype dtype, cudaStream_t stream) {
+                          int d, kda_dtype dtype, const Prologue &pro, cudaStream_t stream) {
     if (N == 0) return cudaSuccess;
     if (dtype == KDA_DTYPE_BF16) {
-        return d == 128 ? launch_decode_t<128, __nv_bfloat16>(q, k, v, g, beta, scale, state, out, N, H, stream)
-                        : launch_decode_t<64, __nv_bfloat16>(q, k, v, g, beta, scale, state, out, N, H, stream);
+        return d == 128 ? launch_decode_t<128, __nv_bfloat16>(q, k, v, g, beta, scale, state, out, N, H, pro, stream)
+                        : launch_decode_t<64, __nv_bfloat16>(q, k, v, g, beta, scale, state, out, N, H, pro, stream);
     }
-    return d == 128 ? launch_decode_t<128, float>(q, k, v, g, beta, scale, state, out, N, H, stream)
-                    : launch_decode_t<64, float>(q, k, v, g, beta, scale, state, out, N, H, stream);
+    return d == 128 ? launch_decode_t<128, float>(q, k, v, g, beta, scale, state, out, N, H, pro, stream)
+                    : launch_decode_t<64, float>(q, k, v, g, beta, scale, state, out, N, H, pro, stream);
 }
 
 }  // namespace kda

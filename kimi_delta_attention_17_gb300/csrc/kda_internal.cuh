@@ -47,6 +47,23 @@ inline size_t table_bytes(long long slots, int num_seqs) {
            align_up((size_t)(num_seqs + 1) * sizeof(int), 256);
 }
 
+// Validated kda_options, passed to the kernels by value.
+struct Prologue {
+    int decay;    // kda_decay: layout of g
+    int gate;     // kda_gate: meaning of g's values
+    float lower;  // KDA_GATE_BOUNDED: lower bound of log a
+    int l2norm;   // normalise q and k per (token, head)
+};
+constexpr float kL2Eps = 1e-6f;  // x / sqrt(sum x^2 + kL2Eps)
+
+// log a from a value of g under the gate transform (KDA_DECAY_NONE never calls
+// this). log sigmoid(z) = min(z, 0) - log(1 + e^-|z|) avoids overflow.
+__device__ __forceinline__ float log_decay(float z, const Prologue &p) {
+    if (p.gate == KDA_GATE_LOGSIGMOID) return fminf(z, 0.f) - log1pf(__expf(-fabsf(z)));
+    if (p.gate == KDA_GATE_BOUNDED) return p.lower / (1.f + __expf(-z));
+    return z;
+}
+
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
@@ -72,8 +89,8 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 const int32_t *cu_seqlens, void *out, float *final_state,
                                 int T_fixed, int H, int d, int num_seqs, kda_dtype dtype,
                                 long long slots, const ChunkEntry *table,
-                                const int *seq_first_slot, float *region, cudaStream_t stream,
-                                cudaEvent_t *events);
+                                const int *seq_first_slot, float *region, const Prologue &pro,
+                                cudaStream_t stream, cudaEvent_t *events);
 
 // Tensor-core prefill (bf16 storage, d = 128).
 size_t tc_region_bytes();
@@ -82,8 +99,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const int32_t *cu_seqlens, void *out, float *final_state,
                               int T_fixed, long long tokens, int H, int num_seqs, long long slots,
                               const ChunkEntry *table, const int *seq_first_slot,
-                              unsigned char *region, int *status, cudaStream_t stream,
-                              cudaEvent_t *events);
+                              unsigned char *region, int *status, const Prologue &pro,
+                              cudaStream_t stream, cudaEvent_t *events);
 
 // Records events[i] (when non-NULL) on the stream: the prefill marks the
 // start (0), the end of the chunk table (1), of the intra-chunk phase (2) and
@@ -95,6 +112,6 @@ inline cudaError_t mark(cudaEvent_t *events, int i, cudaStream_t stream) {
 // Decode step.
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float scale, float *state, void *out, int N, int H,
-                          int d, kda_dtype dtype, cudaStream_t stream);
+                          int d, kda_dtype dtype, const Prologue &pro, cudaStream_t stream);
 
 }  // namespace kda

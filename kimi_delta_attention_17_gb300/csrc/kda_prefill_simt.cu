@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kThreads)
 simt_chunk_prep(const InT *__restrict__ q, const InT *__restrict__ k, const InT *__restrict__ v,
                 const float *__restrict__ g, const float *__restrict__ beta, float scale,
                 const ChunkEntry *__restrict__ table, long long nslots, int H,
-                float *__restrict__ ws) {
+                float *__restrict__ ws, Prologue pro) {
     constexpr int P = D + 1;  // padded row stride
     const int h = blockIdx.x;  // heads fastest: resident CTAs read whole token rows
     const long long slot = (long long)blockIdx.z * gridDim.y + blockIdx.y;
@@ -81,10 +81,13 @@ simt_chunk_prep(const InT *__restrict__ q, const InT *__restrict__ k, const InT 
         const int i = idx / D, c = idx % D;
         float kv = 0.f, qv = 0.f, gv = 0.f, vv = 0.f;
         if (i < ce.len) {
-            const size_t off = ((size_t)(ce.bos + i) * H + h) * D + c;
+            const size_t tok = (size_t)(ce.bos + i) * H + h;
+            const size_t off = tok * D + c;
             kv = to_f32(k[off]);
-            qv = scale * to_f32(q[off]);
-            gv = g[off];
+            qv = to_f32(q[off]);  // scaled below, after any normalisation
+            // log a_t per channel, one per head (broadcast), or none.
+            if (pro.decay == KDA_DECAY_CHANNEL) gv = log_decay(g[off], pro);
+            else if (pro.decay == KDA_DECAY_SCALAR) gv = log_decay(g[tok], pro);
             vv = to_f32(v[off]);
         }
         ks[i * P + c] = kv;
@@ -93,6 +96,21 @@ simt_chunk_prep(const InT *__restrict__ q, const InT *__restrict__ k, const InT 
         vs[i * P + c] = vv;
     }
     if (tid < kChunk) bs[tid] = tid < ce.len ? beta[(size_t)(ce.bos + tid) * H + h] : 0.f;
+    __syncthreads();
+    // q (and, when asked, q and k normalised per token): row r of k or q by
+    // one thread, x / sqrt(sum x^2 + eps), then the query scale.
+    if (tid < 2 * kChunk) {
+        const int r = tid & (kChunk - 1);
+        float *row = (tid < kChunk ? ks : qs) + r * P;
+        float f = tid < kChunk ? 1.f : scale;
+        if (pro.l2norm) {
+            float ss = 0.f;
+            for (int c = 0; c < D; ++c) ss += row[c] * row[c];
+            f *= rsqrtf(ss + kL2Eps);
+        }
+        if (f != 1.f)
+            for (int c = 0; c < D; ++c) row[c] *= f;
+    }
     __syncthreads();
 
     // In-chunk cumulative log-decay, one thread per key channel.
@@ -274,8 +292,8 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
                      const float *beta, float scale, const float *init_state,
                      const int32_t *cu_seqlens, void *out, float *final_state, int T_fixed, int H,
                      int num_seqs, long long slots, const ChunkEntry *table,
-                     const int *seq_first_slot, float *region, cudaStream_t stream,
-                     cudaEvent_t *events) {
+                     const int *seq_first_slot, float *region, const Prologue &pro,
+                     cudaStream_t stream, cudaEvent_t *events) {
     constexpr size_t s1 = prep_smem_bytes<D>();
     constexpr size_t s2 = pass_smem_bytes<D>();
     cudaError_t err = cudaFuncSetAttribute(simt_chunk_prep<D, InT>,
@@ -288,7 +306,7 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
     if (slots > 0) {
         simt_chunk_prep<D, InT><<<head_slot_grid(H, slots), kThreads, s1, stream>>>(
             static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g,
-            beta, scale, table, slots, H, region);
+            beta, scale, table, slots, H, region, pro);
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
@@ -314,10 +332,10 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 const int32_t *cu_seqlens, void *out, float *final_state,
                                 int T_fixed, int H, int d, int num_seqs, kda_dtype dtype,
                                 long long slots, const ChunkEntry *table,
-                                const int *seq_first_slot, float *region, cudaStream_t stream,
-                                cudaEvent_t *events) {
+                                const int *seq_first_slot, float *region, const Prologue &pro,
+                                cudaStream_t stream, cudaEvent_t *events) {
 #define KDA_SIMT_ARGS q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, T_fixed, H, \
-                      num_seqs, slots, table, seq_first_slot, region, stream, events
+                      num_seqs, slots, table, seq_first_slot, region, pro, stream, events
     if (dtype == KDA_DTYPE_BF16)
         return d == 128 ? launch_t<128, __nv_bfloat16>(KDA_SIMT_ARGS)
                         : launch_t<64, __nv_bfloat16>(KDA_SIMT_ARGS);

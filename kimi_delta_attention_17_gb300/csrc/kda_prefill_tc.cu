@@ -37,6 +37,7 @@
 // thread per key channel writes 16-byte runs along the token axis (MN-major
 // tiles when the contraction runs over channels, K-major when it runs over
 // tokens). Accumulators are read back with tcgen05.ld (thread t = TMEM lane t).
+#include <cstring>
 #include <cuda.h>  // CUtensorMap (the encoder is fetched at run time; no libcuda link)
 
 #include "kda_internal.cuh"
@@ -94,7 +95,9 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int bar = 188672;  // mbarriers: staging loaded, MMA done
     static constexpr int tmem = 188688;
     static constexpr int exch = 188704; // fp32 [2][4][128]: block totals and local references of G
-    static constexpr int bytes = 192800;
+    static constexpr int gsc = 192800;  // fp32 [64]: per-head log-decay of the item's tokens
+    static constexpr int nrm = 193056;  // fp32 [2 parities][2 (k, q)][64]: squared norms of k and q
+    static constexpr int bytes = 194080;
     // Reused once the first MMA has consumed am / bm:
     static constexpr int As = am;                // fp32 [64][68]: A
     static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
@@ -115,9 +118,32 @@ __device__ __forceinline__ void st16(unsigned char *p, const float *x) {
     *reinterpret_cast<uint4 *>(p) = pack8(x);
 }
 
+// Sums v[0..15] (one value per token) over the warp's 32 lanes by halving
+// exchanges (16 shuffles in all); lane l ends with the total of token
+// 8 b4 + 4 b3 + 2 b2 + b1, b_i the bits of l (lanes l and l ^ 1 agree).
+__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
+    float w[8], x[4], y[2];
+    const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        w[j] = (u16 ? v[8 + j] : v[j]) + __shfl_xor_sync(0xffffffffu, u16 ? v[j] : v[8 + j], 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        x[j] = (u8 ? w[4 + j] : w[j]) + __shfl_xor_sync(0xffffffffu, u8 ? w[j] : w[4 + j], 8);
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        y[j] = (u4 ? x[2 + j] : x[j]) + __shfl_xor_sync(0xffffffffu, u4 ? x[j] : x[2 + j], 4);
+    float z = (u2 ? y[1] : y[0]) + __shfl_xor_sync(0xffffffffu, u2 ? y[0] : y[1], 2);
+    return z + __shfl_xor_sync(0xffffffffu, z, 1);
+}
+
+// kOpts = false: per-channel log-decay in g and no normalisation, compiled
+// without the option code (the kernel must stay within the instruction cache).
+template <bool kOpts>
 __global__ void __launch_bounds__(kP1Threads, 1)
 tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+               const float *__restrict__ g_head, Prologue pro,
                const float *__restrict__ beta, float scale, const ChunkEntry *__restrict__ table,
                const int *__restrict__ used_slots, long long nslots, int H,
                unsigned char *__restrict__ ws, int *__restrict__ status) {
@@ -158,13 +184,15 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // One thread fetches an item: four 3-D TMA tiles (128 channels x 1 head x
     // 64 tokens) land as dense [token][channel] rows. Tokens past the end of
     // the tensor read as zeros; tokens of the next sequence are masked by len.
+    if (!kOpts) pro = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0.f, 0};
+    const bool g_tile = pro.decay == KDA_DECAY_CHANNEL;  // g arrives as a tile only per channel
     auto issue = [&](int hh, const ChunkEntry e) {
         if (tid != 0) return;
-        mbar_expect_tx(bar_ld, 64u * (3u * 256u + 512u));
+        mbar_expect_tx(bar_ld, 64u * (3u * 256u + (g_tile ? 512u : 0u)));
         tma_load_3d(sm + P1::q, &tm_q, 0, hh, e.bos, bar_ld);
         tma_load_3d(sm + P1::k, &tm_k, 0, hh, e.bos, bar_ld);
         tma_load_3d(sm + P1::v, &tm_v, 0, hh, e.bos, bar_ld);
-        tma_load_3d(sm + P1::g, &tm_g, 0, hh, e.bos, bar_ld);
+        if (g_tile) tma_load_3d(sm + P1::g, &tm_g, 0, hh, e.bos, bar_ld);
     };
 
     // Each item's table entry and beta values are read one item ahead, so
@@ -172,6 +200,15 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto beta_of = [&](int hh, const ChunkEntry &e) {
         return tid < C && tid < e.len ? beta[(size_t)(e.bos + tid) * H + hh] : 0.f;
     };
+    // The per-head decay value of token tid (Gated DeltaNet form), read the
+    // same way; it becomes log a (log_decay) when it is stored for its item.
+    auto ghead_of = [&](int hh, const ChunkEntry &e) {
+        return pro.decay == KDA_DECAY_SCALAR && tid < C && tid < e.len
+                   ? g_head[(size_t)(e.bos + tid) * H + hh]
+                   : 0.f;
+    };
+    float *nrm_s = reinterpret_cast<float *>(sm + P1::nrm);
+    if (pro.l2norm && tid < 2 * C) nrm_s[tid] = 0.f;  // the first item's norm accumulators
     int sl = (int)(blockIdx.x / H), hc = (int)(blockIdx.x % H);  // this item
     ChunkEntry ce{};
     float bcur = 0.f;
@@ -179,17 +216,22 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ce = table[sl];
         issue(hc, ce);
         bcur = beta_of(hc, ce);
+        if (pro.decay == KDA_DECAY_SCALAR && tid < C)
+            reinterpret_cast<float *>(sm + P1::gsc)[tid] =
+                tid < ce.len ? log_decay(ghead_of(hc, ce), pro) : 0.f;
     }
     int sn = sl, hn = hc;  // the next item
     advance(sn, hn);
     ChunkEntry en = sn < used ? table[sn] : ce;
     uint32_t ld_phase = 0, mma_phase = 0;
     bool ok = true;
+    int it_par = 0;
     while (sl < used) {
         const int len = ce.len;
         int snn = sn, hnn = hn;  // the item after next
         ChunkEntry enn;
-        float bn;
+        float bn, gn;
+        const int par = it_par;  // parity of this item's norm accumulators
         unsigned char *reg = ws + ((size_t)sl * H + hc) * TcRegion::bytes;
         ok = __syncthreads_and(mbar_wait(bar_ld, ld_phase));
         ld_phase ^= 1;
@@ -207,26 +249,64 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // thread has the absolute references R_I = G_{16 I + 7} and the chunk
             // total. In-block factors need only the local prefixes (the block's
             // offset cancels in G_i - G_r).
+            float *gsc_s = reinterpret_cast<float *>(sm + P1::gsc);  // written one item ahead
             float G[16];
             float acc = 0.f;
+            if (pro.decay == KDA_DECAY_CHANNEL) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const int tok = 16 * blk + t;
-                acc += tok < len ? gs[tok * D + c] : 0.f;
-                G[t] = acc;
+                for (int t = 0; t < 16; ++t) {
+                    const int tok = 16 * blk + t;
+                    acc += tok < len ? log_decay(gs[tok * D + c], pro) : 0.f;
+                    G[t] = acc;
+                }
+            } else {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) G[t] = 0.f;
             }
             float *tot_s = reinterpret_cast<float *>(sm + P1::exch);
             float *ref_s = tot_s + 4 * D;
+            if (pro.l2norm) {
+                // Squared norms of this block's tokens of k and q: each warp sums
+                // its 32 channels with a transposing shuffle reduction, then the
+                // four warps of the block add into shared memory.
+                const int lane = tid & 31;
+                const int tok_l = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) +
+                                  ((lane >> 1) & 1);
+#pragma unroll
+                for (int tsr = 0; tsr < 2; ++tsr) {
+                    const __nv_bfloat16 *xs = tsr ? qs : ks;
+                    float v16[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int tok = 16 * blk + t;
+                        const float x = tok < len ? __bfloat162float(xs[tok * D + c]) : 0.f;
+                        v16[t] = x * x;
+                    }
+                    const float tot = warp_sum16(v16, lane);
+                    if ((lane & 1) == 0) atomicAdd(nrm_s + par * 2 * C + tsr * C + 16 * blk + tok_l, tot);
+                }
+            }
+            if (tid < C) beta_s[tid] = bcur;
+            if (pro.decay == KDA_DECAY_SCALAR) {
+                // One decay per head: every channel's prefix is the same.
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    acc += gsc_s[16 * blk + t];
+                    G[t] = acc;
+                }
+            }
             tot_s[blk * D + c] = acc;
             ref_s[blk * D + c] = G[7];
-            if (tid < C) beta_s[tid] = bcur;
             __syncthreads();
+            // The other parity's accumulators, cleared for the next item.
+            if (pro.l2norm && tid < 2 * C) nrm_s[(par ^ 1) * 2 * C + tid] = 0.f;
             // The table entry of the item after next and the next item's beta,
             // read here: a CTA barrier waits for its threads' loads, and the next
             // one is the whole elementwise pass away.
             advance(snn, hnn);
             enn = snn < used ? table[snn] : en;
             bn = sn < used ? beta_of(hn, en) : 0.f;
+            gn = sn < used ? ghead_of(hn, en) : 0.f;
             float R[4], off = 0.f;
 #pragma unroll
             for (int I = 0; I < 4; ++I) {
@@ -256,8 +336,13 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int r = 0; r < 8; ++r) {
                     const int i = i0 + r;
                     const bool in = i < len;
-                    kv[r] = in ? __bfloat162float(ks[i * D + c]) : 0.f;
-                    qv[r] = in ? scale * __bfloat162float(qs[i * D + c]) : 0.f;
+                    float fk = 1.f, fq = scale;
+                    if (pro.l2norm) {
+                        fk = rsqrtf(nrm_s[par * 2 * C + i] + kL2Eps);
+                        fq = scale * rsqrtf(nrm_s[par * 2 * C + C + i] + kL2Eps);
+                    }
+                    kv[r] = in ? fk * __bfloat162float(ks[i * D + c]) : 0.f;
+                    qv[r] = in ? fq * __bfloat162float(qs[i * D + c]) : 0.f;
                     const float x = Gi[r] - Rl;
                     E[r] = __expf(x);
                     kF[r] = kv[r] * __expf(-x);
@@ -564,6 +649,11 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             }
         }
+        // The next item's per-head log-decays (this item read its own before
+        // its exchange barrier; the next item's load barrier orders these).
+        if (pro.decay == KDA_DECAY_SCALAR && tid < C)
+            reinterpret_cast<float *>(sm + P1::gsc)[tid] =
+                sn < used && tid < en.len ? log_decay(gn, pro) : 0.f;
         fence_before();
         __syncthreads();
         fence_after();
@@ -574,6 +664,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         hn = hnn;
         en = enn;
         bcur = bn;
+        it_par ^= 1;
     }
     if (!ok) {
         if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
@@ -664,6 +755,13 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     auto wait = [&](uint64_t *bar, uint32_t parity) {
         if (*err) return;
         if (!mbar_wait(bar, parity)) {
+            *err = 1;
+            atomicExch(status, (int)KDA_ERR_TIMEOUT);
+        }
+    };
+    auto spin = [&](uint64_t *bar, uint32_t parity) {  // the same, polling
+        if (*err) return;
+        if (!mbar_spin(bar, parity)) {
             *err = 1;
             atomicExch(status, (int)KDA_ERR_TIMEOUT);
         }
@@ -803,7 +901,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             // The tiles landed long ago (the first product used them); this
             // thread's own wait makes the copied U and gamma visible to it.
             wait(bar_ld + b, (uint32_t)(ch / kP2Bufs) & 1);
-            wait(bar_m1, p1);
+            spin(bar_m1, p1);
             p1 ^= 1;
             fence_after();
             if (zrow) {
@@ -831,7 +929,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             fence_before();
             bar_arrive(kBarZ, kP2Sync);
             const float gam = reinterpret_cast<const float *>(buf + kBufGam)[r];
-            wait(bar_m2, p2);
+            spin(bar_m2, p2);
             p2 ^= 1;
             fence_after();
             {
@@ -915,8 +1013,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const int32_t *cu_seqlens, void *out, float *final_state,
                               int T_fixed, long long tokens, int H, int num_seqs, long long slots,
                               const ChunkEntry *table, const int *seq_first_slot,
-                              unsigned char *region, int *status, cudaStream_t stream,
-                              cudaEvent_t *events) {
+                              unsigned char *region, int *status, const Prologue &pro,
+                              cudaStream_t stream, cudaEvent_t *events) {
     // Per device, once: the SM count (phase 1 runs one persistent CTA per SM)
     // and the dynamic shared-memory opt-ins. Repeating this is idempotent.
     static int sm_counts[64];
@@ -928,8 +1026,12 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         int n = 0;
         if ((err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return err;
-        if ((err = cudaFuncSetAttribute(tc_intra_chunk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        P1::bytes)) != cudaSuccess)
+        if ((err = cudaFuncSetAttribute(tc_intra_chunk<false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
+                cudaSuccess ||
+            (err = cudaFuncSetAttribute(tc_intra_chunk<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
+                cudaSuccess)
             return err;
         if ((err = cudaFuncSetAttribute(tc_state_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kP2Smem)) != cudaSuccess)
@@ -940,15 +1042,25 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     if ((err = mark(events, 1, stream)) != cudaSuccess) return err;
     if (slots > 0 && tokens > 0) {
         CUtensorMap tq, tk, tv, tg;
+        memset(&tg, 0, sizeof(tg));  // read only with a per-channel g
         if ((err = token_rows_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
             (err = token_rows_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
-            (err = token_rows_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
+            (err = token_rows_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess)
+            return err;
+        if (pro.decay == KDA_DECAY_CHANNEL &&
             (err = token_rows_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tokens)) != cudaSuccess)
             return err;
         const long long items = slots * H;
         const unsigned grid = (unsigned)(items < sm_count ? items : sm_count);
-        tc_intra_chunk<<<grid, kP1Threads, P1::bytes, stream>>>(
-            tq, tk, tv, tg, beta, scale, table, seq_first_slot + num_seqs, slots, H, region, status);
+        const bool plain = pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOG && !pro.l2norm;
+        if (plain)
+            tc_intra_chunk<false><<<grid, kP1Threads, P1::bytes, stream>>>(
+                tq, tk, tv, tg, g, pro, beta, scale, table, seq_first_slot + num_seqs, slots, H,
+                region, status);
+        else
+            tc_intra_chunk<true><<<grid, kP1Threads, P1::bytes, stream>>>(
+                tq, tk, tv, tg, g, pro, beta, scale, table, seq_first_slot + num_seqs, slots, H,
+                region, status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if ((err = mark(events, 2, stream)) != cudaSuccess) return err;

@@ -175,6 +175,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
     return false;
 }
 
+// Bounded wait that polls with the non-blocking test (no suspend and wake-up
+// in between): for waits on the critical path whose phase completes within a
+// few hundred cycles. Falls back to the blocking wait after 4096 polls.
+__device__ __forceinline__ bool mbar_spin(uint64_t *mbar, uint32_t parity) {
+    const uint32_t a = smem_u32(mbar);
+    for (int it = 0; it < 4096; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{.reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, "
+            "0, p;}"
+            : "=r"(done)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return mbar_wait(mbar, parity);
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` transactions on mbar.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

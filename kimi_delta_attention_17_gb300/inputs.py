@@ -20,6 +20,18 @@ seed; fixed draw order: sequence lengths, q, k, v, beta, g, initial state):
 * varlen lengths are uniform integers in [lo, hi], packed back to back and
   described by int32 ``cu_seqlens``;
 * the query scale is d_k^{-1/2}, passed separately (q itself is not scaled).
+
+Inputs of the options of kda_chunk_fwd_opt / kda_decode_step_opt
+(``make_prefill_opts``, ``make_decode_opts``; same generator and draw order,
+then the option-specific draws):
+
+* with in-kernel normalisation, q and k are left raw: N(0, 1) times a
+  per-(token, head) magnitude exp(N(0, 0.5^2));
+* gate values by gate kind: "log" as above; "logsigmoid" logits z ~ N(2, 1)
+  (log sigmoid(z) then has the base gate's distribution); "bounded" logits
+  z ~ N(-4, 1) for a lower bound of -5 (mean log-decay near -0.1);
+* decay layout: per channel [.., H, d_k], one per head [.., H] (Gated
+  DeltaNet), or none (g is None).
 """
 from dataclasses import dataclass, field, replace
 from typing import Optional, Tuple
@@ -156,3 +168,83 @@ def make_decode(spec: DecodeSpec):
 def with_(spec, **kw):
     """A copy of a spec with some fields replaced (smaller parity variants)."""
     return replace(spec, **kw)
+
+
+@dataclass(frozen=True)
+class OptionsSpec:
+    """Options of kda_chunk_fwd_opt / kda_decode_step_opt, as the binding names them."""
+    decay: str = "channel"      # "channel", "scalar" or "none"
+    gate: str = "log"           # "log", "logsigmoid" or "bounded"
+    l2norm_qk: bool = False
+    gate_lower: float = -5.0
+
+    def kwargs(self):
+        return dict(decay=self.decay, gate=self.gate, gate_lower=self.gate_lower,
+                    l2norm_qk=self.l2norm_qk)
+
+
+def _gate_values(gen, shape, gate):
+    if gate == "log":
+        return _gate(gen, shape, "base")
+    if gate == "logsigmoid":
+        return torch.randn(shape, generator=gen) + 2.0
+    if gate == "bounded":
+        return torch.randn(shape, generator=gen) - 4.0
+    raise ValueError(gate)
+
+
+def _opt_inputs(gen, lead, H, d, st, opts):
+    """q, k, v, beta, g for the leading shape ``lead`` (tokens or steps x N)."""
+    shape = lead + (H, d)
+    if opts.l2norm_qk:
+        q = torch.randn(shape, generator=gen)
+        k = torch.randn(shape, generator=gen)
+    else:
+        q = _unit(torch.randn(shape, generator=gen))
+        k = _unit(torch.randn(shape, generator=gen))
+    v = torch.randn(shape, generator=gen).to(st)
+    beta = torch.sigmoid(torch.randn(lead + (H,), generator=gen))
+    if opts.decay == "channel":
+        g = _gate_values(gen, shape, opts.gate)
+    elif opts.decay == "scalar":
+        g = _gate_values(gen, lead + (H,), opts.gate)
+    elif opts.decay == "none":
+        g = None
+    else:
+        raise ValueError(opts.decay)
+    if opts.l2norm_qk:
+        q = q * torch.exp(0.5 * torch.randn(lead + (H, 1), generator=gen))
+        k = k * torch.exp(0.5 * torch.randn(lead + (H, 1), generator=gen))
+    return q.to(st), k.to(st), v, beta, g
+
+
+def make_prefill_opts(spec: PrefillSpec, opts: OptionsSpec):
+    """make_prefill for the options: the same keys, with q, k raw when the
+    kernel normalises them, and g shaped by the decay layout (None for "none")."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    lengths = seq_lengths(spec)
+    if spec.lengths is not None:
+        torch.randint(spec.lengths[0], spec.lengths[1] + 1, (spec.num_seqs,), generator=gen)
+    varlen = spec.lengths is not None or spec.fixed_lengths is not None
+    if varlen:
+        B, T = 1, sum(lengths)
+        cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    else:
+        B, T = spec.B, spec.T
+        cu = None
+    H, d = spec.H, spec.d
+    q, k, v, beta, g = _opt_inputs(gen, (B, T), H, d, _dtype(spec.dtype), opts)
+    N = len(lengths)
+    init = None if spec.init == "zero" else 0.1 * torch.randn((N, H, d, d), generator=gen)
+    return dict(q=q, k=k, v=v, g=g, beta=beta, init_state=init, cu_seqlens=cu,
+                scale=d ** -0.5, lengths=lengths)
+
+
+def make_decode_opts(spec: DecodeSpec, opts: OptionsSpec):
+    """make_decode for the options (g [steps, N, H] for "scalar", None for "none")."""
+    gen = torch.Generator().manual_seed(spec.seed)
+    s, N, H, d = spec.steps, spec.N, spec.H, spec.d
+    q, k, v, beta, g = _opt_inputs(gen, (s, N), H, d, _dtype(spec.dtype), opts)
+    state0 = 0.1 * torch.randn((N, H, d, d), generator=gen)
+    return dict(q=q, k=k, v=v, g=g, beta=beta, state0=state0, scale=d ** -0.5)

@@ -48,23 +48,46 @@ def workspace_size(B, T, H, dk, dv, num_seqs, dtype):
                                                        _DTYPES[dtype]))
 
 
+def _options(decay, gate, gate_lower, l2norm_qk):
+    """kda_options for the given names, or None for the plain entry points."""
+    if decay == "channel" and gate == "log" and not l2norm_qk:
+        return None
+    if decay not in _lib.DECAY or gate not in _lib.GATE:
+        raise ValueError("decay must be one of %s and gate one of %s"
+                         % (sorted(_lib.DECAY), sorted(_lib.GATE)))
+    return _lib.Options(_lib.DECAY[decay], _lib.GATE[gate], float(gate_lower), int(bool(l2norm_qk)))
+
+
+def _check_g(g, decay, nd):
+    """g's expected form for the decay family: [..., H, dk], [..., H] or unused."""
+    if decay == "none":
+        if g is not None:
+            _need(g, "g", torch.float32)
+        return
+    _need(g, "g", torch.float32, nd if decay == "channel" else nd - 1)
+
+
 def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=None,
               final_state=None, workspace=None, output_final_state=True, stream=None,
-              phase_events=None):
+              phase_events=None, decay="channel", gate="log", gate_lower=-5.0, l2norm_qk=False):
     """Chunkwise prefill. q, k [B, T, H, dk]; v [B, T, H, dv] (bf16 or fp32);
     g [B, T, H, dk] fp32; beta [B, T, H] fp32; init_state [N, H, dk, dv] fp32
     or None; cu_seqlens int32 [N+1] (device) or None (then N = B).
     Returns (out [B, T, H, dv], final_state [N, H, dk, dv] or None).
     ``phase_events``: optional list of 4 torch.cuda.Event (timing enabled)
     recorded at the start, after the chunk table, after the intra-chunk phase
-    and after the state pass (kda_chunk_fwd_timed)."""
+    and after the state pass.
+    Options (kda_chunk_fwd_opt): ``decay`` "channel" (g [B, T, H, dk]), "scalar"
+    (g [B, T, H], Gated DeltaNet) or "none" (g unused, DeltaNet); ``gate`` "log"
+    (g is log a), "logsigmoid" (a = sigmoid(g)) or "bounded" (log a =
+    gate_lower * sigmoid(g)); ``l2norm_qk`` normalises q and k in the kernel."""
     _need(q, "q", ndim=4)
     dtype = q.dtype
     if dtype not in _DTYPES:
         raise ValueError("q/k/v must be bfloat16 or float32")
     for t, n in ((k, "k"), (v, "v")):
         _need(t, n, dtype, 4)
-    _need(g, "g", torch.float32, 4)
+    _check_g(g, decay, 4)
     _need(beta, "beta", torch.float32, 3)
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -88,31 +111,39 @@ def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     else:
         _need(workspace, "workspace", torch.uint8, 1)
-    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(init_state),
-            _ptr(cu_seqlens), _ptr(out), _ptr(final_state), B, T, H, dk, dv, N, _DTYPES[dtype],
-            _ptr(workspace), workspace.numel(), _stream_ptr(stream))
-    if phase_events is None:
-        _lib.check("kda_chunk_fwd", _lib.lib().kda_chunk_fwd(*args))
-    else:
+    opts = _options(decay, gate, gate_lower, l2norm_qk)
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(init_state),
+            _ptr(cu_seqlens), _ptr(out), _ptr(final_state), B, T, H, dk, dv, N, _DTYPES[dtype])
+    tail = (_ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    handles = None
+    if phase_events is not None:
         if len(phase_events) != 4:
             raise ValueError("phase_events needs 4 events")
         handles = (ctypes.c_void_p * 4)(*[None if e is None else _event_handle(e)
                                           for e in phase_events])
-        _lib.check("kda_chunk_fwd_timed", _lib.lib().kda_chunk_fwd_timed(*args, handles))
+    if opts is not None:
+        _lib.check("kda_chunk_fwd_opt",
+                   _lib.lib().kda_chunk_fwd_opt(*head, ctypes.byref(opts), *tail, handles))
+    elif handles is None:
+        _lib.check("kda_chunk_fwd", _lib.lib().kda_chunk_fwd(*head, *tail))
+    else:
+        _lib.check("kda_chunk_fwd_timed", _lib.lib().kda_chunk_fwd_timed(*head, *tail, handles))
     return out, final_state
 
 
-def decode_step(q, k, v, g, beta, scale, state, *, out=None, stream=None):
+def decode_step(q, k, v, g, beta, scale, state, *, out=None, stream=None, decay="channel",
+                gate="log", gate_lower=-5.0, l2norm_qk=False):
     """One decode step, state updated in place. q, k [N, H, dk]; v [N, H, dv];
     g [N, H, dk] fp32; beta [N, H] fp32; state [N, H, dk, dv] fp32.
-    Returns out [N, H, dv]."""
+    Returns out [N, H, dv]. Options as in chunk_fwd (with "scalar" decay g is
+    [N, H]; kda_decode_step_opt)."""
     _need(q, "q", ndim=3)
     dtype = q.dtype
     if dtype not in _DTYPES:
         raise ValueError("q/k/v must be bfloat16 or float32")
     for t, n in ((k, "k"), (v, "v")):
         _need(t, n, dtype, 3)
-    _need(g, "g", torch.float32, 3)
+    _check_g(g, decay, 3)
     _need(beta, "beta", torch.float32, 2)
     _need(state, "state", torch.float32, 4)
     N, H, dk = q.shape
@@ -121,8 +152,12 @@ def decode_step(q, k, v, g, beta, scale, state, *, out=None, stream=None):
         out = torch.empty((N, H, dv), dtype=dtype, device=q.device)
     else:
         _need(out, "out", dtype, 3)
-    st = _lib.lib().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
-                                    _ptr(state), _ptr(out), N, H, dk, dv, _DTYPES[dtype],
-                                    _stream_ptr(stream))
-    _lib.check("kda_decode_step", st)
+    head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(out),
+            N, H, dk, dv, _DTYPES[dtype])
+    opts = _options(decay, gate, gate_lower, l2norm_qk)
+    if opts is None:
+        _lib.check("kda_decode_step", _lib.lib().kda_decode_step(*head, _stream_ptr(stream)))
+    else:
+        _lib.check("kda_decode_step_opt",
+                   _lib.lib().kda_decode_step_opt(*head, ctypes.byref(opts), _stream_ptr(stream)))
     return out

@@ -98,3 +98,42 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib()
+
+
+def fwd_opt(L, decay=0, gate=0, lower=0.0, l2=0, g=FAKE, opts=True, wsb=16):
+    o = _lib.Options(decay, gate, lower, l2)
+    return L.kda_chunk_fwd_opt(FAKE, FAKE, FAKE, g, FAKE, 0.1, None, None, FAKE, FAKE, 1, 64, 1,
+                               128, 128, 1, 1, ctypes.byref(o) if opts else None, FAKE, wsb, None,
+                               None)
+
+
+def test_options_validation(L):
+    # Accepted options reach the workspace check (an undersized workspace here).
+    assert fwd_opt(L) == WORKSPACE
+    assert fwd_opt(L, opts=False) == WORKSPACE
+    assert fwd_opt(L, decay=1, gate=1, l2=1) == WORKSPACE
+    assert fwd_opt(L, decay=2, g=None) == WORKSPACE          # no decay: g unused, may be NULL
+    assert fwd_opt(L, decay=1, g=FAKE + 4) == WORKSPACE      # per-head g: 4-byte alignment
+    assert fwd_opt(L, gate=2, lower=-5.0) == WORKSPACE
+    # Rejected before any CUDA call.
+    assert fwd_opt(L, decay=3) == INVALID
+    assert fwd_opt(L, gate=7) == INVALID
+    assert fwd_opt(L, decay=0, g=None) == INVALID            # per-channel decay needs g
+    assert fwd_opt(L, decay=0, g=FAKE + 4) == INVALID        # per-channel g: 16-byte alignment
+    assert fwd_opt(L, gate=2, lower=0.0) == INVALID          # bound must be negative
+    assert fwd_opt(L, gate=2, lower=-11.0) == INVALID
+    assert fwd_opt(L, gate=2, lower=float("nan")) == INVALID
+
+
+def test_decode_options_validation(L):
+    def dec(decay=0, gate=0, lower=0.0, g=FAKE, N=4):
+        o = _lib.Options(decay, gate, lower, 0)
+        return L.kda_decode_step_opt(FAKE, FAKE, FAKE, g, FAKE, 0.1, FAKE, FAKE, N, 2, 96, 96, 1,
+                                     ctypes.byref(o), None)
+    # d = 96 is unsupported: accepted options reach that check.
+    assert dec() == UNSUPPORTED
+    assert dec(decay=2, g=None) == UNSUPPORTED
+    assert dec(decay=1, g=FAKE + 4) == UNSUPPORTED
+    assert dec(decay=5) == INVALID
+    assert dec(decay=0, g=None) == INVALID
+    assert dec(gate=2, lower=1.0) == INVALID
