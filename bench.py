@@ -44,6 +44,14 @@ def prefill_bytes(spec, tokens, num_seqs, has_init):
     return tokens * spec.H * per_token_head + num_seqs * spec.H * state * (2 if has_init else 1)
 
 
+def prefill_bytes_g(spec, tokens, num_seqs, has_init, g_bytes_per_token_head):
+    """prefill_bytes with another size of g per (token, head): 4 d for a
+    per-channel decay, 4 for one decay per head, 0 without decay."""
+    d = spec.d
+    return (prefill_bytes(spec, tokens, num_seqs, has_init)
+            - tokens * spec.H * (d * 4 - g_bytes_per_token_head))
+
+
 def prefill_flops(spec, tokens):
     """Dense-contraction flops per (token, head) of the chunk algebra with
     C = 64 full tiles: A, H, W, U, H*Z at 2*C*d each and the three state
@@ -322,6 +330,63 @@ def bench_ours(args):
         decode_ms = d_start.elapsed_time(d_end)
     clocks = clk.summary()
 
+    # ---------------- variants: the options of kda_chunk_fwd_opt / kda_decode_step_opt on the
+    # same resident inputs (one channel of g as the per-head decay; g as gate logits)
+    g_head = d_in["g"][..., 0].contiguous()
+    variant_defs = {
+        "gated_deltanet": (dict(decay="scalar"), g_head, 4),
+        "deltanet": (dict(decay="none"), None, 0),
+        "kda_fused_prologue": (dict(gate="logsigmoid", l2norm_qk=True), d_in["g"], 4 * d),
+    }
+    variants = {}
+    for name, (opts, gv, gbytes) in variant_defs.items():
+        def run_variant():
+            chunk_fwd(d_in["q"], d_in["k"], d_in["v"], gv, d_in["beta"], inp["scale"],
+                      d_in["init_state"], d_in["cu_seqlens"], out=out, final_state=fin,
+                      workspace=ws, **opts)
+        run_variant()
+        torch.cuda.synchronize()
+        v0 = torch.cuda.Event(enable_timing=True)
+        v1 = torch.cuda.Event(enable_timing=True)
+        v0.record(stream)
+        for _ in range(K):
+            run_variant()
+        v1.record(stream)
+        torch.cuda.synchronize()
+        vms = max_over_ranks(v0.elapsed_time(v1), dev) / K
+        vbytes = prefill_bytes_g(spec, tokens, N, inp["init_state"] is not None, gbytes)
+        variants[name] = {
+            "metric": "prefill tokens/s (%s, %s)" % (spec.name, ", ".join(
+                "%s=%s" % kv for kv in sorted(opts.items()))),
+            "value": units_for_world(tokens, world) / (vms / 1e3), "unit": "tokens/s",
+            "ms_per_step": vms,
+            "roofline": {"bound": "hbm", "achieved": vbytes / (vms / 1e3) / 1e9,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                         "algorithmic_bytes_per_launch": vbytes}}
+
+    def decode_fused():
+        for t in range(dspec.steps):
+            decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t],
+                        dinp["scale"], state, out=dout, gate="logsigmoid", l2norm_qk=True)
+    decode_fused()
+    torch.cuda.synchronize()
+    v0 = torch.cuda.Event(enable_timing=True)
+    v1 = torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for _ in range(K):
+        decode_fused()
+    v1.record(stream)
+    torch.cuda.synchronize()
+    dfms = max_over_ranks(v0.elapsed_time(v1), dev) / (K * dspec.steps)
+    variants["decode_fused_prologue"] = {
+        "metric": "decode steps/s (%s, gate=logsigmoid, l2norm_qk=True)" % dspec.name,
+        "value": world / (dfms / 1e3), "unit": "steps/s", "ms_per_step": dfms,
+        "roofline": {"bound": "hbm", "achieved": decode_bytes(dspec) / (dfms / 1e3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": decode_bytes(dspec) / (dfms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": None, "algorithmic_bytes_per_launch": decode_bytes(dspec)}}
+
     prefill_ms = max_over_ranks(prefill_ms, dev)
     decode_ms = max_over_ranks(decode_ms, dev)
     names = ["chunk_table", "intra_chunk", "state_pass"]
@@ -425,6 +490,7 @@ def bench_ours(args):
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": 3 * K + steps_total,
             "clocks": clocks,
+            "variants": variants,
             "decode": {
                 "metric": "KDA decode steps/s (%s)" % dspec.name,
                 "value": dec_steps_s, "unit": "steps/s", "ms_per_step": dec_ms_launch,

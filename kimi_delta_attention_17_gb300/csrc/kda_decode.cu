@@ -24,7 +24,7 @@ constexpr int kSlab = 32;  // state columns per CTA
 // kOpts = false is the plain step (per-channel log-decay in g, no
 // normalisation), compiled without the option branches.
 template <int D, typename InT, bool kOpts>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 7)
 decode_step_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT *__restrict__ v,
                    const float *__restrict__ g, const float *__restrict__ beta, float scale,
                    float *__restrict__ state, InT *__restrict__ out, Prologue pro) {
@@ -43,18 +43,28 @@ decode_step_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const I
 
     const size_t tok = (size_t)nh * D;
     // Decay of this head: per channel, one per head, or none (log a = 0).
-    const float gh = kOpts && pro.decay == KDA_DECAY_SCALAR ? log_decay(g[nh], pro) : 0.f;
+    const float ah = kOpts && pro.decay == KDA_DECAY_SCALAR ? decay_factor(g[nh], pro) : 1.f;
+    // All row loads first (one uniform branch around g), so that they are in
+    // flight together.
+    float zr[R], kin[R], qin[R];
+    const bool chan = !kOpts || pro.decay == KDA_DECAY_CHANNEL;
+    if (chan) {
+#pragma unroll
+        for (int m = 0; m < R; ++m) zr[m] = g[tok + rg + 16 * m];
+    }
+#pragma unroll
+    for (int m = 0; m < R; ++m) {
+        kin[m] = to_f32(k[tok + rg + 16 * m]);
+        qin[m] = to_f32(q[tok + rg + 16 * m]);
+    }
     float av[R], ak[R], aq[R], kr[R];
     float qk = 0.f, kss = 0.f, qss = 0.f;  // q.k and the squared norms of raw k and q
 #pragma unroll
     for (int m = 0; m < R; ++m) {
-        const int r = rg + 16 * m;
-        const float a = !kOpts ? expf(g[tok + r])
-                        : pro.decay == KDA_DECAY_CHANNEL ? expf(log_decay(g[tok + r], pro))
-                        : pro.decay == KDA_DECAY_SCALAR  ? expf(gh)
-                                                         : 1.f;
-        const float kk = to_f32(k[tok + r]);
-        const float q0 = to_f32(q[tok + r]);
+        const float a = !kOpts ? expf(zr[m]) : chan ? decay_factor(zr[m], pro)
+                                                    : ah;  // per head, or 1 without decay
+        const float kk = kin[m];
+        const float q0 = qin[m];
         const float qq = scale * q0;
         av[m] = a;
         kr[m] = kk;

@@ -57,11 +57,19 @@ struct Prologue {
 constexpr float kL2Eps = 1e-6f;  // x / sqrt(sum x^2 + kL2Eps)
 
 // log a from a value of g under the gate transform (KDA_DECAY_NONE never calls
-// this). log sigmoid(z) = min(z, 0) - log(1 + e^-|z|) avoids overflow.
+// this). log sigmoid(z) = min(z, 0) - log(1 + e^-|z|) avoids overflow; the
+// fast exp/log are accurate to ~1e-7 absolute here, far inside the tolerances.
 __device__ __forceinline__ float log_decay(float z, const Prologue &p) {
-    if (p.gate == KDA_GATE_LOGSIGMOID) return fminf(z, 0.f) - log1pf(__expf(-fabsf(z)));
-    if (p.gate == KDA_GATE_BOUNDED) return p.lower / (1.f + __expf(-z));
+    if (p.gate == KDA_GATE_LOGSIGMOID) return fminf(z, 0.f) - __logf(1.f + __expf(-fabsf(z)));
+    if (p.gate == KDA_GATE_BOUNDED) return p.lower * __fdividef(1.f, 1.f + __expf(-z));
     return z;
+}
+// a itself (= exp(log_decay)) where only the factor is needed: sigmoid(z) for
+// the log-sigmoid gate without a logarithm.
+__device__ __forceinline__ float decay_factor(float z, const Prologue &p) {
+    if (p.gate == KDA_GATE_LOGSIGMOID) return __fdividef(1.f, 1.f + __expf(-z));
+    if (p.gate == KDA_GATE_BOUNDED) return __expf(p.lower * __fdividef(1.f, 1.f + __expf(-z)));
+    return expf(z);
 }
 
 template <typename T> __device__ __forceinline__ float to_f32(T x);

@@ -253,10 +253,21 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float G[16];
             float acc = 0.f;
             if (pro.decay == KDA_DECAY_CHANNEL) {
+                if (pro.gate != KDA_GATE_LOG) {
+                    // Gate logits -> log a in place: this thread's column of its
+                    // block is read by no other thread (a rolled loop keeps one
+                    // copy of the transform in the instruction cache).
+                    float *gw = reinterpret_cast<float *>(sm + P1::g);
+#pragma unroll 1
+                    for (int t = 0; t < 16; ++t) {
+                        const int tok = 16 * blk + t;
+                        gw[tok * D + c] = log_decay(gw[tok * D + c], pro);
+                    }
+                }
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int tok = 16 * blk + t;
-                    acc += tok < len ? log_decay(gs[tok * D + c], pro) : 0.f;
+                    acc += tok < len ? gs[tok * D + c] : 0.f;
                     G[t] = acc;
                 }
             } else {
@@ -272,7 +283,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 const int lane = tid & 31;
                 const int tok_l = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) +
                                   ((lane >> 1) & 1);
-#pragma unroll
+#pragma unroll 1
                 for (int tsr = 0; tsr < 2; ++tsr) {
                     const __nv_bfloat16 *xs = tsr ? qs : ks;
                     float v16[16];
