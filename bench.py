@@ -365,6 +365,34 @@ def bench_ours(args):
                          "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
                          "algorithmic_bytes_per_launch": vbytes}}
 
+    # Output gate + RMS normalisation (kda_output_gate_rmsnorm) on the prefill's
+    # output, gate logits drawn on the device: o and z read, out written.
+    from kimi_delta_attention_17_gb300 import output_gate_rmsnorm
+    zgate = torch.randn(out.shape, device=dev, dtype=out.dtype,
+                        generator=torch.Generator(device=dev).manual_seed(17))
+    wnorm = torch.ones(d, device=dev)
+    eout = torch.empty_like(out)
+    output_gate_rmsnorm(out, zgate, wnorm, out=eout)
+    torch.cuda.synchronize()
+    v0 = torch.cuda.Event(enable_timing=True)
+    v1 = torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for _ in range(K):
+        output_gate_rmsnorm(out, zgate, wnorm, out=eout)
+    v1.record(stream)
+    torch.cuda.synchronize()
+    ems = max_over_ranks(v0.elapsed_time(v1), dev) / K
+    ebytes = 3 * out.numel() * out.element_size() + wnorm.numel() * 4
+    variants["output_gate_rmsnorm"] = {
+        "metric": "gated RMSNorm epilogue tokens/s (%s outputs)" % spec.name,
+        "value": units_for_world(tokens, world) / (ems / 1e3), "unit": "tokens/s",
+        "ms_per_step": ems,
+        "roofline": {"bound": "hbm", "achieved": ebytes / (ems / 1e3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": ebytes / (ems / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes_per_launch": ebytes}}
+    del zgate, eout
+
     def decode_fused():
         for t in range(dspec.steps):
             decode_step(dd["q"][t], dd["k"][t], dd["v"][t], dd["g"][t], dd["beta"][t],

@@ -257,6 +257,25 @@ kda_status kda_decode_step_opt(const void *q, const void *k, const void *v, cons
                                int H, int dk, int dv, kda_dtype dtype, const kda_options *options,
                                cudaStream_t stream);
 
+/*
+ * Output gate and RMS normalisation of the attention outputs, per token and
+ * head ("Understanding Kimi Delta Attention", closing remarks: the module
+ * applies output gating and RMS normalisation to the heads' outputs):
+ *
+ *     out_t = w o (o_t / sqrt(mean_c o_t,c^2 + eps)) o sigmoid(z_t)
+ *
+ * (o = elementwise product; the normalisation runs over the d_v channels of
+ * one head).
+ *  o, z, out  [tokens][H][dv], dtype (z: gate logits); out may alias o
+ *  weight     [dv] fp32 per-channel scale shared by the heads, or NULL (ones)
+ *  eps        finite, > 0 (1e-6 is customary)
+ *  tokens >= 0, H > 0, dv in {64, 128}. o, z, out 16-byte aligned; weight
+ *  4-byte aligned. Asynchronous on `stream`; no workspace.
+ */
+kda_status kda_output_gate_rmsnorm(const void *o, const void *z, const float *weight, float eps,
+                                   void *out, long long tokens, int H, int dv, kda_dtype dtype,
+                                   cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -4,6 +4,7 @@ The compute lives in libkda.so (C ABI: include/kda.h); this package is its thin
 Python binding plus the seeded synthetic-input generator. Importing the package
 does not load the library; the first call does, and raises if it is missing.
 """
-from .kda import chunk_fwd, decode_step, status_string, workspace_size  # noqa: F401
+from .kda import (chunk_fwd, decode_step, output_gate_rmsnorm, status_string,  # noqa: F401
+                  workspace_size)
 
-__all__ = ["chunk_fwd", "decode_step", "status_string", "workspace_size"]
+__all__ = ["chunk_fwd", "decode_step", "output_gate_rmsnorm", "status_string", "workspace_size"]

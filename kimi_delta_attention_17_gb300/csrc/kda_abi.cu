@@ -284,3 +284,18 @@ extern "C" kda_status kda_decode_step_opt(const void *q, const void *k, const vo
                                           cudaStream_t stream) {
     return decode_impl(q, k, v, g, beta, scale, state, out, N, H, dk, dv, dtype, options, stream);
 }
+
+extern "C" kda_status kda_output_gate_rmsnorm(const void *o, const void *z, const float *weight,
+                                              float eps, void *out, long long tokens, int H,
+                                              int dv, kda_dtype dtype, cudaStream_t stream) {
+    if (dtype != KDA_DTYPE_F32 && dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARGUMENT;
+    if (tokens < 0 || H <= 0 || !(eps > 0.f) || !isfinite(eps)) return KDA_ERR_INVALID_ARGUMENT;
+    if (tokens * H >= (1LL << 34)) return KDA_ERR_INVALID_ARGUMENT;  // grid of rows / 8 blocks
+    if (tokens > 0 && (!o || !z || !out)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(o) || !aligned16(z) || !aligned16(out)) return KDA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(weight) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
+    if (dv != 64 && dv != 128) return KDA_ERR_UNSUPPORTED;
+    const cudaError_t err =
+        launch_output_gate_rmsnorm(o, z, weight, eps, out, tokens * H, dv, dtype, stream);
+    return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}

@@ -117,6 +117,11 @@ inline cudaError_t mark(cudaEvent_t *events, int i, cudaStream_t stream) {
     return (events && events[i]) ? cudaEventRecord(events[i], stream) : cudaSuccess;
 }
 
+// Output gate + RMS normalisation over rows of dv values (rows = tokens * H).
+cudaError_t launch_output_gate_rmsnorm(const void *o, const void *z, const float *w, float eps,
+                                       void *out, long long rows, int dv, kda_dtype dtype,
+                                       cudaStream_t stream);
+
 // Decode step.
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const float *beta, float scale, float *state, void *out, int N, int H,

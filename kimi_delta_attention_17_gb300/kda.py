@@ -161,3 +161,29 @@ def decode_step(q, k, v, g, beta, scale, state, *, out=None, stream=None, decay=
         _lib.check("kda_decode_step_opt",
                    _lib.lib().kda_decode_step_opt(*head, ctypes.byref(opts), _stream_ptr(stream)))
     return out
+
+
+def output_gate_rmsnorm(o, z, weight=None, eps=1e-6, *, out=None, stream=None):
+    """out = weight * o / sqrt(mean(o^2 over d_v) + eps) * sigmoid(z), per token
+    and head (kda_output_gate_rmsnorm). o, z [..., H, dv] of one dtype (bf16 or
+    fp32); weight [dv] fp32 or None. ``out`` may be ``o`` (in place)."""
+    _need(o, "o")
+    dtype = o.dtype
+    if dtype not in _DTYPES:
+        raise ValueError("o must be bfloat16 or float32")
+    _need(z, "z", dtype)
+    if z.shape != o.shape or o.dim() < 2:
+        raise ValueError("z must have o's shape [..., H, dv]")
+    H, dv = o.shape[-2], o.shape[-1]
+    if weight is not None:
+        _need(weight, "weight", torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(o)
+    else:
+        _need(out, "out", dtype)
+    tokens = o.numel() // (H * dv)
+    _lib.check("kda_output_gate_rmsnorm",
+               _lib.lib().kda_output_gate_rmsnorm(_ptr(o), _ptr(z), _ptr(weight), float(eps),
+                                                  _ptr(out), tokens, H, dv, _DTYPES[dtype],
+                                                  _stream_ptr(stream)))
+    return out

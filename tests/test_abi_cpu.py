@@ -137,3 +137,16 @@ def test_decode_options_validation(L):
     assert dec(decay=5) == INVALID
     assert dec(decay=0, g=None) == INVALID
     assert dec(gate=2, lower=1.0) == INVALID
+
+
+def test_output_gate_rmsnorm_validation(L):
+    f = L.kda_output_gate_rmsnorm
+    assert f(FAKE, FAKE, None, 1e-6, FAKE, 0, 2, 128, 1, None) == 0        # no tokens: nothing to do
+    assert f(FAKE, FAKE, None, 1e-6, FAKE, 10, 2, 96, 1, None) == UNSUPPORTED
+    assert f(FAKE, FAKE, None, 0.0, FAKE, 10, 2, 128, 1, None) == INVALID   # eps must be > 0
+    assert f(FAKE, FAKE, None, float("inf"), FAKE, 10, 2, 128, 1, None) == INVALID
+    assert f(None, FAKE, None, 1e-6, FAKE, 10, 2, 128, 1, None) == INVALID
+    assert f(FAKE + 8, FAKE, None, 1e-6, FAKE, 10, 2, 128, 1, None) == INVALID
+    assert f(FAKE, FAKE, FAKE + 2, 1e-6, FAKE, 10, 2, 128, 1, None) == INVALID
+    assert f(FAKE, FAKE, None, 1e-6, FAKE, -1, 2, 128, 1, None) == INVALID
+    assert f(FAKE, FAKE, None, 1e-6, FAKE, 10, 2, 128, 5, None) == INVALID

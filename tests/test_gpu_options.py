@@ -144,3 +144,25 @@ def test_default_options_match_plain_entry_point():
     assert st == 0
     torch.cuda.synchronize()
     assert torch.equal(out1, out2) and torch.equal(fin1, fin2)
+
+
+@pytest.mark.parametrize("dv,dtype", [(128, "bf16"), (64, "bf16"), (128, "f32"), (64, "f32")])
+@pytest.mark.parametrize("with_weight,in_place", [(True, False), (False, True)])
+def test_output_gate_rmsnorm(dv, dtype, with_weight, in_place):
+    """kda_output_gate_rmsnorm against the fp64 definition (oracle/epilogue.py),
+    on the outputs of a prefill-sized tensor [B, T, H, dv] (1003 tokens)."""
+    from oracle.epilogue import output_gate_rmsnorm as ref_fn
+    from kimi_delta_attention_17_gb300 import output_gate_rmsnorm
+    gen = torch.Generator().manual_seed(16)
+    st = torch.bfloat16 if dtype == "bf16" else torch.float32
+    o = (torch.randn((1, 1003, 3, dv), generator=gen) * 0.3).to(st)
+    z = torch.randn((1, 1003, 3, dv), generator=gen).to(st)
+    w = torch.randn((dv,), generator=gen) if with_weight else None
+    ref = ref_fn(f64(o), f64(z), None if w is None else f64(w), 1e-6)
+    od = o.cuda()
+    got = output_gate_rmsnorm(od, z.cuda(), None if w is None else w.cuda(), 1e-6,
+                              out=od if in_place else None)
+    torch.cuda.synchronize()
+    if in_place:
+        assert got.data_ptr() == od.data_ptr()
+    assert_parity(f64(got), ref, dtype, "gated RMSNorm output")

@@ -112,3 +112,23 @@ def test_prepare_shapes_and_broadcast():
     assert not g0.any()
     with pytest.raises(ValueError):
         prepare(q, q, gh, decay="channel")
+
+
+def test_output_gate_rmsnorm_pins():
+    from oracle.epilogue import output_gate_rmsnorm
+    eps = 1e-6
+    # Worked example: o = [3, 4], mean square 12.5; z = 0 halves; z -> +inf keeps.
+    got = output_gate_rmsnorm(np.array([3.0, 4.0]), np.array([0.0, 60.0]), eps=eps)
+    r = 1.0 / math.sqrt(12.5 + eps)
+    assert got == pytest.approx([0.5 * 3.0 * r, 4.0 * r], rel=1e-12)
+    # A constant row normalises to +-1 (up to eps); z -> -inf closes the gate.
+    c = output_gate_rmsnorm(np.full(8, -2.5), np.full(8, 60.0), eps=eps)
+    assert c == pytest.approx(-1.0, rel=1e-6)
+    assert np.all(np.abs(output_gate_rmsnorm(np.ones(4), np.full(4, -60.0))) < 1e-25)
+    # Linear in the weight, per channel.
+    rng = np.random.default_rng(3)
+    o, z, w = rng.normal(size=(5, 16)), rng.normal(size=(5, 16)), rng.normal(size=16)
+    assert output_gate_rmsnorm(o, z, w) == pytest.approx(w * output_gate_rmsnorm(o, z), rel=1e-12)
+    # Each row's mean square after normalisation (gate open) is 1.
+    y = output_gate_rmsnorm(o * 7.0, np.full_like(o, 60.0))
+    assert np.mean(y * y, axis=-1) == pytest.approx(1.0, rel=1e-6)
