@@ -276,6 +276,17 @@ kda_status kda_output_gate_rmsnorm(const void *o, const void *z, const float *we
                                    void *out, long long tokens, int H, int dv, kda_dtype dtype,
                                    cudaStream_t stream);
 
+/*
+ * Diagnostic of the failure detection (no counterpart on the pages): launches
+ * one CTA that waits, with the kernels' bounded mbarrier wait limited to
+ * `limit` polls (1 .. 4194304), on a barrier nothing ever completes; when the
+ * wait gives up it writes KDA_ERR_TIMEOUT into *status (a device int), as the
+ * prefill kernels write their workspace status word, and returns. Nothing
+ * faults or hangs, and the context stays usable. status must be 4-byte
+ * aligned device memory.
+ */
+kda_status kda_selftest_wait_timeout(int *status, unsigned int limit, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,7 @@ _SIGNATURES = {
                           + [ctypes.c_int] * 7 + [_vp, _vp, ctypes.c_size_t, _vp, _vp], ctypes.c_int),
     "kda_decode_step_opt": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]
                             + [ctypes.c_int] * 5 + [_vp, _vp], ctypes.c_int),
+    "kda_selftest_wait_timeout": ([_vp, ctypes.c_uint, _vp], ctypes.c_int),
     "kda_output_gate_rmsnorm": ([_vp, _vp, _vp, ctypes.c_float, _vp, ctypes.c_longlong,
                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp], ctypes.c_int),
 }

@@ -150,7 +150,8 @@ __device__ __forceinline__ bool bar_and(bool pred, int id, int nthreads) {
 // Bounded wait for the phase with the given parity to complete. Returns false
 // if it gave up (after roughly a second or more of polling). A phase that has
 // already completed is seen by the first, non-blocking test.
-__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, uint32_t limit = 1u << 22);
+__device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, uint32_t limit) {
     const uint32_t a = smem_u32(mbar);
     {
         uint32_t done;
@@ -162,7 +163,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity) {
             : "memory");
         if (done) return true;
     }
-    for (uint32_t it = 0; it < (1u << 22); ++it) {
+    for (uint32_t it = 0; it < limit; ++it) {
         uint32_t ok;
         asm volatile(
             "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, "

@@ -187,3 +187,150 @@ def output_gate_rmsnorm(o, z, weight=None, eps=1e-6, *, out=None, stream=None):
                                                   _ptr(out), tokens, H, dv, _DTYPES[dtype],
                                                   _stream_ptr(stream)))
     return out
+
+
+def chunk_fwd_host(q, k, v, g, beta, scale, init_state=None, *, out=None, final_state=None,
+                   segment_tokens=16384, scratch=None, device=None, **options):
+    """Prefill from pinned host tensors, for fixed-length batches (q, k, v
+    [B, T, H, d], g, beta as in chunk_fwd; no cu_seqlens). Each sequence is cut
+    into segments of ``segment_tokens`` tokens (a multiple of the 64-token
+    chunk, so the chunking and every result are those of one call); segment
+    i + 1 is copied to the device while segment i runs, and segment i's outputs
+    are copied back while segment i + 1 runs. The state crosses segments in
+    fp32 through init_state / final_state. Returns host tensors
+    (out [B, T, H, dv], final_state [B, H, dk, dv]); ``out`` / ``final_state``
+    may be given (pinned). ``scratch``: a dict kept between calls for the
+    device buffers and streams. ``options`` as in chunk_fwd."""
+    if segment_tokens <= 0 or segment_tokens % 64:
+        raise ValueError("segment_tokens must be a positive multiple of 64")
+    if q.dim() != 4 or q.shape[1] == 0:
+        raise ValueError("q must be [B, T, H, d] with T > 0")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta")):
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("%s must be a pinned host tensor" % n)
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    sc = {} if scratch is None else scratch
+    seg = min(segment_tokens, max(T, 1))
+    key = (seg, H, dk, dv, q.dtype, None if g is None else tuple(g.shape[2:]))
+    if sc.get("key") != key:
+        sc.clear()
+        sc["key"] = key
+        sc["streams"] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))  # in, out copies
+        sc["bufs"] = []
+        for _ in range(2):  # double-buffered device segments
+            b = {n: torch.empty((1, seg) + tuple(t.shape[2:]), dtype=t.dtype, device=dev)
+                 for n, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g))
+                 if t is not None}
+            b["out"] = torch.empty((1, seg, H, dv), dtype=q.dtype, device=dev)
+            sc["bufs"].append(b)
+        sc["state"] = torch.empty((1, H, dk, dv), dtype=torch.float32, device=dev)
+        sc["ws"] = torch.empty(max(1, workspace_size(1, seg, H, dk, dv, 1, q.dtype)),
+                               dtype=torch.uint8, device=dev)
+    s_in, s_out = sc["streams"]
+    comp = torch.cuda.current_stream(dev)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype).pin_memory()
+    if final_state is None:
+        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
+    state = sc["state"]
+    jobs = [(b, t0, min(T, t0 + seg)) for b in range(B) for t0 in range(0, max(T, 1), seg)]
+    freed = [torch.cuda.Event(), torch.cuda.Event()]  # buffer i may be refilled
+    drained = [torch.cuda.Event(), torch.cuda.Event()]  # buffer i's outputs copied out
+    for i in range(2):
+        freed[i].record(comp)
+        drained[i].record(comp)
+    for j, (b, t0, t1) in enumerate(jobs):
+        buf = sc["bufs"][j % 2]
+        n = t1 - t0
+        loaded = torch.cuda.Event()
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(freed[j % 2])
+            for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+                if t is not None:
+                    buf[name][:, :n].copy_(t[b:b + 1, t0:t1], non_blocking=True)
+            loaded.record(s_in)
+        comp.wait_event(loaded)
+        comp.wait_event(drained[j % 2])
+        first = t0 == 0
+        if first and init_state is not None:
+            state.copy_(init_state[b:b + 1], non_blocking=True)
+        # [:, :n] of a (1, seg, ...) buffer is contiguous: the short last
+        # segment runs in place.
+        qd, kd, vd, bd = (buf[nm][:, :n] for nm in ("q", "k", "v", "beta"))
+        chunk_fwd(qd, kd, vd, None if g is None else buf["g"][:, :n], bd, scale,
+                  None if (first and init_state is None) else state, out=buf["out"][:, :n],
+                  final_state=state, workspace=sc["ws"], **options)
+        freed[j % 2].record(comp)
+        done = torch.cuda.Event()
+        done.record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            out[b:b + 1, t0:t1].copy_(buf["out"][:, :n], non_blocking=True)
+            if t1 == T:
+                final_state[b:b + 1].copy_(state, non_blocking=True)
+            drained[j % 2].record(s_out)
+        if t1 == T:
+            # the next sequence's first segment must not overwrite this state early
+            comp.wait_stream(s_out)
+    comp.wait_stream(s_out)
+    return out, final_state
+
+
+def decode_host(q, k, v, g, beta, scale, state, *, out=None, scratch=None, **options):
+    """``steps`` successive decode steps from pinned host tensors q, k [steps,
+    N, H, dk], v [steps, N, H, dv], g [steps, N, H, dk] (or per the decay
+    option), beta [steps, N, H]; ``state`` [N, H, dk, dv] fp32 stays on the
+    device and is updated in place. Step t + 1's inputs are copied in while
+    step t runs, and step t's outputs are copied back while step t + 1 runs.
+    Returns the host outputs [steps, N, H, dv] (``out``, pinned, may be given).
+    ``scratch``: a dict kept between calls for the device buffers and streams.
+    ``options`` as in decode_step."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta")):
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("%s must be a pinned host tensor" % n)
+    steps = q.shape[0]
+    dev = state.device
+    sc = {} if scratch is None else scratch
+    key = (tuple(q.shape[1:]), tuple(v.shape[1:]), q.dtype, None if g is None else tuple(g.shape[1:]))
+    if sc.get("key") != key:
+        sc.clear()
+        sc["key"] = key
+        sc["streams"] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+        sc["bufs"] = [{n: torch.empty(tuple(t.shape[1:]), dtype=t.dtype, device=dev)
+                       for n, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g))
+                       if t is not None} for _ in range(2)]
+        for b in sc["bufs"]:
+            b["out"] = torch.empty(tuple(v.shape[1:]), dtype=q.dtype, device=dev)
+    s_in, s_out = sc["streams"]
+    comp = torch.cuda.current_stream(dev)
+    if out is None:
+        out = torch.empty(tuple(v.shape), dtype=q.dtype).pin_memory()
+    freed = [torch.cuda.Event(), torch.cuda.Event()]
+    drained = [torch.cuda.Event(), torch.cuda.Event()]
+    for i in range(2):
+        freed[i].record(comp)
+        drained[i].record(comp)
+    for t in range(steps):
+        buf = sc["bufs"][t % 2]
+        loaded = torch.cuda.Event()
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(freed[t % 2])
+            for name, x in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
+                if x is not None:
+                    buf[name].copy_(x[t], non_blocking=True)
+            loaded.record(s_in)
+        comp.wait_event(loaded)
+        comp.wait_event(drained[t % 2])
+        decode_step(buf["q"], buf["k"], buf["v"], buf.get("g"), buf["beta"], scale, state,
+                    out=buf["out"], **options)
+        freed[t % 2].record(comp)
+        done = torch.cuda.Event()
+        done.record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            out[t].copy_(buf["out"], non_blocking=True)
+            drained[t % 2].record(s_out)
+    comp.wait_stream(s_out)
+    return out

@@ -150,3 +150,11 @@ def test_output_gate_rmsnorm_validation(L):
     assert f(FAKE, FAKE, FAKE + 2, 1e-6, FAKE, 10, 2, 128, 1, None) == INVALID
     assert f(FAKE, FAKE, None, 1e-6, FAKE, -1, 2, 128, 1, None) == INVALID
     assert f(FAKE, FAKE, None, 1e-6, FAKE, 10, 2, 128, 5, None) == INVALID
+
+
+def test_selftest_validation(L):
+    f = L.kda_selftest_wait_timeout
+    assert f(None, 100, None) == INVALID
+    assert f(FAKE + 2, 100, None) == INVALID
+    assert f(FAKE, 0, None) == INVALID
+    assert f(FAKE, (1 << 22) + 1, None) == INVALID

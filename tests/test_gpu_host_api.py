@@ -1,0 +1,67 @@
+"""The host-buffer APIs (chunk_fwd_host, decode_host) pipeline copies with the
+compute; their results are bit-identical to the device-tensor calls: segments
+are whole 64-token chunks and the fp32 state crosses them unchanged."""
+import pytest
+import torch
+
+from kimi_delta_attention_17_gb300 import (build, chunk_fwd, chunk_fwd_host, decode_host,
+                                           decode_step)
+from kimi_delta_attention_17_gb300.inputs import (DecodeSpec, OptionsSpec, PrefillSpec, make_decode,
+                                                  make_prefill, make_prefill_opts)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+
+
+def _pin(inp, keys):
+    return {n: None if inp[n] is None else inp[n].pin_memory() for n in keys}
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_chunk_fwd_host_matches_device_call(dtype, d):
+    spec = PrefillSpec("host", H=3, d=d, B=2, T=300, dtype=dtype, init="normal0.1", seed=19)
+    inp = make_prefill(spec)
+    h = _pin(inp, ("q", "k", "v", "g", "beta", "init_state"))
+    scratch = {}
+    out_h, fin_h = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
+                                  h["init_state"], segment_tokens=128, scratch=scratch)
+    out_h2, _ = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
+                               h["init_state"], segment_tokens=128, scratch=scratch)
+    torch.cuda.synchronize()
+    out_d, fin_d = chunk_fwd(*(inp[n].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"],
+                             inp["init_state"].cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(fin_h, fin_d.cpu())
+    assert torch.equal(out_h2, out_h)
+
+
+def test_chunk_fwd_host_with_options():
+    opts = OptionsSpec("scalar", "logsigmoid", True)
+    inp = make_prefill_opts(PrefillSpec("host-opt", H=2, d=128, B=1, T=200, seed=20), opts)
+    h = _pin(inp, ("q", "k", "v", "g", "beta"))
+    out_h, fin_h = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
+                                  segment_tokens=64, **opts.kwargs())
+    torch.cuda.synchronize()
+    out_d, fin_d = chunk_fwd(*(inp[n].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"],
+                             **opts.kwargs())
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(fin_h, fin_d.cpu())
+
+
+def test_decode_host_matches_device_steps():
+    spec = DecodeSpec("host-decode", N=6, H=2, d=128, steps=5, seed=21)
+    inp = make_decode(spec)
+    h = _pin(inp, ("q", "k", "v", "g", "beta"))
+    s1 = inp["state0"].cuda()
+    out_h = decode_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"], s1)
+    s2 = inp["state0"].cuda()
+    outs = [decode_step(*(inp[n][t].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"], s2)
+            for t in range(spec.steps)]
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, torch.stack(outs).cpu()) and torch.equal(s1, s2)
