@@ -11,14 +11,23 @@ namespace {
 // Builds the chunk table on the device (cu_seqlens lives there; reading it on
 // the host would need a synchronising copy). One CTA: an exclusive scan of
 // per-sequence chunk counts, then each sequence writes its own slots; the
-// slots past the last used one are marked unused.
+// slots past the last used one are marked unused. It also writes the order in
+// which the state passes take the sequences: each state-pass CTA walks one
+// sequence's chunks in series, so a mixed-length batch finishes soonest when
+// the longest chains are dispatched first (longest-processing-time order;
+// ties by index). Up to kOrderMaxSeqs packed sequences are ranked, by a
+// count over shared memory; beyond that, and for fixed-length batches, the
+// order is the identity.
 constexpr int kTableThreads = 1024;
+constexpr int kOrderMaxSeqs = 1024;
 
 __global__ void __launch_bounds__(kTableThreads)
 chunk_table_kernel(const int32_t *__restrict__ cu_seqlens, int num_seqs, int T_fixed,
                    long long slots, ChunkEntry *__restrict__ table,
-                   int *__restrict__ seq_first_slot, int *__restrict__ status) {
+                   int *__restrict__ seq_first_slot, int *__restrict__ seq_order,
+                   int *__restrict__ status) {
     __shared__ int part[kTableThreads];
+    __shared__ int nch[kOrderMaxSeqs];
     const int tid = threadIdx.x;
     if (tid == 0) *status = 0;
     // Sequences [lo, hi) belong to this thread.
@@ -33,14 +42,26 @@ chunk_table_kernel(const int32_t *__restrict__ cu_seqlens, int num_seqs, int T_f
             len = T_fixed;
         }
     };
+    const bool rank = cu_seqlens != nullptr && num_seqs <= kOrderMaxSeqs;
     int mine = 0;
     for (int n = lo; n < hi; ++n) {
         int bos, len;
         seq_bounds(n, bos, len);
-        mine += (len + kChunk - 1) / kChunk;
+        const int c = (len + kChunk - 1) / kChunk;
+        mine += c;
+        if (rank) nch[n] = c;
     }
     part[tid] = mine;
     __syncthreads();
+    for (int n = lo; n < hi; ++n) {
+        int r = n;
+        if (rank) {
+            const int c = nch[n];
+            r = 0;
+            for (int m = 0; m < num_seqs; ++m) r += nch[m] > c || (nch[m] == c && m < n);
+        }
+        seq_order[r] = n;
+    }
     // Inclusive Hillis-Steele scan over the per-thread totals.
     for (int off = 1; off < kTableThreads; off <<= 1) {
         const int add = tid >= off ? part[tid - off] : 0;
@@ -93,7 +114,8 @@ cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fi
                                long long slots, ChunkEntry *table, int *seq_first_slot,
                                int *status, cudaStream_t stream) {
     chunk_table_kernel<<<1, kTableThreads, 0, stream>>>(cu_seqlens, num_seqs, T_fixed, slots,
-                                                        table, seq_first_slot, status);
+                                                        table, seq_first_slot,
+                                                        seq_first_slot + num_seqs + 1, status);
     return cudaGetLastError();
 }
 
@@ -165,6 +187,7 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if (cu_seqlens ? B != 1 : num_seqs != B) return KDA_ERR_INVALID_ARGUMENT;
     if ((long long)B * T * H * (dk > dv ? dk : dv) >= (1LL << 40)) return KDA_ERR_INVALID_ARGUMENT;
     if ((long long)B * T >= (1LL << 31) - kChunk) return KDA_ERR_INVALID_ARGUMENT;
+    if ((long long)num_seqs * H * kMaxStateTiles >= (1LL << 31)) return KDA_ERR_UNSUPPORTED;
     const bool have_tokens = (long long)B * T > 0;
     if (have_tokens && (!q || !k || !v || !beta || !out)) return KDA_ERR_INVALID_ARGUMENT;
     if (!g_ok(g, pro, have_tokens)) return KDA_ERR_INVALID_ARGUMENT;

@@ -42,10 +42,16 @@ inline dim3 head_slot_grid(int H, long long slots) {
 // the chunk table, the per-sequence first-slot offsets, and the per-path
 // regions.
 constexpr size_t kWsHeader = 256;
+// Workspace head: the status word, the chunk table, then seq_first_slot
+// [num_seqs + 1] followed by seq_order [num_seqs] (the state passes' sequence
+// order, longest first).
 inline size_t table_bytes(long long slots, int num_seqs) {
     return kWsHeader + align_up((size_t)slots * sizeof(ChunkEntry), 256) +
-           align_up((size_t)(num_seqs + 1) * sizeof(int), 256);
+           align_up((size_t)(2 * num_seqs + 1) * sizeof(int), 256);
 }
+
+// State-pass CTAs per (sequence, head) at most (d_v tiles), for the 1-D grids.
+constexpr int kMaxStateTiles = 8;
 
 // Validated kda_options, passed to the kernels by value.
 struct Prologue {

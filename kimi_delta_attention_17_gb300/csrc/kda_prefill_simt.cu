@@ -209,10 +209,17 @@ constexpr size_t pass_smem_bytes() {
 template <int D, typename OutT>
 __global__ void __launch_bounds__(kThreads)
 simt_state_pass(const float *__restrict__ ws, const int *__restrict__ seq_first_slot,
-                const int32_t *__restrict__ cu_seqlens, int T_fixed, const float *init_state,
-                OutT *__restrict__ out, float *final_state, int H) {
+                const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens,
+                int T_fixed, const float *init_state, OutT *__restrict__ out, float *final_state,
+                int H) {
     constexpr int P = D + 1;
-    const int n = blockIdx.x, h = blockIdx.y, j0 = blockIdx.z * kSlabCols;
+    // 1-D grid, sequences slowest in seq_order (longest first), then heads,
+    // then the column slabs of one head.
+    constexpr int kTiles = D / kSlabCols;
+    const int per_seq = H * kTiles;
+    const int r = (int)blockIdx.x / per_seq, rem = (int)blockIdx.x - r * per_seq;
+    const int h = rem / kTiles, j0 = (rem - h * kTiles) * kSlabCols;
+    const int n = seq_order[r];
     const int tid = threadIdx.x;
     int bos, len;
     if (cu_seqlens) {
@@ -312,9 +319,10 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
     }
     if ((err = mark(events, 2, stream)) != cudaSuccess) return err;
     if (num_seqs > 0) {
-        simt_state_pass<D, InT><<<dim3(num_seqs, H, D / kSlabCols), kThreads, s2, stream>>>(
-            region, seq_first_slot, cu_seqlens, T_fixed, init_state, static_cast<InT *>(out),
-            final_state, H);
+        static_assert(D / kSlabCols <= kMaxStateTiles, "grid bound checked with kMaxStateTiles");
+        simt_state_pass<D, InT><<<(unsigned)num_seqs * H * (D / kSlabCols), kThreads, s2, stream>>>(
+            region, seq_first_slot, seq_first_slot + num_seqs + 1, cu_seqlens, T_fixed, init_state,
+            static_cast<InT *>(out), final_state, H);
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }

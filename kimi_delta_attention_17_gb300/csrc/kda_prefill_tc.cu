@@ -738,10 +738,17 @@ constexpr int kD2Col = 128;
 
 __global__ void __launch_bounds__(kP2Threads, 1)
 tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
-              const int32_t *__restrict__ cu_seqlens, int T_fixed, const float *init_state,
-              __nv_bfloat16 *__restrict__ out, float *final_state, int H, int *__restrict__ status) {
+              const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens,
+              int T_fixed, const float *init_state, __nv_bfloat16 *__restrict__ out,
+              float *final_state, int H, int *__restrict__ status) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    const int n = blockIdx.x, h = blockIdx.y, jt = blockIdx.z, j0 = jt * kTN;
+    // 1-D grid, sequences slowest in seq_order (longest first), then heads,
+    // then the column tiles of one head (adjacent: they read the same tiles).
+    constexpr int kTiles = D / kTN;
+    const int per_seq = H * kTiles;
+    const int rank = (int)blockIdx.x / per_seq, rem = (int)blockIdx.x - rank * per_seq;
+    const int h = rem / kTiles, jt = rem - h * kTiles, j0 = jt * kTN;
+    const int n = seq_order[rank];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int bos, len;
     if (cu_seqlens) {
@@ -1076,8 +1083,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     }
     if ((err = mark(events, 2, stream)) != cudaSuccess) return err;
     if (num_seqs > 0) {
-        tc_state_pass<<<dim3(num_seqs, H, D / kTN), kP2Threads, kP2Smem, stream>>>(
-            region, seq_first_slot, cu_seqlens, T_fixed, init_state,
+        static_assert(D / kTN <= kMaxStateTiles, "grid bound checked with kMaxStateTiles");
+        tc_state_pass<<<(unsigned)num_seqs * H * (D / kTN), kP2Threads, kP2Smem, stream>>>(
+            region, seq_first_slot, seq_first_slot + num_seqs + 1, cu_seqlens, T_fixed, init_state,
             static_cast<__nv_bfloat16 *>(out), final_state, H, status);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
