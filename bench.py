@@ -366,6 +366,45 @@ def bench_ours(args):
                          "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
                          "algorithmic_bytes_per_launch": vbytes}}
 
+    # Few (sequence, head) chains: the first 4 heads of the same inputs (a
+    # 4-head shard of the workload) with one serial state chain per head and
+    # with the automatic segmented state pass (chunk-level parallel prefix).
+    if inp["cu_seqlens"] is None and H >= 4:
+        sub = {n: (None if d_in[n] is None else d_in[n][:, :, :4].contiguous())
+               for n in ("q", "k", "v", "g", "beta")}
+        sub_init = None if d_in["init_state"] is None else d_in["init_state"][:, :4].contiguous()
+        sub_out = torch.empty_like(sub["v"])
+        sub_fin = torch.empty((N, 4, d, d), dtype=torch.float32, device=dev)
+        sub_ws = torch.empty(max(1, workspace_size(B, T, 4, d, d, N, dt_storage)),
+                             dtype=torch.uint8, device=dev)
+        sub_spec = kin.with_(spec, H=4)
+        for name, segs in (("four_heads_serial_chain", 1), ("four_heads_parallel_prefix", 0)):
+            def run_sub():
+                chunk_fwd(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], inp["scale"],
+                          sub_init, None, out=sub_out, final_state=sub_fin, workspace=sub_ws,
+                          segments=segs)
+            run_sub()
+            torch.cuda.synchronize()
+            v0 = torch.cuda.Event(enable_timing=True)
+            v1 = torch.cuda.Event(enable_timing=True)
+            v0.record(stream)
+            for _ in range(K):
+                run_sub()
+            v1.record(stream)
+            torch.cuda.synchronize()
+            vms = max_over_ranks(v0.elapsed_time(v1), dev) / K
+            vbytes = prefill_bytes(sub_spec, tokens, N, sub_init is not None)
+            variants[name] = {
+                "metric": "prefill tokens/s (%s restricted to 4 heads, segments=%s)" % (
+                    spec.name, "auto" if segs == 0 else segs),
+                "value": units_for_world(tokens, world) / (vms / 1e3), "unit": "tokens/s",
+                "ms_per_step": vms,
+                "roofline": {"bound": "hbm", "achieved": vbytes / (vms / 1e3) / 1e9,
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                             "traffic": None, "algorithmic_bytes_per_launch": vbytes}}
+        del sub, sub_out, sub_ws
+
     # Output gate + RMS normalisation (kda_output_gate_rmsnorm) on the prefill's
     # output, gate logits drawn on the device: o and z read, out written.
     from kimi_delta_attention_17_gb300 import output_gate_rmsnorm

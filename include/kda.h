@@ -98,7 +98,7 @@ typedef enum {
 
 /*
  * Options of kda_chunk_fwd_opt and kda_decode_step_opt. A NULL pointer means
- * {KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0, 0}, the behaviour of kda_chunk_fwd and
+ * {KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0, 0, 0}, the behaviour of kda_chunk_fwd and
  * kda_decode_step.
  *  decay       layout of g (above)
  *  gate        meaning of g's values (above); ignored with KDA_DECAY_NONE
@@ -109,12 +109,28 @@ typedef enum {
  *              uses them ("Kimi Delta Attention: How It Works, Step by Step",
  *              section 16: the key and query are normalised); the query
  *              scale still applies after it
+ *  segments    prefill only, tensor-core path (bf16, d = 128) with fixed-length
+ *              batches (no cu_seqlens): how the state crosses the chunks.
+ *              1: one serial chain per (sequence, head). k >= 2: each sequence
+ *              is cut into up to k segments of whole chunks; every segment
+ *              but the last first computes its affine map S_out = M S_in + E
+ *              from the same recurrence (M from identity columns with v = 0,
+ *              E from a zero state), the maps are composed in order, and the
+ *              segments then rerun from their true entering states, all in
+ *              parallel ("Understanding Kimi Delta Attention": composing the
+ *              affine transitions; a chunk-level parallel prefix). k is
+ *              clamped so that (sequences x H x k) <= 32 and k <= chunks.
+ *              0 (the default): segments only when few (sequence, head)
+ *              chains leave most of the GPU idle and T >= 2048, else 1.
+ *              Results equal the serial chain's up to fp32 rounding. Must be
+ *              >= 0; ignored by the decode step and the fp32 SIMT path.
  */
 typedef struct {
     kda_decay decay;
     kda_gate gate;
     float gate_lower;
     int l2norm_qk;
+    int segments;
 } kda_options;
 
 /* Human-readable name of a status code (static storage; never NULL). */

@@ -143,7 +143,10 @@ extern "C" size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int 
     const bool packed = num_seqs != B;
     if (packed && B != 1) return 0;
     const long long slots = max_chunk_slots(B, T, num_seqs, packed);
-    return table_bytes(slots, num_seqs) + path_region_bytes(slots, H, dk, dtype);
+    const int segs = seg_limit(B, T, H, num_seqs, packed, use_tc(dk, dtype));
+    return table_bytes(slots, num_seqs) +
+           align_up(path_region_bytes(slots, H, dk, dtype), 256) +
+           seg_bytes((long long)num_seqs * H, segs, dk);
 }
 
 namespace {
@@ -158,6 +161,7 @@ bool make_prologue(const kda_options *o, Prologue *p) {
     if (o->gate != KDA_GATE_LOG && o->gate != KDA_GATE_LOGSIGMOID && o->gate != KDA_GATE_BOUNDED)
         return false;
     if (o->gate == KDA_GATE_BOUNDED && !(o->gate_lower >= -10.f && o->gate_lower < 0.f)) return false;
+    if (o->segments < 0) return false;
     *p = Prologue{(int)o->decay, (int)o->gate, o->gate == KDA_GATE_BOUNDED ? o->gate_lower : 0.f,
                   o->l2norm_qk ? 1 : 0};
     return true;
@@ -211,6 +215,10 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     int *seq_first_slot = reinterpret_cast<int *>(
         ws + kWsHeader + align_up((size_t)slots * sizeof(ChunkEntry), 256));
     char *region = ws + table_bytes(slots, num_seqs);
+    const int seg_max = seg_limit(B, T, H, num_seqs, packed, use_tc(dk, dtype));
+    float *seg_ws = seg_max >= 2 ? reinterpret_cast<float *>(
+                                       region + align_up(path_region_bytes(slots, H, dk, dtype), 256))
+                                 : nullptr;
     const int T_fixed = packed ? 0 : T;
 
     if (events && events[0] && cudaEventRecord(events[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
@@ -220,8 +228,8 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if (use_tc(dk, dtype))
         err = launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
                                 T_fixed, (long long)B * T, H, num_seqs, slots, table, seq_first_slot,
-                                reinterpret_cast<unsigned char *>(region), status, pro, stream,
-                                events);
+                                reinterpret_cast<unsigned char *>(region), status, pro,
+                                options ? options->segments : 0, seg_max, seg_ws, stream, events);
     else
         err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
                                   final_state, T_fixed, H, dk, num_seqs, dtype, slots, table,

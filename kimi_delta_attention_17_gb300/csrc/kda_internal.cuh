@@ -53,6 +53,27 @@ inline size_t table_bytes(long long slots, int num_seqs) {
 // State-pass CTAs per (sequence, head) at most (d_v tiles), for the 1-D grids.
 constexpr int kMaxStateTiles = 8;
 
+// Segmented state pass (tensor-core path, fixed-length batches): the number
+// of segments per sequence is capped so that chains x segments <= this bound,
+// which also bounds the buffers the workspace reserves for it.
+constexpr long long kSegChainBound = 32;
+
+// Most segments a call with these sizes may use (1: the serial chain only).
+inline int seg_limit(int B, int T, int H, int num_seqs, bool packed, bool tc_path) {
+    if (packed || !tc_path || B <= 0 || H <= 0 || num_seqs != B) return 1;
+    const long long chains = (long long)num_seqs * H;
+    const long long nchunks = (T + kChunk - 1) / kChunk;
+    long long p = kSegChainBound / chains;
+    if (p > nchunks) p = nchunks;
+    return p >= 2 ? (int)p : 1;
+}
+
+// Bytes of the segment buffers for `segs` segments: per (sequence, head,
+// segment) the map [E | M] (d x 2d fp32) and the entering state (d x d fp32).
+inline size_t seg_bytes(long long chains, int segs, int d) {
+    return segs >= 2 ? (size_t)chains * segs * (size_t)d * d * 3 * sizeof(float) : 0;
+}
+
 // Validated kda_options, passed to the kernels by value.
 struct Prologue {
     int decay;    // kda_decay: layout of g
@@ -114,7 +135,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               int T_fixed, long long tokens, int H, int num_seqs, long long slots,
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, const Prologue &pro,
-                              cudaStream_t stream, cudaEvent_t *events);
+                              int segments, int seg_max, float *seg_ws, cudaStream_t stream,
+                              cudaEvent_t *events);
 
 // Records events[i] (when non-NULL) on the stream: the prefill marks the
 // start (0), the end of the chunk table (1), of the intra-chunk phase (2) and

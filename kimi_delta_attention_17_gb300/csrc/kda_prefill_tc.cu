@@ -736,18 +736,48 @@ constexpr uint32_t kB2Lbo = 128, kB2Sbo = 1024;
 // product runs); D2 = Kbar^T Z at [128, 192).
 constexpr int kD2Col = 128;
 
+// Which chunks a state-pass launch walks. The serial pass is one segment of
+// every chunk. The segmented pass (a chunk-level parallel prefix over the
+// affine chunk maps S -> (Diag(gamma) - Kbar^T W) S + Kbar^T U) cuts each
+// sequence into P segments of L chunks and runs two launches:
+//  * transfer (segments 0 .. P-2): segment 0 runs from the true initial state
+//    with outputs and stores its end state as the state entering segment 1;
+//    segment p >= 1 runs its d_v tiles from a zero state (E_p) and d_k more
+//    "identity" tiles from identity columns with U = 0 (M_p), without
+//    outputs, into xfer;
+//  * final (segments 1 .. P-1), after seg_combine: each segment runs from the
+//    state entering it, with outputs; the last one writes the final state.
+struct SegPass {
+    int L;         // chunks per segment
+    int P;         // segments per sequence (1: the serial pass)
+    int p_lo, np;  // segments of this launch: p_lo .. p_lo + np - 1
+    int transfer;  // 1: transfer launch, 0: outputs launch
+    float *xfer;   // [seq][H][P][D][2 D]: E_p in columns 0 .. D-1, M_p in D .. 2D-1
+    float *enter;  // [seq][H][P][D][D]: the state entering segment p
+};
+
 __global__ void __launch_bounds__(kP2Threads, 1)
 tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
               const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens,
               int T_fixed, const float *init_state, __nv_bfloat16 *__restrict__ out,
-              float *final_state, int H, int *__restrict__ status) {
+              float *final_state, int H, int *__restrict__ status, const SegPass sp) {
     extern __shared__ __align__(1024) unsigned char sm[];
     // 1-D grid, sequences slowest in seq_order (longest first), then heads,
-    // then the column tiles of one head (adjacent: they read the same tiles).
+    // then segments, then the column tiles of one head and segment (adjacent:
+    // they read the same tiles). A transfer launch has 2 D / kTN tiles: the
+    // d_v tiles, then the identity tiles.
     constexpr int kTiles = D / kTN;
-    const int per_seq = H * kTiles;
+    const int tiles = sp.transfer ? 2 * kTiles : kTiles;
+    const int per_h = sp.np * tiles, per_seq = H * per_h;
     const int rank = (int)blockIdx.x / per_seq, rem = (int)blockIdx.x - rank * per_seq;
-    const int h = rem / kTiles, jt = rem - h * kTiles, j0 = jt * kTN;
+    const int h = rem / per_h, rem2 = rem - h * per_h;
+    const int p = sp.p_lo + rem2 / tiles, jt = rem2 - (rem2 / tiles) * tiles;
+    const bool ident = jt >= kTiles;
+    const int j0 = (ident ? jt - kTiles : jt) * kTN;
+    // Segment 0 of a transfer launch starts from the true initial state: it
+    // needs no map, so its identity tiles have nothing to do.
+    if (sp.transfer && p == 0 && ident) return;
+    const bool outputs = !sp.transfer || p == 0;
     const int n = seq_order[rank];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int bos, len;
@@ -758,8 +788,30 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         bos = n * T_fixed;
         len = T_fixed;
     }
-    const int nchunks = (len + C - 1) / C;
-    const int slot0 = seq_first_slot[n];
+    const int all_chunks = (len + C - 1) / C;
+    const int c0 = (int)min((long long)all_chunks, (long long)p * sp.L);
+    const int nchunks = min(all_chunks - c0, sp.L);  // this segment's chunks
+    const int slot0 = seq_first_slot[n] + c0;
+    // Where the state comes from and where it goes, row r, columns j0 + js:
+    const size_t nh = (size_t)n * H + h;
+    const float *st_src = nullptr;  // NULL: zero (or identity columns)
+    float *st_dst = nullptr;
+    size_t dst_row = D;
+    if (p == 0) {
+        if (init_state) st_src = init_state + nh * D * D;
+    } else if (!sp.transfer) {
+        st_src = sp.enter + (nh * sp.P + p) * D * D;
+    }
+    if (sp.transfer) {
+        if (p == 0) {
+            st_dst = sp.enter + (nh * sp.P + 1) * D * D;
+        } else {
+            st_dst = sp.xfer + (nh * sp.P + p) * D * 2 * D + (ident ? D : 0);
+            dst_row = 2 * D;
+        }
+    } else if (p == sp.P - 1 && final_state) {
+        st_dst = final_state + nh * D * D;
+    }
     unsigned char *B1 = sm + kP2B1;
     unsigned char *B2 = sm + kP2B2;
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kP2Bar);  // [kP2Bufs] tiles landed
@@ -788,10 +840,9 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     // Compute-thread coordinates: TMEM lane / state row r, slab columns js .. js + 7.
     const int r = 32 * (warp & 3) + lane, js = 8 * ((warp >> 2) & 3);
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const size_t st_off = (((size_t)n * H + h) * D + r) * D + j0 + js;
     float S[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) S[j] = 0.f;
+    for (int j = 0; j < 8; ++j) S[j] = ident && r == j0 + js + j ? 1.f : 0.f;
     auto put_state = [&]() {  // B1 rows js + j (hi) and 32 + js + j (lo), K-row r
         uint4 hi, lo;
         split8(S, hi, lo);
@@ -799,9 +850,10 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         *reinterpret_cast<uint4 *>(B1 + mnmaj(kTN + js, r, kB1Lbo, kB1Sbo)) = lo;
     };
     if (warp < kP2MmaWarp) {
-        if (init_state) {
-            const float4 t0 = *reinterpret_cast<const float4 *>(init_state + st_off);
-            const float4 t1 = *reinterpret_cast<const float4 *>(init_state + st_off + 4);
+        if (st_src) {
+            const float *src = st_src + (size_t)r * D + j0 + js;
+            const float4 t0 = *reinterpret_cast<const float4 *>(src);
+            const float4 t1 = *reinterpret_cast<const float4 *>(src + 4);
             S[0] = t0.x; S[1] = t0.y; S[2] = t0.z; S[3] = t0.w;
             S[4] = t1.x; S[5] = t1.y; S[6] = t1.z; S[7] = t1.w;
         }
@@ -831,9 +883,12 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 if (*err) break;
                 const unsigned char *rg = ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes;
                 unsigned char *dst = sm + b * kBufBytes;
-                mbar_expect_tx(bar_ld + b, kLoadBytes);
+                // Identity tiles take U = 0: no slab.
+                mbar_expect_tx(bar_ld + b, ident ? (uint32_t)TcRegion::shared : kLoadBytes);
                 bulk_g2s(dst, rg, (uint32_t)TcRegion::shared, bar_ld + b);
-                bulk_g2s(dst + kBufU, rg + TcRegion::U + (size_t)jt * kSlabBytes, kSlabBytes, bar_ld + b);
+                if (!ident)
+                    bulk_g2s(dst + kBufU, rg + TcRegion::U + (size_t)jt * kSlabBytes, kSlabBytes,
+                             bar_ld + b);
                 issued = ch + 1;
             }
             // Every copy lands before the CTA exits (bounded waits; a buffer's
@@ -881,10 +936,12 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                         mma_bf16(tmem + kD2Col, desc(smem_u32(buf + kBufA2) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo),
                                  desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, s > 0);
                     commit(bar_m2);
+                    if (outputs) {
 #pragma unroll
-                    for (int s = 0; s < C / 16; ++s)
-                        mma_bf16(d1, desc(smem_u32(buf + kBufH) + s * 2 * 1024, 1024, 128),
-                                 desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, 1);
+                        for (int s = 0; s < C / 16; ++s)
+                            mma_bf16(d1, desc(smem_u32(buf + kBufH) + s * 2 * 1024, 1024, 128),
+                                     desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, 1);
+                    }
                 }
             }
             __syncwarp();
@@ -898,8 +955,8 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         uint32_t p1 = 0, p2 = 0;  // phases of the two product barriers
         const bool zrow = r >= 64;
         // Token outputs of chunk `ch` (rows 0-63 of its D1): s Qbar S + H Z.
-        auto put_outputs = [&](int ch) {
-            const int clen = min(C, len - ch * C);
+        auto put_outputs = [&](int ch) {  // ch counts this segment's chunks
+            const int clen = min(C, len - (c0 + ch) * C);
             const uint32_t d1 = tmem + lane_base + 64 * (ch & 1);
             float hi[8], lo[8];
             tmem_ld8(d1 + js, hi);
@@ -909,7 +966,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 float o8[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) o8[j] = hi[j] + lo[j];
-                *reinterpret_cast<uint4 *>(out + ((size_t)(bos + ch * C + r) * H + h) * D + j0 + js) = pack8(o8);
+                *reinterpret_cast<uint4 *>(out + ((size_t)(bos + (c0 + ch) * C + r) * H + h) * D + j0 + js) = pack8(o8);
             }
         };
         for (int ch = 0; ch < nchunks; ++ch) {
@@ -929,8 +986,9 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 tmem_ld8(d1 + lane_base + js, hi);
                 tmem_ld8(d1 + lane_base + kTN + js, lo);
                 const float *Us = reinterpret_cast<const float *>(buf + kBufU);
-                const float4 u0 = *reinterpret_cast<const float4 *>(Us + slab_idx(i, js));
-                const float4 u1 = *reinterpret_cast<const float4 *>(Us + slab_idx(i, js + 4));
+                const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 u0 = ident ? zero4 : *reinterpret_cast<const float4 *>(Us + slab_idx(i, js));
+                const float4 u1 = ident ? zero4 : *reinterpret_cast<const float4 *>(Us + slab_idx(i, js + 4));
                 tmem_wait_ld();
                 const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                 float z[8];
@@ -940,7 +998,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 split8(z, zh, zl);
                 *reinterpret_cast<uint4 *>(B2 + mnmaj(js, i, kB2Lbo, kB2Sbo)) = zh;
                 *reinterpret_cast<uint4 *>(B2 + mnmaj(kTN + js, i, kB2Lbo, kB2Sbo)) = zl;
-            } else if (ch > 0) {
+            } else if (ch > 0 && outputs) {
                 put_outputs(ch - 1);  // overlaps this chunk's Z
             }
             fence_async_smem();
@@ -970,16 +1028,74 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         if (nchunks > 0) {
             wait(bar_m1, p1);
             fence_after();
-            if (!zrow) put_outputs(nchunks - 1);
+            if (!zrow && outputs) put_outputs(nchunks - 1);
         }
-        if (final_state && !*err) {
-            *reinterpret_cast<float4 *>(final_state + st_off) = make_float4(S[0], S[1], S[2], S[3]);
-            *reinterpret_cast<float4 *>(final_state + st_off + 4) = make_float4(S[4], S[5], S[6], S[7]);
+        if (st_dst && !*err) {
+            float *dst = st_dst + (size_t)r * dst_row + j0 + js;
+            *reinterpret_cast<float4 *>(dst) = make_float4(S[0], S[1], S[2], S[3]);
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(S[4], S[5], S[6], S[7]);
         }
     }
     fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc<256>(tmem);
+}
+
+// Composition of the segment maps, in order: enter[p + 1] = M_p enter[p] + E_p
+// for p = 1 .. P - 2 (enter[1] is segment 0's end state). One CTA per
+// (sequence, head, 32-column tile of the state); fp32 throughout. Thread t
+// owns row t / 2 and 16 columns; the state tile stays in shared memory from
+// one segment to the next.
+constexpr int kCombThreads = 256;
+constexpr int kCombCols = 32;
+constexpr int kCombMs = D + 1;  // padded row stride of M_p: rows t / 2 fall in distinct banks
+constexpr size_t kCombSmem = sizeof(float) * ((size_t)D * kCombMs + (size_t)D * kCombCols);
+
+__global__ void __launch_bounds__(kCombThreads)
+seg_combine(const float *__restrict__ xfer, float *__restrict__ enter, int P) {
+    extern __shared__ float csm[];
+    float *Ms = csm;                   // [D][kCombMs]
+    float *Ss = csm + D * kCombMs;     // [D][kCombCols]
+    const int nh = blockIdx.x / (D / kCombCols), j0 = (blockIdx.x % (D / kCombCols)) * kCombCols;
+    const int tid = threadIdx.x, i = tid >> 1, jh = (tid & 1) * 16;
+    const float *x0 = xfer + (size_t)nh * P * D * 2 * D;
+    float *e0 = enter + (size_t)nh * P * D * D;
+    for (int idx = tid; idx < D * kCombCols; idx += kCombThreads) {
+        const int k = idx / kCombCols, j = idx % kCombCols;
+        Ss[k * kCombCols + j] = e0[((size_t)1 * D + k) * D + j0 + j];
+    }
+    for (int p = 1; p + 1 < P; ++p) {
+        const float *xp = x0 + (size_t)p * D * 2 * D;
+        for (int idx = tid; idx < D * D / 4; idx += kCombThreads) {
+            const int row = idx / (D / 4), c4 = idx % (D / 4);
+            const float4 m = *reinterpret_cast<const float4 *>(xp + (size_t)row * 2 * D + D + 4 * c4);
+            float *dst = Ms + row * kCombMs + 4 * c4;
+            dst[0] = m.x; dst[1] = m.y; dst[2] = m.z; dst[3] = m.w;
+        }
+        __syncthreads();
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = xp[(size_t)i * 2 * D + j0 + jh + j];
+#pragma unroll 4
+        for (int k = 0; k < D; ++k) {
+            const float m = Ms[i * kCombMs + k];
+            const float4 *sr = reinterpret_cast<const float4 *>(Ss + k * kCombCols + jh);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 sv = sr[q];
+                acc[4 * q] += m * sv.x; acc[4 * q + 1] += m * sv.y;
+                acc[4 * q + 2] += m * sv.z; acc[4 * q + 3] += m * sv.w;
+            }
+        }
+        __syncthreads();  // every thread is done with Ss and Ms
+        float *ep = e0 + ((size_t)(p + 1) * D + i) * D + j0 + jh;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 v = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+            *reinterpret_cast<float4 *>(ep + 4 * q) = v;
+            *reinterpret_cast<float4 *>(Ss + i * kCombCols + jh + 4 * q) = v;
+        }
+    }
 }
 
 }  // namespace
@@ -1024,6 +1140,24 @@ cudaError_t token_rows_map(CUtensorMap *m, const void *base, CUtensorMapDataType
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Segments of the state pass for the `segments` option (0: automatic, 1: the
+// serial chain, k: k segments), at most seg_max (the workspace's bound) and
+// one per chunk. Automatic: as many as keep the transfer launch within one
+// wave (chains x (D/kTN + 2 D/kTN (P - 2)) CTAs <= SMs), with at least 8
+// chunks per segment, and only when that makes 3 or more (with two, as many
+// chunks run in series as with one) and T >= 32 chunks.
+int state_segments(int segments, int seg_max, int nch, long long chains, int sm_count) {
+    constexpr int kTiles = D / kTN;
+    if (seg_max < 2 || segments == 1 || nch < 2 || chains <= 0) return 1;
+    if (segments >= 2) return min(segments, min(seg_max, nch));
+    if (nch < 32) return 1;
+    const long long per = sm_count / chains;  // CTAs per chain in one wave
+    long long p = per >= kTiles ? (per - kTiles) / (2 * kTiles) + 2 : 1;
+    if (p > seg_max) p = seg_max;
+    if (p > nch / 8) p = nch / 8;
+    return p >= 3 ? (int)p : 1;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
@@ -1032,7 +1166,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               int T_fixed, long long tokens, int H, int num_seqs, long long slots,
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, const Prologue &pro,
-                              cudaStream_t stream, cudaEvent_t *events) {
+                              int segments, int seg_max, float *seg_ws, cudaStream_t stream,
+                              cudaEvent_t *events) {
     // Per device, once: the SM count (phase 1 runs one persistent CTA per SM)
     // and the dynamic shared-memory opt-ins. Repeating this is idempotent.
     static int sm_counts[64];
@@ -1052,7 +1187,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                 cudaSuccess)
             return err;
         if ((err = cudaFuncSetAttribute(tc_state_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kP2Smem)) != cudaSuccess)
+                                        kP2Smem)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kCombSmem)) != cudaSuccess)
             return err;
         sm_counts[dev] = n;
     }
@@ -1083,11 +1220,40 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     }
     if ((err = mark(events, 2, stream)) != cudaSuccess) return err;
     if (num_seqs > 0) {
-        static_assert(D / kTN <= kMaxStateTiles, "grid bound checked with kMaxStateTiles");
-        tc_state_pass<<<(unsigned)num_seqs * H * (D / kTN), kP2Threads, kP2Smem, stream>>>(
-            region, seq_first_slot, seq_first_slot + num_seqs + 1, cu_seqlens, T_fixed, init_state,
-            static_cast<__nv_bfloat16 *>(out), final_state, H, status);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        static_assert(2 * (D / kTN) <= kMaxStateTiles, "grid bound checked with kMaxStateTiles");
+        constexpr int kTiles = D / kTN;
+        const int *order = seq_first_slot + num_seqs + 1;
+        const int nch = (T_fixed + C - 1) / C;
+        const int P = state_segments(segments, seg_max, nch, (long long)num_seqs * H, sm_count);
+        if (P <= 1) {
+            const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
+            tc_state_pass<<<(unsigned)num_seqs * H * kTiles, kP2Threads, kP2Smem, stream>>>(
+                region, seq_first_slot, order, cu_seqlens, T_fixed, init_state,
+                static_cast<__nv_bfloat16 *>(out), final_state, H, status, sp);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        } else {
+            const int L = (nch + P - 1) / P;
+            const int Pn = (nch + L - 1) / L;  // no empty segment
+            float *xfer = seg_ws;
+            float *enter = seg_ws + (size_t)num_seqs * H * Pn * D * 2 * D;
+            const SegPass sa{L, Pn, 0, Pn - 1, 1, xfer, enter};
+            tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * 2 * kTiles, kP2Threads, kP2Smem,
+                            stream>>>(region, seq_first_slot, order, cu_seqlens, T_fixed,
+                                      init_state, static_cast<__nv_bfloat16 *>(out), final_state,
+                                      H, status, sa);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            if (Pn > 2) {
+                seg_combine<<<(unsigned)num_seqs * H * (D / kCombCols), kCombThreads, kCombSmem,
+                              stream>>>(xfer, enter, Pn);
+                if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            }
+            const SegPass sc{L, Pn, 1, Pn - 1, 0, xfer, enter};
+            tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * kTiles, kP2Threads, kP2Smem,
+                            stream>>>(region, seq_first_slot, order, cu_seqlens, T_fixed,
+                                      init_state, static_cast<__nv_bfloat16 *>(out), final_state,
+                                      H, status, sc);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        }
     }
     return mark(events, 3, stream);
 }

@@ -48,14 +48,17 @@ def workspace_size(B, T, H, dk, dv, num_seqs, dtype):
                                                        _DTYPES[dtype]))
 
 
-def _options(decay, gate, gate_lower, l2norm_qk):
+def _options(decay, gate, gate_lower, l2norm_qk, segments=0):
     """kda_options for the given names, or None for the plain entry points."""
-    if decay == "channel" and gate == "log" and not l2norm_qk:
+    if decay == "channel" and gate == "log" and not l2norm_qk and segments == 0:
         return None
     if decay not in _lib.DECAY or gate not in _lib.GATE:
         raise ValueError("decay must be one of %s and gate one of %s"
                          % (sorted(_lib.DECAY), sorted(_lib.GATE)))
-    return _lib.Options(_lib.DECAY[decay], _lib.GATE[gate], float(gate_lower), int(bool(l2norm_qk)))
+    if int(segments) < 0:
+        raise ValueError("segments must be >= 0")
+    return _lib.Options(_lib.DECAY[decay], _lib.GATE[gate], float(gate_lower), int(bool(l2norm_qk)),
+                        int(segments))
 
 
 def _check_g(g, decay, nd):
@@ -69,7 +72,8 @@ def _check_g(g, decay, nd):
 
 def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=None,
               final_state=None, workspace=None, output_final_state=True, stream=None,
-              phase_events=None, decay="channel", gate="log", gate_lower=-5.0, l2norm_qk=False):
+              phase_events=None, decay="channel", gate="log", gate_lower=-5.0, l2norm_qk=False,
+              segments=0):
     """Chunkwise prefill. q, k [B, T, H, dk]; v [B, T, H, dv] (bf16 or fp32);
     g [B, T, H, dk] fp32; beta [B, T, H] fp32; init_state [N, H, dk, dv] fp32
     or None; cu_seqlens int32 [N+1] (device) or None (then N = B).
@@ -80,7 +84,10 @@ def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=
     Options (kda_chunk_fwd_opt): ``decay`` "channel" (g [B, T, H, dk]), "scalar"
     (g [B, T, H], Gated DeltaNet) or "none" (g unused, DeltaNet); ``gate`` "log"
     (g is log a), "logsigmoid" (a = sigmoid(g)) or "bounded" (log a =
-    gate_lower * sigmoid(g)); ``l2norm_qk`` normalises q and k in the kernel."""
+    gate_lower * sigmoid(g)); ``l2norm_qk`` normalises q and k in the kernel;
+    ``segments`` how the state crosses the chunks on the tensor-core path (0
+    automatic, 1 one serial chain, k up to k segments composed as affine maps;
+    kda_options.segments)."""
     _need(q, "q", ndim=4)
     dtype = q.dtype
     if dtype not in _DTYPES:
@@ -111,7 +118,7 @@ def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     else:
         _need(workspace, "workspace", torch.uint8, 1)
-    opts = _options(decay, gate, gate_lower, l2norm_qk)
+    opts = _options(decay, gate, gate_lower, l2norm_qk, segments)
     head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(init_state),
             _ptr(cu_seqlens), _ptr(out), _ptr(final_state), B, T, H, dk, dv, N, _DTYPES[dtype])
     tail = (_ptr(workspace), workspace.numel(), _stream_ptr(stream))
@@ -194,7 +201,8 @@ def chunk_fwd_host(q, k, v, g, beta, scale, init_state=None, *, out=None, final_
     """Prefill from pinned host tensors, for fixed-length batches (q, k, v
     [B, T, H, d], g, beta as in chunk_fwd; no cu_seqlens). Each sequence is cut
     into segments of ``segment_tokens`` tokens (a multiple of the 64-token
-    chunk, so the chunking and every result are those of one call); segment
+    chunk, so the chunking is that of one call, and with a serial state pass,
+    segments=1, every result is bit-identical to one call's); segment
     i + 1 is copied to the device while segment i runs, and segment i's outputs
     are copied back while segment i + 1 runs. The state crosses segments in
     fp32 through init_state / final_state. Returns host tensors

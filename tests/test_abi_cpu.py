@@ -100,8 +100,8 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
         _lib.lib()
 
 
-def fwd_opt(L, decay=0, gate=0, lower=0.0, l2=0, g=FAKE, opts=True, wsb=16):
-    o = _lib.Options(decay, gate, lower, l2)
+def fwd_opt(L, decay=0, gate=0, lower=0.0, l2=0, g=FAKE, opts=True, wsb=16, segments=0):
+    o = _lib.Options(decay, gate, lower, l2, segments)
     return L.kda_chunk_fwd_opt(FAKE, FAKE, FAKE, g, FAKE, 0.1, None, None, FAKE, FAKE, 1, 64, 1,
                                128, 128, 1, 1, ctypes.byref(o) if opts else None, FAKE, wsb, None,
                                None)
@@ -123,6 +123,22 @@ def test_options_validation(L):
     assert fwd_opt(L, gate=2, lower=0.0) == INVALID          # bound must be negative
     assert fwd_opt(L, gate=2, lower=-11.0) == INVALID
     assert fwd_opt(L, gate=2, lower=float("nan")) == INVALID
+    # Segments of the state pass: any count >= 0 (clamped later), never negative.
+    assert fwd_opt(L, segments=1) == WORKSPACE
+    assert fwd_opt(L, segments=1000) == WORKSPACE
+    assert fwd_opt(L, segments=-1) == INVALID
+
+
+def test_workspace_reserves_segment_buffers(L):
+    # Fixed-length bf16 d=128 batches with few (sequence, head) chains reserve
+    # [E | M] and the entering state (3 d^2 fp32) per chain and segment, with
+    # chains x segments <= 32; packed batches and the fp32 path reserve none.
+    ws = L.kda_chunk_fwd_workspace_size
+    per = 3 * 128 * 128 * 4
+    few = ws(1, 4096, 4, 128, 128, 1, 1)
+    many = ws(1, 4096, 32, 128, 128, 1, 1)
+    assert few - many // 8 >= 4 * 8 * per - 4096
+    assert ws(1, 4096, 4, 128, 128, 1, 1) > ws(1, 4096, 4, 128, 128, 1, 0) // 2
 
 
 def test_decode_options_validation(L):
