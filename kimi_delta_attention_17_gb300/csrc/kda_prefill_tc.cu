@@ -484,13 +484,17 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float *Ts = reinterpret_cast<float *>(sm + P1::Ts);
             float *Ms = reinterpret_cast<float *>(sm + P1::Ms);
             float *Rs = reinterpret_cast<float *>(sm + P1::Rs);
-            // Diagonal blocks T_II = (I - A_II)^{-1}, column by column: four
-            // threads share a column, each owning rows sub, sub + 4, sub + 8,
-            // sub + 12. Once x_r is final its owner broadcasts it (one shuffle)
-            // and every thread pushes it into its later rows, so the dependent
-            // chain is one shuffle and one FMA per row.
-            if (tid < 256) {
-                const int I = tid >> 6, col = (tid >> 2) & 15, sub = tid & 3;
+            // Block row I of the substitution (I - A_II) X = [A_I0 .. A_I,I-1 | I]
+            // gives M_IK = T_II A_IK (K < I) and T_II = (I - A_II)^{-1} together:
+            // 16 (I + 1) right-hand columns, 160 in all, two per group of four
+            // threads; each thread owns rows sub, sub + 4, sub + 8, sub + 12 of its
+            // two columns. Once x_r is final its owner broadcasts it (one shuffle
+            // per column) and every thread pushes it into its later rows, so the
+            // dependent chain is one shuffle and one FMA per row.
+            if (tid < 320) {
+                const int pr2 = tid >> 2, sub = tid & 3;  // column pair; warps never span two block rows
+                const int I = pr2 < 8 ? 0 : pr2 < 24 ? 1 : pr2 < 48 ? 2 : 3;
+                const int cc = 2 * (pr2 - 4 * I * (I + 1));  // first column, in [0, 16 (I + 1))
                 const float *Ab = As + 16 * I * kAS + 16 * I;
                 // This thread's rows of A_II, loaded before the dependent chain
                 // (a[q][r] = A_II[4 q + sub][r], r < 4 q + sub; the rest unused).
@@ -504,27 +508,50 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             a[q][r4] = t.x; a[q][r4 + 1] = t.y; a[q][r4 + 2] = t.z; a[q][r4 + 3] = t.w;
                         }
                     }
-                float x[4];
+                // Right-hand sides: columns of A_IK (K < I), or of the identity.
+                const bool rhs_a = cc < 16 * I;
+                float x0[4], x1[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) x[q] = 4 * q + sub == col ? 1.f : 0.f;
-#pragma unroll
-                for (int r = 0; r < 15; ++r) {
-                    const float xr = __shfl_sync(0xffffffffu, x[r >> 2], (tid & 31 & ~3) | (r & 3));
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (4 * q + 3 > r && 4 * q + sub > r) x[q] += a[q][r] * xr;
+                for (int q = 0; q < 4; ++q) {
+                    const int row = 4 * q + sub;
+                    if (rhs_a) {
+                        const float2 t = *reinterpret_cast<const float2 *>(As + (16 * I + row) * kAS + cc);
+                        x0[q] = t.x;
+                        x1[q] = t.y;
+                    } else {
+                        x0[q] = row == cc - 16 * I ? 1.f : 0.f;
+                        x1[q] = row == cc + 1 - 16 * I ? 1.f : 0.f;
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) Ts[(16 * I + 4 * q + sub) * kAS + 16 * I + col] = x[q];
+                for (int r = 0; r < 15; ++r) {
+                    const int src = (tid & 31 & ~3) | (r & 3);
+                    const float xr0 = __shfl_sync(0xffffffffu, x0[r >> 2], src);
+                    const float xr1 = __shfl_sync(0xffffffffu, x1[r >> 2], src);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (4 * q + 3 > r && 4 * q + sub > r) {
+                            x0[q] += a[q][r] * xr0;
+                            x1[q] += a[q][r] * xr1;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = 4 * q + sub;
+                    float *dst = rhs_a ? Ms + (I * (I - 1) / 2 + (cc >> 4)) * 16 * kMS + row * kMS + (cc & 15)
+                                       : Ts + (16 * I + row) * kAS + cc;
+                    *reinterpret_cast<float2 *>(dst) = make_float2(x0[q], x1[q]);
+                }
             }
             __syncthreads();
             // Off-diagonal blocks: with M_IK = T_II A_IK (K < I), block row I of
-            // (I - A) T = I gives T_IJ = sum_{K = J}^{I - 1} M_IK T_KJ. Stage 1
-            // forms the six M blocks; stage 2 the first subdiagonal and the terms
-            // of the lower blocks that need only T_JJ; stages 3 and 4 finish the
-            // second and third subdiagonals. Each thread computes a 1 x 4 strip
-            // (row r, columns 4 cg .. 4 cg + 3) of one 16 x 16 product.
+            // (I - A) T = I gives T_IJ = sum_{K = J}^{I - 1} M_IK T_KJ. The
+            // substitution above formed the six M blocks; stage 2 forms the first
+            // subdiagonal and the terms of the lower blocks that need only T_JJ;
+            // stages 3 and 4 finish the second and third subdiagonals. Each thread
+            // computes a 1 x 4 strip (row r, columns 4 cg .. 4 cg + 3) of one
+            // 16 x 16 product.
             auto mi = [](int I, int K) { return I * (I - 1) / 2 + K; };  // M block index, K < I
             // acc += P (16 x 16, row stride ps) row r  x  Q (16 x 16, row stride qs) columns 4 cg ..
             auto prod = [](float4 acc, const float *P, int ps, const float *Q, int qs, int r, int cg) {
@@ -557,7 +584,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             auto put = [](float *B, int stride, int r, int cg, float4 v) {
                 *reinterpret_cast<float4 *>(B + r * stride + 4 * cg) = v;
             };
-            // Stage 1: M_IK for (I, K) = (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).
             // Stage 2: T_10, T_21, T_32 = M_{J+1,J} T_JJ; R_20 = M_20 T_00,
             //          R_31 = M_31 T_11, R_30 = M_30 T_00.
             // Stage 3: T_20 = R_20 + M_21 T_10, T_31 = R_31 + M_32 T_21; R_30 += M_31 T_10.
@@ -565,19 +591,14 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // One runtime loop picks each stage's operands and expands a single
             // product (the kernel must stay within the instruction cache).
 #pragma unroll 1
-            for (int stg = 0; stg < 4; ++stg) {
-                const int nprod = stg < 2 ? 6 : stg == 2 ? 3 : 1;
+            for (int stg = 1; stg < 4; ++stg) {
+                const int nprod = stg == 1 ? 6 : stg == 2 ? 3 : 1;
                 if (pr < nprod) {
                     const float *P, *Q;
                     float *dst;
                     int ps, qs = kAS, ds;
                     const float *init = nullptr;  // partial sum to start from (R block)
-                    if (stg == 0) {
-                        const int I = pr < 1 ? 1 : pr < 3 ? 2 : 3, K = pr - I * (I - 1) / 2;
-                        P = Tb(I, I); ps = kAS;
-                        Q = As + 16 * I * kAS + 16 * K;
-                        dst = Mb(I, K); ds = kMS;
-                    } else if (stg == 1) {
+                    if (stg == 1) {
                         const int J = pr < 3 ? pr : pr < 5 ? pr - 3 : 0;
                         const int I = pr < 3 ? J + 1 : pr < 5 ? J + 2 : 3;
                         P = Mb(I, J); ps = kMS;
