@@ -96,8 +96,8 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int tmem = 188688;
     static constexpr int exch = 188704; // fp32 [2][4][128]: block totals and local references of G
     static constexpr int gsc = 192800;  // fp32 [64]: per-head log-decay of the item's tokens
-    static constexpr int nrm = 193056;  // fp32 [2 parities][2 (k, q)][64]: squared norms of k and q
-    static constexpr int bytes = 194080;
+    static constexpr int fac = 193056;  // fp32 [2 (k, q)][64]: reciprocal norms (q's times the scale)
+    static constexpr int bytes = 193568;
     // Reused once the first MMA has consumed am / bm:
     static constexpr int As = am;                // fp32 [64][68]: A
     static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
@@ -116,25 +116,6 @@ __host__ __device__ constexpr int ver_J(int v) { return v - ver_I(v) * (ver_I(v)
 
 __device__ __forceinline__ void st16(unsigned char *p, const float *x) {
     *reinterpret_cast<uint4 *>(p) = pack8(x);
-}
-
-// Sums v[0..15] (one value per token) over the warp's 32 lanes by halving
-// exchanges (16 shuffles in all); lane l ends with the total of token
-// 8 b4 + 4 b3 + 2 b2 + b1, b_i the bits of l (lanes l and l ^ 1 agree).
-__device__ __forceinline__ float warp_sum16(const float (&v)[16], int lane) {
-    float w[8], x[4], y[2];
-    const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        w[j] = (u16 ? v[8 + j] : v[j]) + __shfl_xor_sync(0xffffffffu, u16 ? v[j] : v[8 + j], 16);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        x[j] = (u8 ? w[4 + j] : w[j]) + __shfl_xor_sync(0xffffffffu, u8 ? w[j] : w[4 + j], 8);
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-        y[j] = (u4 ? x[2 + j] : x[j]) + __shfl_xor_sync(0xffffffffu, u4 ? x[j] : x[2 + j], 4);
-    float z = (u2 ? y[1] : y[0]) + __shfl_xor_sync(0xffffffffu, u2 ? y[0] : y[1], 2);
-    return z + __shfl_xor_sync(0xffffffffu, z, 1);
 }
 
 // kOpts = false: per-channel log-decay in g and no normalisation, compiled
@@ -207,8 +188,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                    ? g_head[(size_t)(e.bos + tid) * H + hh]
                    : 0.f;
     };
-    float *nrm_s = reinterpret_cast<float *>(sm + P1::nrm);
-    if (pro.l2norm && tid < 2 * C) nrm_s[tid] = 0.f;  // the first item's norm accumulators
     int sl = (int)(blockIdx.x / H), hc = (int)(blockIdx.x % H);  // this item
     ChunkEntry ce{};
     float bcur = 0.f;
@@ -225,13 +204,11 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     ChunkEntry en = sn < used ? table[sn] : ce;
     uint32_t ld_phase = 0, mma_phase = 0;
     bool ok = true;
-    int it_par = 0;
     while (sl < used) {
         const int len = ce.len;
         int snn = sn, hnn = hn;  // the item after next
         ChunkEntry enn;
         float bn, gn;
-        const int par = it_par;  // parity of this item's norm accumulators
         unsigned char *reg = ws + ((size_t)sl * H + hc) * TcRegion::bytes;
         ok = __syncthreads_and(mbar_wait(bar_ld, ld_phase));
         ld_phase ^= 1;
@@ -252,22 +229,31 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float *gsc_s = reinterpret_cast<float *>(sm + P1::gsc);  // written one item ahead
             float G[16];
             float acc = 0.f;
-            if (pro.decay == KDA_DECAY_CHANNEL) {
-                if (pro.gate != KDA_GATE_LOG) {
-                    // Gate logits -> log a in place: this thread's column of its
-                    // block is read by no other thread (a rolled loop keeps one
-                    // copy of the transform in the instruction cache).
-                    float *gw = reinterpret_cast<float *>(sm + P1::g);
-#pragma unroll 1
-                    for (int t = 0; t < 16; ++t) {
-                        const int tok = 16 * blk + t;
-                        gw[tok * D + c] = log_decay(gw[tok * D + c], pro);
-                    }
-                }
+            if (pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOG) {
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const int tok = 16 * blk + t;
                     acc += tok < len ? gs[tok * D + c] : 0.f;
+                    G[t] = acc;
+                }
+            } else if (pro.decay == KDA_DECAY_CHANNEL) {
+                // Gate logits become log a in registers as they are summed (the
+                // staged g is read nowhere else); the 16 transforms are
+                // independent, so they issue back to back.
+                float gv[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) gv[t] = gs[(16 * blk + t) * D + c];
+                if (pro.gate == KDA_GATE_LOGSIGMOID) {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        gv[t] = fminf(gv[t], 0.f) - __logf(1.f + __expf(-fabsf(gv[t])));
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) gv[t] = pro.lower * __fdividef(1.f, 1.f + __expf(-gv[t]));
+                }
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    acc += 16 * blk + t < len ? gv[t] : 0.f;
                     G[t] = acc;
                 }
             } else {
@@ -276,26 +262,30 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             float *tot_s = reinterpret_cast<float *>(sm + P1::exch);
             float *ref_s = tot_s + 4 * D;
+            float *fac_s = reinterpret_cast<float *>(sm + P1::fac);
             if (pro.l2norm) {
-                // Squared norms of this block's tokens of k and q: each warp sums
-                // its 32 channels with a transposing shuffle reduction, then the
-                // four warps of the block add into shared memory.
-                const int lane = tid & 31;
-                const int tok_l = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) +
-                                  ((lane >> 1) & 1);
-#pragma unroll 1
-                for (int tsr = 0; tsr < 2; ++tsr) {
-                    const __nv_bfloat16 *xs = tsr ? qs : ks;
-                    float v16[16];
+                // Reciprocal norms of k and q per token (the query scale folded
+                // in): four threads per (tensor, token) each sum 32 channels of
+                // the staged row, in 16-byte pieces rotated by the token so that
+                // a warp's reads spread over all banks; two shuffles combine them.
+                const int pair = tid >> 2, part = tid & 3;
+                const int tsr = pair >> 6, tok = pair & 63;  // tensor 0: k, 1: q
+                const __nv_bfloat16 *row = (tsr ? qs : ks) + tok * D;
+                float ss = 0.f;
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int tok = 16 * blk + t;
-                        const float x = tok < len ? __bfloat162float(xs[tok * D + c]) : 0.f;
-                        v16[t] = x * x;
+                for (int j = 0; j < 4; ++j) {
+                    const int piece = 4 * part + ((j + tok) & 3);  // 8 channels
+                    const uint4 w = *reinterpret_cast<const uint4 *>(row + 8 * piece);
+                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(u[e] << 16), hi = __uint_as_float(u[e] & 0xFFFF0000u);
+                        ss += lo * lo + hi * hi;
                     }
-                    const float tot = warp_sum16(v16, lane);
-                    if ((lane & 1) == 0) atomicAdd(nrm_s + par * 2 * C + tsr * C + 16 * blk + tok_l, tot);
                 }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                if (part == 0) fac_s[pair] = rsqrtf(ss + kL2Eps) * (tsr ? scale : 1.f);
             }
             if (tid < C) beta_s[tid] = bcur;
             if (pro.decay == KDA_DECAY_SCALAR) {
@@ -309,8 +299,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tot_s[blk * D + c] = acc;
             ref_s[blk * D + c] = G[7];
             __syncthreads();
-            // The other parity's accumulators, cleared for the next item.
-            if (pro.l2norm && tid < 2 * C) nrm_s[(par ^ 1) * 2 * C + tid] = 0.f;
             // The table entry of the item after next and the next item's beta,
             // read here: a CTA barrier waits for its threads' loads, and the next
             // one is the whole elementwise pass away.
@@ -349,8 +337,8 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     const bool in = i < len;
                     float fk = 1.f, fq = scale;
                     if (pro.l2norm) {
-                        fk = rsqrtf(nrm_s[par * 2 * C + i] + kL2Eps);
-                        fq = scale * rsqrtf(nrm_s[par * 2 * C + C + i] + kL2Eps);
+                        fk = fac_s[i];
+                        fq = fac_s[C + i];
                     }
                     kv[r] = in ? fk * __bfloat162float(ks[i * D + c]) : 0.f;
                     qv[r] = in ? fq * __bfloat162float(qs[i * D + c]) : 0.f;
@@ -696,7 +684,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         hn = hnn;
         en = enn;
         bcur = bn;
-        it_par ^= 1;
     }
     if (!ok) {
         if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
