@@ -118,9 +118,13 @@ __device__ __forceinline__ void st16(unsigned char *p, const float *x) {
     *reinterpret_cast<uint4 *>(p) = pack8(x);
 }
 
-// kOpts = false: per-channel log-decay in g and no normalisation, compiled
-// without the option code (the kernel must stay within the instruction cache).
-template <bool kOpts>
+// Instances: kVar fixes the options at compile time, so that each common
+// form is compiled without the code of the others (the kernel must stay
+// within the instruction cache): 0 per-channel log-decay (KDA), 2 one
+// log-decay per head (Gated DeltaNet), 3 no decay (DeltaNet), all with g
+// holding log a and no normalisation; 1 takes every option at run time.
+constexpr int kVarChannel = 0, kVarRuntime = 1, kVarScalar = 2, kVarNone = 3;
+template <int kVar>
 __global__ void __launch_bounds__(kP1Threads, 1)
 tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -165,7 +169,9 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // One thread fetches an item: four 3-D TMA tiles (128 channels x 1 head x
     // 64 tokens) land as dense [token][channel] rows. Tokens past the end of
     // the tensor read as zeros; tokens of the next sequence are masked by len.
-    if (!kOpts) pro = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0.f, 0};
+    if (kVar == kVarChannel) pro = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0.f, 0};
+    if (kVar == kVarScalar) pro = Prologue{KDA_DECAY_SCALAR, KDA_GATE_LOG, 0.f, 0};
+    if (kVar == kVarNone) pro = Prologue{KDA_DECAY_NONE, KDA_GATE_LOG, 0.f, 0};
     const bool g_tile = pro.decay == KDA_DECAY_CHANNEL;  // g arrives as a tile only per channel
     auto issue = [&](int hh, const ChunkEntry e) {
         if (tid != 0) return;
@@ -1187,10 +1193,16 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         int n = 0;
         if ((err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return err;
-        if ((err = cudaFuncSetAttribute(tc_intra_chunk<false>,
+        if ((err = cudaFuncSetAttribute(tc_intra_chunk<kVarChannel>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
                 cudaSuccess ||
-            (err = cudaFuncSetAttribute(tc_intra_chunk<true>,
+            (err = cudaFuncSetAttribute(tc_intra_chunk<kVarRuntime>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
+                cudaSuccess ||
+            (err = cudaFuncSetAttribute(tc_intra_chunk<kVarScalar>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
+                cudaSuccess ||
+            (err = cudaFuncSetAttribute(tc_intra_chunk<kVarNone>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
                 cudaSuccess)
             return err;
@@ -1215,15 +1227,24 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             return err;
         const long long items = slots * H;
         const unsigned grid = (unsigned)(items < sm_count ? items : sm_count);
-        const bool plain = pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOG && !pro.l2norm;
-        if (plain)
-            tc_intra_chunk<false><<<grid, kP1Threads, P1::bytes, stream>>>(
-                tq, tk, tv, tg, g, pro, beta, scale, table, seq_first_slot + num_seqs, slots, H,
-                region, status);
-        else
-            tc_intra_chunk<true><<<grid, kP1Threads, P1::bytes, stream>>>(
-                tq, tk, tv, tg, g, pro, beta, scale, table, seq_first_slot + num_seqs, slots, H,
-                region, status);
+        int var = kVarRuntime;
+        if (!pro.l2norm) {
+            if (pro.decay == KDA_DECAY_NONE)  // the gate is never applied
+                var = kVarNone;
+            else if (pro.gate == KDA_GATE_LOG)
+                var = pro.decay == KDA_DECAY_CHANNEL ? kVarChannel : kVarScalar;
+        }
+        const int *used = seq_first_slot + num_seqs;
+#define KDA_P1_LAUNCH(V)                                                                        \
+    tc_intra_chunk<V><<<grid, kP1Threads, P1::bytes, stream>>>(tq, tk, tv, tg, g, pro, beta, scale, \
+                                                               table, used, slots, H, region, status)
+        switch (var) {
+            case kVarChannel: KDA_P1_LAUNCH(kVarChannel); break;
+            case kVarScalar: KDA_P1_LAUNCH(kVarScalar); break;
+            case kVarNone: KDA_P1_LAUNCH(kVarNone); break;
+            default: KDA_P1_LAUNCH(kVarRuntime); break;
+        }
+#undef KDA_P1_LAUNCH
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     if ((err = mark(events, 2, stream)) != cudaSuccess) return err;
