@@ -455,6 +455,48 @@ def bench_ours(args):
                      "frac": decode_bytes(dspec) / (dfms / 1e3) / 1e9 / peaks["hbm_gbs"],
                      "traffic": None, "algorithmic_bytes_per_launch": decode_bytes(dspec)}}
 
+    # Small-batch decode (4 sequences x the same heads, 128 steps): the steps
+    # are too short for per-call host work to hide, so they are timed eagerly
+    # (one C call per step) and as one CUDA-graph replay of all the steps.
+    from kimi_delta_attention_17_gb300 import DecodeGraph
+    sspec = kin.with_(dspec, N=4, name="decode bf16 4 seqs x H=%d d=%d, %d steps" % (
+        dspec.H, dspec.d, dspec.steps))
+    sinp = kin.make_decode(sspec)
+    sb = {n: sinp[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    sstate = sinp["state0"].to(dev)
+    sout = torch.empty(tuple(sb["v"].shape[1:]), dtype=sb["v"].dtype, device=dev)
+
+    def small_eager():
+        for t in range(sspec.steps):
+            decode_step(sb["q"][t], sb["k"][t], sb["v"][t], sb["g"][t], sb["beta"][t],
+                        sinp["scale"], sstate, out=sout)
+    small_graph = DecodeGraph(sb["q"], sb["k"], sb["v"], sb["g"], sb["beta"], sinp["scale"],
+                              sstate)
+    sbytes = decode_bytes(sspec)
+    for name, fn in (("decode_small_batch_eager", small_eager),
+                     ("decode_small_batch_graph", small_graph.replay)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        v0 = torch.cuda.Event(enable_timing=True)
+        v1 = torch.cuda.Event(enable_timing=True)
+        v0.record(stream)
+        for _ in range(K):
+            fn()
+        v1.record(stream)
+        torch.cuda.synchronize()
+        sms = max_over_ranks(v0.elapsed_time(v1), dev) / (K * sspec.steps)
+        variants[name] = {
+            "metric": "decode steps/s (%s, %s)" % (
+                sspec.name, "one C call per step" if name.endswith("eager") else
+                "all steps replayed as one CUDA graph"),
+            "value": world / (sms / 1e3), "unit": "steps/s", "ms_per_step": sms,
+            "roofline": {"bound": "hbm", "achieved": sbytes / (sms / 1e3) / 1e9,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": sbytes / (sms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "traffic": None, "algorithmic_bytes_per_launch": sbytes}}
+    del small_graph
+
     prefill_ms = max_over_ranks(prefill_ms, dev)
     decode_ms = max_over_ranks(decode_ms, dev)
     names = ["chunk_table", "intra_chunk", "state_pass"]

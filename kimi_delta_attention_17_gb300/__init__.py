@@ -4,8 +4,8 @@ The compute lives in libkda.so (C ABI: include/kda.h); this package is its thin
 Python binding plus the seeded synthetic-input generator. Importing the package
 does not load the library; the first call does, and raises if it is missing.
 """
-from .kda import (chunk_fwd, chunk_fwd_host, decode_host, decode_step,  # noqa: F401
-                  output_gate_rmsnorm, status_string, workspace_size)
+from .kda import (DecodeGraph, chunk_fwd, chunk_fwd_host, decode_host,  # noqa: F401
+                  decode_step, output_gate_rmsnorm, status_string, workspace_size)
 
-__all__ = ["chunk_fwd", "chunk_fwd_host", "decode_host", "decode_step", "output_gate_rmsnorm",
-           "status_string", "workspace_size"]
+__all__ = ["DecodeGraph", "chunk_fwd", "chunk_fwd_host", "decode_host", "decode_step",
+           "output_gate_rmsnorm", "status_string", "workspace_size"]

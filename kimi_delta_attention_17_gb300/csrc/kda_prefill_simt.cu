@@ -303,12 +303,22 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
                      cudaStream_t stream, cudaEvent_t *events) {
     constexpr size_t s1 = prep_smem_bytes<D>();
     constexpr size_t s2 = pass_smem_bytes<D>();
-    cudaError_t err = cudaFuncSetAttribute(simt_chunk_prep<D, InT>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+    // The shared-memory opt-ins, once per device and instance (nothing but
+    // launches then reaches the stream, so a call can be graph-captured).
+    static bool ready[64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(simt_state_pass<D, InT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)s2);
-    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev]) {
+        err = cudaFuncSetAttribute(simt_chunk_prep<D, InT>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(simt_state_pass<D, InT>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+        if (err != cudaSuccess) return err;
+        ready[dev] = true;
+    }
     if ((err = mark(events, 1, stream)) != cudaSuccess) return err;
     if (slots > 0) {
         simt_chunk_prep<D, InT><<<head_slot_grid(H, slots), kThreads, s1, stream>>>(

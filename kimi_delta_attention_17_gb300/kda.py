@@ -342,3 +342,41 @@ def decode_host(q, k, v, g, beta, scale, state, *, out=None, scratch=None, **opt
             drained[t % 2].record(s_out)
     comp.wait_stream(s_out)
     return out
+
+
+class DecodeGraph:
+    """``steps`` successive decode steps captured once as one CUDA graph and
+    then replayed: the per-step host work (argument checks, the C call, the
+    launch) is paid at capture only, which is what bounds small-batch decode.
+
+    q, k [steps, N, H, dk]; v [steps, N, H, dv]; g and beta as in decode_step
+    with a leading steps axis: device tensors that the caller refills in place
+    between replays. ``state`` [N, H, dk, dv] fp32 is advanced in place by
+    every replay (by all ``steps`` steps). ``out`` [steps, N, H, dv] (allocated
+    when None) receives the outputs of every replay. ``options`` as in
+    decode_step. Capturing runs no step on ``state``: one warm-up step runs on
+    a copy, outside the graph."""
+
+    def __init__(self, q, k, v, g, beta, scale, state, *, out=None, **options):
+        if q.dim() != 4 or q.shape[0] < 1:
+            raise ValueError("q must be [steps, N, H, dk] with steps >= 1")
+        self.steps = q.shape[0]
+        if out is None:
+            out = torch.empty(tuple(v.shape), dtype=q.dtype, device=q.device)
+        self.out = out
+
+        def step(t, st):
+            decode_step(q[t], k[t], v[t], None if g is None else g[t], beta[t], scale, st,
+                        out=out[t], **options)
+
+        warm = state.clone()
+        step(0, warm)  # loads the library and checks the arguments outside the capture
+        torch.cuda.current_stream().synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            for t in range(self.steps):
+                step(t, state)
+
+    def replay(self):
+        """Runs the captured steps on the current stream."""
+        self.graph.replay()
