@@ -164,7 +164,8 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num
  *  init_state [num_seqs][H][dk][dv] fp32, or NULL for zero initial states
  *  cu_seqlens int32 [num_seqs + 1] device array, or NULL. When given: B must
  *             be 1, T = cu_seqlens[num_seqs], values non-decreasing from 0.
- *             The contents are trusted (not read on the host).
+ *             The contents are not read on the host; the first kernel checks
+ *             them (see the status word below).
  *  out        [tokens][H][dv], dtype      token outputs o_t (written)
  *  final_state[num_seqs][H][dk][dv] fp32 (written), or NULL. May alias
  *             init_state exactly (in-place state carry).
@@ -175,6 +176,14 @@ size_t kda_chunk_fwd_workspace_size(int B, int T, int H, int dk, int dv, int num
  *  stream     CUDA stream for all work.
  *
  * A zero-length sequence writes its initial state (or zeros) to final_state.
+ *
+ * Device-side status: the call's kernels write an int status word at the
+ * start of the workspace, to be read once the stream has completed the call.
+ * KDA_OK: the call completed. KDA_ERR_INVALID_ARGUMENT: cu_seqlens failed its
+ * check (cu_seqlens[0] != 0, a decrease, or cu_seqlens[num_seqs] != T); the
+ * call then computed nothing and left out and final_state unwritten.
+ * KDA_ERR_TIMEOUT: a bounded wait inside a kernel gave up (the results are
+ * not valid; the context stays usable).
  */
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const float *g,
                          const float *beta, float scale, const float *init_state,

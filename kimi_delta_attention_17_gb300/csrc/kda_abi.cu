@@ -17,13 +17,16 @@ namespace {
 // the longest chains are dispatched first (longest-processing-time order;
 // ties by index). Up to kOrderMaxSeqs packed sequences are ranked, by a
 // count over shared memory; beyond that, and for fixed-length batches, the
-// order is the identity.
+// order is the identity. Packed offsets are checked first (cu_seqlens[0] = 0,
+// non-decreasing, cu_seqlens[num_seqs] = tokens): on a violation the status
+// word reads KDA_ERR_INVALID_ARGUMENT, the table is empty and the state
+// passes, which read the status word first, do nothing.
 constexpr int kTableThreads = 1024;
 constexpr int kOrderMaxSeqs = 1024;
 
 __global__ void __launch_bounds__(kTableThreads)
 chunk_table_kernel(const int32_t *__restrict__ cu_seqlens, int num_seqs, int T_fixed,
-                   long long slots, ChunkEntry *__restrict__ table,
+                   long long tokens, long long slots, ChunkEntry *__restrict__ table,
                    int *__restrict__ seq_first_slot, int *__restrict__ seq_order,
                    int *__restrict__ status) {
     __shared__ int part[kTableThreads];
@@ -33,6 +36,30 @@ chunk_table_kernel(const int32_t *__restrict__ cu_seqlens, int num_seqs, int T_f
     // Sequences [lo, hi) belong to this thread.
     const int per = (num_seqs + kTableThreads - 1) / kTableThreads;
     const int lo = min(num_seqs, tid * per), hi = min(num_seqs, lo + per);
+    bool bad = false;
+    if (cu_seqlens) {
+        for (int n = lo; n < hi; ++n) bad |= cu_seqlens[n + 1] < cu_seqlens[n];
+        if (tid == 0) bad |= cu_seqlens[0] != 0 || (long long)cu_seqlens[num_seqs] != tokens;
+    }
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) {
+            *status = (int)KDA_ERR_INVALID_ARGUMENT;
+            seq_first_slot[num_seqs] = 0;  // no used slot: phase 1 has no item
+        }
+        for (int n = tid; n < num_seqs; n += kTableThreads) {
+            seq_first_slot[n] = 0;
+            seq_order[n] = n;
+        }
+        for (long long s = tid; s < slots; s += kTableThreads) {
+            ChunkEntry e;
+            e.seq = -1;
+            e.bos = 0;
+            e.len = 0;
+            e.idx = 0;
+            table[s] = e;
+        }
+        return;
+    }
     auto seq_bounds = [&](int n, int &bos, int &len) {
         if (cu_seqlens) {
             bos = cu_seqlens[n];
@@ -110,10 +137,10 @@ size_t path_region_bytes(long long slots, int H, int d, kda_dtype dtype) {
 
 }  // namespace
 
-cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fixed,
+cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fixed, long long tokens,
                                long long slots, ChunkEntry *table, int *seq_first_slot,
                                int *status, cudaStream_t stream) {
-    chunk_table_kernel<<<1, kTableThreads, 0, stream>>>(cu_seqlens, num_seqs, T_fixed, slots,
+    chunk_table_kernel<<<1, kTableThreads, 0, stream>>>(cu_seqlens, num_seqs, T_fixed, tokens, slots,
                                                         table, seq_first_slot,
                                                         seq_first_slot + num_seqs + 1, status);
     return cudaGetLastError();
@@ -222,7 +249,7 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     const int T_fixed = packed ? 0 : T;
 
     if (events && events[0] && cudaEventRecord(events[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
-    cudaError_t err = launch_chunk_table(cu_seqlens, num_seqs, T_fixed, slots, table,
+    cudaError_t err = launch_chunk_table(cu_seqlens, num_seqs, T_fixed, (long long)B * T, slots, table,
                                          seq_first_slot, status, stream);
     if (err != cudaSuccess) return KDA_ERR_CUDA;
     if (use_tc(dk, dtype))
@@ -233,8 +260,8 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     else
         err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
                                   final_state, T_fixed, H, dk, num_seqs, dtype, slots, table,
-                                  seq_first_slot, reinterpret_cast<float *>(region), pro, stream,
-                                  events);
+                                  seq_first_slot, reinterpret_cast<float *>(region), status, pro,
+                                  stream, events);
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

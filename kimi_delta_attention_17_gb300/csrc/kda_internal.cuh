@@ -113,7 +113,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // Fills `table` and `seq_first_slot` from cu_seqlens (device) or, when
 // cu_seqlens is NULL, from num_seqs sequences of length T_fixed, and clears
 // the status word.
-cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fixed,
+cudaError_t launch_chunk_table(const int32_t *cu_seqlens, int num_seqs, int T_fixed, long long tokens,
                                long long slots, ChunkEntry *table, int *seq_first_slot,
                                int *status, cudaStream_t stream);
 
@@ -124,8 +124,8 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 const int32_t *cu_seqlens, void *out, float *final_state,
                                 int T_fixed, int H, int d, int num_seqs, kda_dtype dtype,
                                 long long slots, const ChunkEntry *table,
-                                const int *seq_first_slot, float *region, const Prologue &pro,
-                                cudaStream_t stream, cudaEvent_t *events);
+                                const int *seq_first_slot, float *region, const int *status,
+                                const Prologue &pro, cudaStream_t stream, cudaEvent_t *events);
 
 // Tensor-core prefill (bf16 storage, d = 128).
 size_t tc_region_bytes();

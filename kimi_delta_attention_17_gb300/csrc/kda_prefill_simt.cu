@@ -211,7 +211,10 @@ __global__ void __launch_bounds__(kThreads)
 simt_state_pass(const float *__restrict__ ws, const int *__restrict__ seq_first_slot,
                 const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens,
                 int T_fixed, const float *init_state, OutT *__restrict__ out, float *final_state,
-                int H) {
+                int H, const int *__restrict__ status) {
+    // A call whose chunk table was refused (or that already failed) does
+    // nothing; the decision is taken once for the whole CTA.
+    if (__syncthreads_or(threadIdx.x == 0 && *status != 0)) return;
     constexpr int P = D + 1;
     // 1-D grid, sequences slowest in seq_order (longest first), then heads,
     // then the column slabs of one head.
@@ -299,8 +302,8 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
                      const float *beta, float scale, const float *init_state,
                      const int32_t *cu_seqlens, void *out, float *final_state, int T_fixed, int H,
                      int num_seqs, long long slots, const ChunkEntry *table,
-                     const int *seq_first_slot, float *region, const Prologue &pro,
-                     cudaStream_t stream, cudaEvent_t *events) {
+                     const int *seq_first_slot, float *region, const int *status,
+                     const Prologue &pro, cudaStream_t stream, cudaEvent_t *events) {
     constexpr size_t s1 = prep_smem_bytes<D>();
     constexpr size_t s2 = pass_smem_bytes<D>();
     // The shared-memory opt-ins, once per device and instance (nothing but
@@ -332,7 +335,7 @@ cudaError_t launch_t(const void *q, const void *k, const void *v, const float *g
         static_assert(D / kSlabCols <= kMaxStateTiles, "grid bound checked with kMaxStateTiles");
         simt_state_pass<D, InT><<<(unsigned)num_seqs * H * (D / kSlabCols), kThreads, s2, stream>>>(
             region, seq_first_slot, seq_first_slot + num_seqs + 1, cu_seqlens, T_fixed, init_state,
-            static_cast<InT *>(out), final_state, H);
+            static_cast<InT *>(out), final_state, H, status);
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
@@ -350,10 +353,10 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 const int32_t *cu_seqlens, void *out, float *final_state,
                                 int T_fixed, int H, int d, int num_seqs, kda_dtype dtype,
                                 long long slots, const ChunkEntry *table,
-                                const int *seq_first_slot, float *region, const Prologue &pro,
-                                cudaStream_t stream, cudaEvent_t *events) {
+                                const int *seq_first_slot, float *region, const int *status,
+                                const Prologue &pro, cudaStream_t stream, cudaEvent_t *events) {
 #define KDA_SIMT_ARGS q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, T_fixed, H, \
-                      num_seqs, slots, table, seq_first_slot, region, pro, stream, events
+                      num_seqs, slots, table, seq_first_slot, region, status, pro, stream, events
     if (dtype == KDA_DTYPE_BF16)
         return d == 128 ? launch_t<128, __nv_bfloat16>(KDA_SIMT_ARGS)
                         : launch_t<64, __nv_bfloat16>(KDA_SIMT_ARGS);

@@ -776,6 +776,9 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
               int T_fixed, const float *init_state, __nv_bfloat16 *__restrict__ out,
               float *final_state, int H, int *__restrict__ status, const SegPass sp) {
     extern __shared__ __align__(1024) unsigned char sm[];
+    // A call whose chunk table was refused (or that already failed) does
+    // nothing; the decision is taken once for the whole CTA.
+    if (__syncthreads_or(threadIdx.x == 0 && *status != 0)) return;
     // 1-D grid, sequences slowest in seq_order (longest first), then heads,
     // then segments, then the column tiles of one head and segment (adjacent:
     // they read the same tiles). A transfer launch has 2 D / kTN tiles: the
