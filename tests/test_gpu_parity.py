@@ -145,3 +145,15 @@ def test_decode_equals_prefill():
         assert np.abs(f64(out) - out_p[:, t]).max() <= 1e-4
     torch.cuda.synchronize()
     assert np.abs(f64(state) - fin_p).max() <= 1e-4
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f32")])
+def test_more_sequences_than_table_threads(d, dtype):
+    """1100 packed sequences of 0-70 tokens (some empty, some past one chunk):
+    more sequences than the chunk table kernel has threads, and more than it
+    ranks longest-first (their order is then the identity)."""
+    rng = np.random.default_rng(13)
+    lengths = tuple(int(x) for x in rng.integers(0, 71, size=1100))
+    spec = PrefillSpec("many sequences", H=1, d=d, fixed_lengths=lengths, dtype=dtype,
+                       init="normal0.1", seed=14)
+    check_prefill(spec)
