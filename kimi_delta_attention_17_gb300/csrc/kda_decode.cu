@@ -21,13 +21,18 @@ namespace {
 constexpr int kDecodeThreads = 128;
 constexpr int kSlab = 32;  // state columns per CTA
 
-// kOpts = false is the plain step (per-channel log-decay in g, no
-// normalisation), compiled without the option branches.
-template <int D, typename InT, bool kOpts>
+// Instances: kVar 0 is the plain step (per-channel log-decay in g, no
+// normalisation) and 2 the KDA layer's own prologue (per-channel decay from
+// gate logits through the log-sigmoid, q and k normalised), each compiled
+// with its options fixed; 1 takes every option at run time.
+constexpr int kDecPlain = 0, kDecRuntime = 1, kDecGated = 2;
+template <int D, typename InT, int kVar>
 __global__ void __launch_bounds__(kDecodeThreads, 7)
 decode_step_kernel(const InT *__restrict__ q, const InT *__restrict__ k, const InT *__restrict__ v,
                    const float *__restrict__ g, const float *__restrict__ beta, float scale,
                    float *__restrict__ state, InT *__restrict__ out, Prologue pro) {
+    constexpr bool kOpts = kVar != kDecPlain;
+    if (kVar == kDecGated) pro = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOGSIGMOID, 0.f, 1};
     constexpr int R = D / 16;  // rows per thread
     const int nh = blockIdx.x;           // (sequence, head) flattened
     const int col0 = blockIdx.y * kSlab;  // first state column of this slab
@@ -160,15 +165,20 @@ cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const f
                             const float *beta, float scale, float *state, void *out, int N, int H,
                             const Prologue &pro, cudaStream_t stream) {
     dim3 grid((unsigned)(N * H), D / kSlab);
-    const bool plain = pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOG && !pro.l2norm;
-    if (plain)
-        decode_step_kernel<D, InT, false><<<grid, kDecodeThreads, 0, stream>>>(
-            static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g,
-            beta, scale, state, static_cast<InT *>(out), pro);
-    else
-        decode_step_kernel<D, InT, true><<<grid, kDecodeThreads, 0, stream>>>(
-            static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g,
-            beta, scale, state, static_cast<InT *>(out), pro);
+    const bool chan = pro.decay == KDA_DECAY_CHANNEL;
+    const int var = chan && pro.gate == KDA_GATE_LOG && !pro.l2norm              ? kDecPlain
+                    : chan && pro.gate == KDA_GATE_LOGSIGMOID && pro.l2norm ? kDecGated
+                                                                               : kDecRuntime;
+#define KDA_DECODE_LAUNCH(V)                                                                   \
+    decode_step_kernel<D, InT, V><<<grid, kDecodeThreads, 0, stream>>>(                          \
+        static_cast<const InT *>(q), static_cast<const InT *>(k), static_cast<const InT *>(v), g, \
+        beta, scale, state, static_cast<InT *>(out), pro)
+    switch (var) {
+        case kDecPlain: KDA_DECODE_LAUNCH(kDecPlain); break;
+        case kDecGated: KDA_DECODE_LAUNCH(kDecGated); break;
+        default: KDA_DECODE_LAUNCH(kDecRuntime); break;
+    }
+#undef KDA_DECODE_LAUNCH
     return cudaGetLastError();
 }
 

@@ -122,8 +122,10 @@ __device__ __forceinline__ void st16(unsigned char *p, const float *x) {
 // form is compiled without the code of the others (the kernel must stay
 // within the instruction cache): 0 per-channel log-decay (KDA), 2 one
 // log-decay per head (Gated DeltaNet), 3 no decay (DeltaNet), all with g
-// holding log a and no normalisation; 1 takes every option at run time.
-constexpr int kVarChannel = 0, kVarRuntime = 1, kVarScalar = 2, kVarNone = 3;
+// holding log a and no normalisation; 4 per-channel decay from gate logits
+// through the log-sigmoid with q and k normalised (the KDA layer's own
+// prologue); 1 takes every option at run time.
+constexpr int kVarChannel = 0, kVarRuntime = 1, kVarScalar = 2, kVarNone = 3, kVarGated = 4;
 template <int kVar>
 __global__ void __launch_bounds__(kP1Threads, 1)
 tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -172,6 +174,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (kVar == kVarChannel) pro = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0.f, 0};
     if (kVar == kVarScalar) pro = Prologue{KDA_DECAY_SCALAR, KDA_GATE_LOG, 0.f, 0};
     if (kVar == kVarNone) pro = Prologue{KDA_DECAY_NONE, KDA_GATE_LOG, 0.f, 0};
+    if (kVar == kVarGated) pro = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOGSIGMOID, 0.f, 1};
     const bool g_tile = pro.decay == KDA_DECAY_CHANNEL;  // g arrives as a tile only per channel
     auto issue = [&](int hh, const ChunkEntry e) {
         if (tid != 0) return;
@@ -1207,6 +1210,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                 cudaSuccess ||
             (err = cudaFuncSetAttribute(tc_intra_chunk<kVarNone>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
+                cudaSuccess ||
+            (err = cudaFuncSetAttribute(tc_intra_chunk<kVarGated>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
                 cudaSuccess)
             return err;
         if ((err = cudaFuncSetAttribute(tc_state_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1236,6 +1242,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                 var = kVarNone;
             else if (pro.gate == KDA_GATE_LOG)
                 var = pro.decay == KDA_DECAY_CHANNEL ? kVarChannel : kVarScalar;
+        } else if (pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOGSIGMOID) {
+            var = kVarGated;
         }
         const int *used = seq_first_slot + num_seqs;
 #define KDA_P1_LAUNCH(V)                                                                        \
@@ -1245,6 +1253,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             case kVarChannel: KDA_P1_LAUNCH(kVarChannel); break;
             case kVarScalar: KDA_P1_LAUNCH(kVarScalar); break;
             case kVarNone: KDA_P1_LAUNCH(kVarNone); break;
+            case kVarGated: KDA_P1_LAUNCH(kVarGated); break;
             default: KDA_P1_LAUNCH(kVarRuntime); break;
         }
 #undef KDA_P1_LAUNCH
