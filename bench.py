@@ -124,6 +124,13 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
+            # The timed work starts once the sampler is producing samples (at most 3 s).
+            t0 = time.time()
+            while time.time() - t0 < 3.0 and self.proc.poll() is None:
+                self.fh.flush()
+                if os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.02)
         except (OSError, ValueError):
             self.proc = None
         return self
