@@ -73,3 +73,29 @@ def test_decode_workload():
         assert_parity(f64(outs[t]), ref_out, spec.dtype, "decode O step %d" % t)
     es = assert_parity(f64(state[seqs]), ref_state, spec.dtype, "decode state after %d steps" % spec.steps)
     print("\n%s: state after %d steps max|err| %.3g rel %.3g" % (spec.name, spec.steps, es[0], es[1]))
+
+
+def test_four_head_shard_parallel_prefix():
+    """The 131072-token prefill on 4 heads, as the benchmark times its
+    parallel-prefix variant (automatic: 6 segments of 342 chunks): two heads
+    against the oracle over all tokens, and all four against the serial chain."""
+    from kimi_delta_attention_17_gb300.inputs import with_
+    spec = with_(LONG_128K, H=4, name="prefill bf16 B=1 H=4 T=131072 d=128")
+    inp = make_prefill(spec)
+    dev = "cuda"
+    args = [inp[n].to(dev) for n in ("q", "k", "v", "g", "beta")]
+    out_p, fin_p = chunk_fwd(*args, inp["scale"], segments=0)
+    out_s, fin_s = chunk_fwd(*args, inp["scale"], segments=1)
+    torch.cuda.synchronize()
+    for a, b, what in ((out_p, out_s, "O"), (fin_p, fin_s, "final state")):
+        a64, b64 = a.double(), b.double()
+        rel = float(torch.linalg.norm(a64 - b64) / torch.linalg.norm(b64))
+        assert rel < 2e-4, (what, rel)
+    heads = [0, 3]
+    out_h, fin_h = f64(out_p[:, :, heads]), f64(fin_p[:, heads])
+    del out_p, fin_p, out_s, fin_s
+    ref_out, ref_fin = oracle_prefill(inp, heads=heads)
+    eo = assert_parity(out_h, ref_out, spec.dtype, "O")
+    es = assert_parity(fin_h, ref_fin, spec.dtype, "final state")
+    print("\n%s, parallel prefix: O max|err| %.3g rel %.3g; final state max|err| %.3g rel %.3g"
+          % (spec.name, eo[0], eo[1], es[0], es[1]))
