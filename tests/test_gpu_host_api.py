@@ -65,3 +65,20 @@ def test_decode_host_matches_device_steps():
             for t in range(spec.steps)]
     torch.cuda.synchronize()
     assert torch.equal(out_h, torch.stack(outs).cpu()) and torch.equal(s1, s2)
+
+
+@pytest.mark.slow
+def test_chunk_fwd_host_full_size_matches_device_call():
+    """The benchmark's end-to-end call at its size: the 131072-token, 32-head
+    prefill through pinned host buffers in 16384-token segments equals one
+    device call bit for bit."""
+    from kimi_delta_attention_17_gb300.inputs import LONG_128K
+    inp = make_prefill(LONG_128K)
+    h = _pin(inp, ("q", "k", "v", "g", "beta"))
+    out_h, fin_h = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
+                                  segment_tokens=16384)
+    torch.cuda.synchronize()
+    out_d, fin_d = chunk_fwd(*(h[n].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"])
+    torch.cuda.synchronize()
+    assert torch.equal(fin_h, fin_d.cpu())
+    assert torch.equal(out_h, out_d.cpu())
