@@ -706,19 +706,19 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 }
 
 // ---------------------------------------------------------------- phase 2
-// One CTA of 256 threads per (sequence, head, 32-column slab). Thread t owns
-// TMEM lane / state row t mod 128 and slab columns [16 s, 16 s + 16) with
-// s = t / 128. Per chunk, with S the state entering it:
+// One CTA of 576 threads per (sequence, head, 32-column slab) and, with the
+// segmented pass, per segment. Compute thread t owns TMEM lane / state row
+// 32 (w % 4) + (t % 32) of warp w = t / 32 and slab columns 8 (w / 4) .. + 7.
+// Per chunk, with S the state entering it:
 //   round trip 1:  D1 = [s Qbar; W] S          (rows 0-63: Qbar S, 64-127: W S)
 //                  Z  = U - W S                 (lanes 64-127)
 //   round trip 2:  D2 = Kbar^T Z,  D1[0:64] += H Z
 //                  S <- Diag(exp G_n) S + D2,  O = D1[0:64] = s Qbar S + H Z
 // ("Understanding Kimi Delta Attention", "The token outputs" and "One state
 // crosses the chunk boundary"). S and Z enter the MMAs as bf16 hi + lo pairs.
-// Warp roles: warps 0-15 compute (warp w reads TMEM lanes 32 (w % 4) ..
-// + 31 and owns state columns 8 (w / 4) .. + 7 of the slab); warp 16 issues
-// the MMAs; warp 17's lane 0 issues every bulk copy of the chunk tiles (a
-// copy's issue can hold its thread for a hundred cycles or more).
+// Warp roles: warps 0-15 compute; warp 16 issues the MMAs; warp 17's lane 0
+// issues every bulk copy of the chunk tiles (a copy's issue can hold its
+// thread for a hundred cycles or more).
 constexpr int kP2Compute = 512;
 constexpr int kP2MmaWarp = kP2Compute / 32;
 constexpr int kP2ProdWarp = kP2MmaWarp + 1;
