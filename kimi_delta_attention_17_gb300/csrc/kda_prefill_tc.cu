@@ -16,6 +16,8 @@
 //     Z = U - W S                               elementwise
 //     S <- Diag(exp(G_n)) S + Kbar^T Z          one MMA
 //     O = s Qbar S + H Z                        one MMA into the first one's rows
+//   (with few (sequence, head) chains the chunks are cut into segments whose
+//   affine maps are composed before the segments run in parallel: SegPass)
 //
 // Decay absorption with secondary chunking ("Kimi Delta Attention: a half-life
 // per channel", section "What changes in the kernel"): the per-channel pair
