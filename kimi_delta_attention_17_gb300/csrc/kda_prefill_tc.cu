@@ -169,6 +169,14 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // Operand descriptors, built once: a K step adds a constant to the
+    // address field (byte address / 16), which keeps descriptor arithmetic
+    // off the MMA issue path.
+    const uint64_t d_am = desc(smem_u32(sm + P1::am), kA1Lbo, kA1Sbo);
+    const uint64_t d_bm = desc(smem_u32(sm + P1::bm), kA1Lbo, kA1Sbo);
+    const uint64_t d_lt = desc(smem_u32(sm + P1::lt), kA2Lbo, kA2Sbo);
+    const uint64_t d_vt = desc(smem_u32(sm + P1::vt), kA2Lbo, kA2Sbo);
+    const uint64_t d_tb = desc(smem_u32(sm + P1::TBs), 1024, 128);
 
     // One thread fetches an item: four 3-D TMA tiles (128 channels x 1 head x
     // 64 tokens) land as dense [token][channel] rows. Tokens past the end of
@@ -404,8 +412,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t id = idesc_bf16(128, 160, 1, 1);
 #pragma unroll
             for (int s = 0; s < D / 16; ++s)
-                mma_bf16(tmem, desc(smem_u32(sm + P1::am) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo),
-                         desc(smem_u32(sm + P1::bm) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo), id, s > 0);
+                mma_bf16(tmem, d_am + s * (2 * kA1Lbo >> 4), d_bm + s * (2 * kA1Lbo >> 4), id, s > 0);
             commit(bar_mma);
         }
         // The staging rows are consumed: fetch the next item's while this one runs.
@@ -650,9 +657,9 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
             for (int s = 0; s < C / 16; ++s) {
-                const uint64_t b = desc(smem_u32(sm + P1::TBs) + s * 2 * 1024, 1024, 128);
-                mma_bf16(tmem + 0, desc(smem_u32(sm + P1::lt) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
-                mma_bf16(tmem + 64, desc(smem_u32(sm + P1::vt) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo), b, id, s > 0);
+                const uint64_t b = d_tb + s * (2 * 1024 >> 4);
+                mma_bf16(tmem + 0, d_lt + s * (2 * kA2Lbo >> 4), b, id, s > 0);
+                mma_bf16(tmem + 64, d_vt + s * (2 * kA2Lbo >> 4), b, id, s > 0);
             }
             commit(bar_mma);
         }
@@ -739,10 +746,10 @@ constexpr uint32_t kLoadBytes = (uint32_t)TcRegion::shared + kSlabBytes;
 static_assert(kBufU + (int)kSlabBytes <= kBufBytes, "chunk buffer too small");
 constexpr int kP2B1 = kP2Bufs * kBufBytes;      // S (hi | lo) bf16, MN-major [K = ch][N = 64]
 constexpr int kP2B2 = kP2B1 + 16384;            // [Z_hi | Z_lo] bf16, MN-major [K = token][N = 64]
-// mbarriers: loaded[3], free[3], first product, second product; then the
-// TMEM base and the error flag.
+// mbarriers: loaded[3], free[3], first product, second product, H Z product;
+// then the TMEM base and the error flag.
 constexpr int kP2Bar = kP2B2 + 8192;
-constexpr int kP2NBar = 2 * kP2Bufs + 2;
+constexpr int kP2NBar = 2 * kP2Bufs + 3;
 constexpr int kP2Tmem = kP2Bar + 8 * kP2NBar;
 constexpr int kP2Err = kP2Tmem + 4;
 constexpr int kP2Smem = kP2Err + 4;
@@ -840,20 +847,27 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     uint64_t *bar_fr = bar_ld + kP2Bufs;                            // [kP2Bufs] tiles consumed
     uint64_t *bar_m1 = bar_fr + kP2Bufs;                            // first product done
     uint64_t *bar_m2 = bar_m1 + 1;                                  // second product done
+    uint64_t *bar_m3 = bar_m2 + 1;                                  // H Z product done
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kP2Tmem);
     volatile int *err = reinterpret_cast<volatile int *>(sm + kP2Err);
-    // A bounded wait that is skipped once any warp has given up; a timeout
-    // raises the CTA's error flag and the call's status.
-    auto wait = [&](uint64_t *bar, uint32_t parity) {
-        if (*err) return;
+    // Bounded waits. A phase that has completed returns at once; otherwise the
+    // CTA's error flag is read first (a volatile shared read costs about as
+    // much as a barrier test, so it stays off the path of waits that succeed
+    // at once) and the wait is skipped once any warp has given up. A timeout
+    // raises the flag and the call's status.
+    auto wait = [&](uint64_t *bar, uint32_t parity) {  // false: gave up, or skipped after an error
+        if (mbar_test(bar, parity)) return true;
+        if (*err) return false;
         if (!mbar_wait(bar, parity)) {
             *err = 1;
             atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            return false;
         }
+        return true;
     };
-    auto spin = [&](uint64_t *bar, uint32_t parity) {  // the same, polling
-        if (*err) return;
-        if (!mbar_spin(bar, parity)) {
+    auto spin = [&](uint64_t *bar, uint32_t parity) {  // the same, polling first
+        if (mbar_poll(bar, parity) || *err) return;
+        if (!mbar_wait(bar, parity)) {
             *err = 1;
             atomicExch(status, (int)KDA_ERR_TIMEOUT);
         }
@@ -922,59 +936,71 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     } else if (warp == kP2MmaWarp) {
         // One lane issues; the whole warp keeps the named-barrier protocol, so
         // the compute warps never wait on a barrier that cannot complete.
+        // Descriptors of buffer 0's tiles and of the state-side operands are
+        // built once; a chunk adds its buffer's offset and a K step a constant
+        // (the address field is the byte address / 16).
+        const uint64_t d_a1 = desc(smem_u32(sm), kA1Lbo, kA1Sbo);
+        const uint64_t d_a2 = desc(smem_u32(sm + kBufA2), kA2Lbo, kA2Sbo);
+        const uint64_t d_h = desc(smem_u32(sm + kBufH), 1024, 128);
+        const uint64_t d_b1 = desc(smem_u32(B1), kB1Lbo, kB1Sbo);
+        const uint64_t d_b2 = desc(smem_u32(B2), kB2Lbo, kB2Sbo);
+        const uint32_t id1 = idesc_bf16(128, 2 * kTN, 1, 1), id2 = idesc_bf16(128, 2 * kTN, 0, 1);
+        // Chunk ch's tiles are waited for before its first product: chunk 0's
+        // here, every later one while the compute warps update the state of
+        // the chunk before it (off the chain of dependent steps).
+        bool ok_ld = true;
+        if (lane == 0 && nchunks > 0) ok_ld = wait(bar_ld, 0);
         for (int ch = 0; ch < nchunks; ++ch) {
             const int b = ch % kP2Bufs;
-            unsigned char *buf = sm + b * kBufBytes;
+            const uint64_t boff = (uint64_t)b * (kBufBytes >> 4);
             const uint32_t d1 = tmem + 64 * (ch & 1);
-            const uint32_t lp = (uint32_t)(ch / kP2Bufs) & 1;
-            if (lane == 0) {
-                wait(bar_ld + b, lp);
-                if (!*err) {
-                    // [s Qbar S; W S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
-                    fence_after();
-                    const uint32_t id = idesc_bf16(128, 2 * kTN, 1, 1);
+            if (lane == 0 && ok_ld) {
+                // [s Qbar S; W S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
+                fence_after();
 #pragma unroll
-                    for (int s = 0; s < D / 16; ++s)
-                        mma_bf16(d1, desc(smem_u32(buf) + s * 2 * kA1Lbo, kA1Lbo, kA1Sbo),
-                                 desc(smem_u32(B1) + s * 2 * kB1Lbo, kB1Lbo, kB1Sbo), id, s > 0);
-                    commit(bar_m1);  // also covers the previous chunk's H Z product
-                }
+                for (int s = 0; s < D / 16; ++s)
+                    mma_bf16(d1, d_a1 + boff + s * (2 * kA1Lbo >> 4), d_b1 + s * (2 * kB1Lbo >> 4),
+                             id1, s > 0);
+                commit(bar_m1);
             }
             __syncwarp();
             bar_sync(kBarZ, kP2Sync);  // Z of this chunk is in B2
             fence_after();
             if (lane == 0) {
-                // The compute warps saw the first product complete, and with it the
-                // previous chunk's H Z product: that chunk's buffer is free.
-                if (ch > 0) mbar_arrive(bar_fr + (ch - 1) % kP2Bufs);
-                if (!*err) {
+                if (ok_ld) {
                     // D2 = Kbar^T [Z_hi | Z_lo] (N = 64); then D1 += H [Z_hi | Z_lo], which
                     // adds H Z to the s Qbar S rows 0-63 (rows 64-127 take products of
                     // whatever follows H in shared memory; W S there is consumed).
-                    fence_after();
-                    const uint32_t id = idesc_bf16(128, 2 * kTN, 0, 1);
 #pragma unroll
                     for (int s = 0; s < C / 16; ++s)
-                        mma_bf16(tmem + kD2Col, desc(smem_u32(buf + kBufA2) + s * 2 * kA2Lbo, kA2Lbo, kA2Sbo),
-                                 desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, s > 0);
+                        mma_bf16(tmem + kD2Col, d_a2 + boff + s * (2 * kA2Lbo >> 4),
+                                 d_b2 + s * (2 * kB2Lbo >> 4), id2, s > 0);
                     commit(bar_m2);
-                    if (outputs) {
-#pragma unroll
-                        for (int s = 0; s < C / 16; ++s)
-                            mma_bf16(d1, desc(smem_u32(buf + kBufH) + s * 2 * 1024, 1024, 128),
-                                     desc(smem_u32(B2) + s * 2 * kB2Lbo, kB2Lbo, kB2Sbo), id, 1);
-                    }
                 }
+                // The compute warps saw this chunk's first product complete, and
+                // with it every product of the previous chunk: its buffer is free.
+                // Then the next chunk's tiles; both while the products run, before
+                // the H Z issue below, which holds this thread until the tensor
+                // pipe has taken it.
+                if (ch > 0) mbar_arrive(bar_fr + (ch - 1) % kP2Bufs);
+                const bool ok_next = ch + 1 >= nchunks || !ok_ld ||
+                                     wait(bar_ld + (ch + 1) % kP2Bufs, (uint32_t)((ch + 1) / kP2Bufs) & 1);
+                if (ok_ld && outputs) {
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        mma_bf16(d1, d_h + boff + s * (2 * 1024 >> 4), d_b2 + s * (2 * kB2Lbo >> 4),
+                                 id2, 1);
+                    commit(bar_m3);
+                }
+                ok_ld = ok_ld && ok_next;
             }
             __syncwarp();
             bar_sync(kBarS, kP2Sync);  // the new state is in B1
             fence_after();
         }
-        // The last chunk's H Z product: one more commit covers it.
-        if (lane == 0 && nchunks > 0 && !*err) commit(bar_m1);
         __syncwarp();
     } else {
-        uint32_t p1 = 0, p2 = 0;  // phases of the two product barriers
+        uint32_t p1 = 0, p2 = 0, p3 = 0;  // phases of the three product barriers
         const bool zrow = r >= 64;
         // Token outputs of chunk `ch` (rows 0-63 of its D1): s Qbar S + H Z.
         auto put_outputs = [&](int ch) {  // ch counts this segment's chunks
@@ -998,6 +1024,22 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             // The tiles landed long ago (the first product used them); this
             // thread's own wait makes the copied U and gamma visible to it.
             wait(bar_ld + b, (uint32_t)(ch / kP2Bufs) & 1);
+            // This chunk's U row and decay, read while the first product runs.
+            const float gam = reinterpret_cast<const float *>(buf + kBufGam)[r];
+            float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f), u1 = u0;
+            if (zrow && !ident) {
+                const float *Us = reinterpret_cast<const float *>(buf + kBufU);
+                u0 = *reinterpret_cast<const float4 *>(Us + slab_idx(r - 64, js));
+                u1 = *reinterpret_cast<const float4 *>(Us + slab_idx(r - 64, js + 4));
+            }
+            if (!zrow && outputs && ch > 0) {
+                // The previous chunk's outputs, complete once its H Z product is:
+                // written while this chunk's first product runs.
+                wait(bar_m3, p3);
+                p3 ^= 1;
+                fence_after();
+                put_outputs(ch - 1);
+            }
             spin(bar_m1, p1);
             p1 ^= 1;
             fence_after();
@@ -1007,10 +1049,6 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 float hi[8], lo[8];
                 tmem_ld8(d1 + lane_base + js, hi);
                 tmem_ld8(d1 + lane_base + kTN + js, lo);
-                const float *Us = reinterpret_cast<const float *>(buf + kBufU);
-                const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float4 u0 = ident ? zero4 : *reinterpret_cast<const float4 *>(Us + slab_idx(i, js));
-                const float4 u1 = ident ? zero4 : *reinterpret_cast<const float4 *>(Us + slab_idx(i, js + 4));
                 tmem_wait_ld();
                 const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                 float z[8];
@@ -1020,13 +1058,10 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 split8(z, zh, zl);
                 *reinterpret_cast<uint4 *>(B2 + mnmaj(js, i, kB2Lbo, kB2Sbo)) = zh;
                 *reinterpret_cast<uint4 *>(B2 + mnmaj(kTN + js, i, kB2Lbo, kB2Sbo)) = zl;
-            } else if (ch > 0 && outputs) {
-                put_outputs(ch - 1);  // overlaps this chunk's Z
             }
             fence_async_smem();
             fence_before();
             bar_arrive(kBarZ, kP2Sync);
-            const float gam = reinterpret_cast<const float *>(buf + kBufGam)[r];
             spin(bar_m2, p2);
             p2 ^= 1;
             fence_after();
@@ -1047,10 +1082,10 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             // made the product waits fall through.
             bar_sync(kBarS, kP2Sync);
         }
-        if (nchunks > 0) {
-            wait(bar_m1, p1);
+        if (nchunks > 0 && !zrow && outputs) {
+            wait(bar_m3, p3);
             fence_after();
-            if (!zrow && outputs) put_outputs(nchunks - 1);
+            put_outputs(nchunks - 1);
         }
         if (st_dst && !*err) {
             float *dst = st_dst + (size_t)r * dst_row + j0 + js;

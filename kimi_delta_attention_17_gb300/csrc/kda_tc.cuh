@@ -176,6 +176,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t parity, uint3
     return false;
 }
 
+// One non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint64_t *mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{.reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, "
+        "p;}"
+        : "=r"(done)
+        : "r"(smem_u32(mbar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Up to 4096 non-blocking tests; returns whether the phase completed.
+__device__ __forceinline__ bool mbar_poll(uint64_t *mbar, uint32_t parity) {
+    for (int it = 0; it < 4096; ++it)
+        if (mbar_test(mbar, parity)) return true;
+    return false;
+}
+
 // Bounded wait that polls with the non-blocking test (no suspend and wake-up
 // in between): for waits on the critical path whose phase completes within a
 // few hundred cycles. Falls back to the blocking wait after 4096 polls.
