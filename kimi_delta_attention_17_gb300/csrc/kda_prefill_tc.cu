@@ -99,7 +99,8 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int exch = 188704; // fp32 [2][4][128]: block totals and local references of G
     static constexpr int gsc = 192800;  // fp32 [64]: per-head log-decay of the item's tokens
     static constexpr int fac = 193056;  // fp32 [2 (k, q)][64]: reciprocal norms (q's times the scale)
-    static constexpr int bytes = 193568;
+    static constexpr int dg = 193568;   // fp32 [2 (A, H)][64][16]: diagonal blocks of steep items
+    static constexpr int bytes = 201760;
     // Reused once the first MMA has consumed am / bm:
     static constexpr int As = am;                // fp32 [64][68]: A
     static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
@@ -111,6 +112,11 @@ constexpr int kMS = 20;  // row stride (floats) of the M / R blocks: 8 rows hit 
 static_assert(P1::Rs + 3 * 16 * kMS * 4 <= P1::lt, "solve scratch overlaps L^T");
 static_assert(P1::bytes <= 232448, "phase-1 shared memory exceeds 227 KiB");
 constexpr int kAS = 68;  // row stride (floats) of A and T: 16-byte rows, 8 rows hit 8 bank groups
+// Largest total decay, in nats, of one channel over a 16-token block for which
+// the block-centred references are used: every factor then stays within
+// e^64 ~ 6e27, far inside fp32 and bf16 range. An item in which some channel's
+// block decays more takes the steep-decay form.
+constexpr float kSteepNats = 64.f;
 
 // (I, J) of column version v = I (I + 1) / 2 + J.
 __host__ __device__ constexpr int ver_I(int v) { return v < 1 ? 0 : v < 3 ? 1 : v < 6 ? 2 : 3; }
@@ -118,6 +124,67 @@ __host__ __device__ constexpr int ver_J(int v) { return v - ver_I(v) * (ver_I(v)
 
 __device__ __forceinline__ void st16(unsigned char *p, const float *x) {
     *reinterpret_cast<uint4 *>(p) = pack8(x);
+}
+
+// Steep item (kSteepNats): the diagonal 16 x 16 blocks of A and H in fp32,
+// sum_c x_ic k_jc exp(G_ic - G_jc) with the pair decay formed directly (its
+// exponent is <= 0 wherever j <= i), into P1::dg as raw sums (the readback
+// applies -beta and the causal masks). Reads the staged q, k rows, the
+// reciprocal norms and the in-block log-decay prefixes that replaced g in
+// staging. Thread (row i, group of 16 channels); the eight groups of a row
+// combine by shuffles. Kept out of line: it runs only for steep items and the
+// kernel's common path must stay within the instruction cache.
+__device__ __noinline__ void steep_diagonal_blocks(unsigned char *sm, int tid, int len, int l2norm,
+                                                   float scale) {
+    const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::q);
+    const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::k);
+    const float *gG = reinterpret_cast<const float *>(sm + P1::g);
+    const float *fac_s = reinterpret_cast<const float *>(sm + P1::fac);
+    float *dgA = reinterpret_cast<float *>(sm + P1::dg), *dgH = dgA + 64 * 16;
+    const int i = tid >> 3, cg = tid & 7, i0 = i & ~15;
+    const float fki = l2norm ? fac_s[i] : 1.f, fqi = l2norm ? fac_s[C + i] : scale;
+#pragma unroll 1
+    for (int jj = 0; jj < 16; ++jj) {
+        const int j = i0 + jj;
+        const float fkj = j < len ? (l2norm ? fac_s[j] : 1.f) : 0.f;
+        float a = 0.f, hq = 0.f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int c0 = 16 * cg + 8 * hf;
+            const uint4 kiw = *reinterpret_cast<const uint4 *>(ks + i * D + c0);
+            const uint4 qiw = *reinterpret_cast<const uint4 *>(qs + i * D + c0);
+            const uint4 kjw = *reinterpret_cast<const uint4 *>(ks + j * D + c0);
+            const float4 gi0 = *reinterpret_cast<const float4 *>(gG + i * D + c0);
+            const float4 gi1 = *reinterpret_cast<const float4 *>(gG + i * D + c0 + 4);
+            const float4 gj0 = *reinterpret_cast<const float4 *>(gG + j * D + c0);
+            const float4 gj1 = *reinterpret_cast<const float4 *>(gG + j * D + c0 + 4);
+            const uint32_t ki[4] = {kiw.x, kiw.y, kiw.z, kiw.w};
+            const uint32_t qi[4] = {qiw.x, qiw.y, qiw.z, qiw.w};
+            const uint32_t kj[4] = {kjw.x, kjw.y, kjw.z, kjw.w};
+            const float gi[8] = {gi0.x, gi0.y, gi0.z, gi0.w, gi1.x, gi1.y, gi1.z, gi1.w};
+            const float gj[8] = {gj0.x, gj0.y, gj0.z, gj0.w, gj1.x, gj1.y, gj1.z, gj1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t sh = (e & 1) ? 0u : 16u;  // element 2m sits in the low half
+                const float kie = __uint_as_float((ki[e >> 1] << sh) & 0xFFFF0000u);
+                const float qie = __uint_as_float((qi[e >> 1] << sh) & 0xFFFF0000u);
+                const float kje = __uint_as_float((kj[e >> 1] << sh) & 0xFFFF0000u);
+                const float w = kje * __expf(gi[e] - gj[e]);
+                a += kie * w;
+                hq += qie * w;
+            }
+        }
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, m);
+            hq += __shfl_xor_sync(0xffffffffu, hq, m);
+        }
+        if (cg == 0) {
+            const bool in = i < len;
+            dgA[i * 16 + jj] = in ? fki * fkj * a : 0.f;
+            dgH[i * 16 + jj] = in ? fqi * fkj * hq : 0.f;
+        }
+    }
 }
 
 // Instances: kVar fixes the options at compile time, so that each common
@@ -223,6 +290,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     ChunkEntry en = sn < used ? table[sn] : ce;
     uint32_t ld_phase = 0, mma_phase = 0;
     bool ok = true;
+    bool steep = false;  // this item takes the steep-decay form
     while (sl < used) {
         const int len = ce.len;
         int snn = sn, hnn = hn;  // the item after next
@@ -317,7 +385,11 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             tot_s[blk * D + c] = acc;
             ref_s[blk * D + c] = G[7];
-            __syncthreads();
+            // The block's total decay bounds every factor of its references
+            // (the log-decay is non-increasing within the block); over
+            // kSteepNats anywhere, the whole item takes the steep-decay form
+            // (the decision is CTA-uniform).
+            steep = __syncthreads_or(acc < -kSteepNats) != 0;
             // The table entry of the item after next and the next item's beta,
             // read here: a CTA barrier waits for its threads' loads, and the next
             // one is the whole elementwise pass away.
@@ -325,22 +397,36 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             enn = snn < used ? table[snn] : en;
             bn = sn < used ? beta_of(hn, en) : 0.f;
             gn = sn < used ? ghead_of(hn, en) : 0.f;
-            float R[4], off = 0.f;
+            // References of every block for this channel, as cumulative
+            // log-decays from the chunk start: rows (K-tilde, Q-tilde, L, Qbar)
+            // are scaled relative to Rr, columns (the versions, Kbar) relative
+            // to Rc. Normally both are the block's 8th token (no factor spans
+            // more than 8 tokens). In a steep item rows take the point before
+            // the block's first token and columns its last token, so that every
+            // factor is exp(x) with x <= 0; the diagonal blocks, which no single
+            // reference can split safely, are then formed directly below.
+            float Rr[4], Rc[4], off = 0.f;
 #pragma unroll
             for (int I = 0; I < 4; ++I) {
-                R[I] = off + ref_s[I * D + c];
-                off += tot_s[I * D + c];
+                const float rf = ref_s[I * D + c], tt = tot_s[I * D + c];
+                Rr[I] = steep ? off : off + rf;
+                Rc[I] = steep ? off + tt : off + rf;
+                off += tt;
             }
             const float Gend = off;
             // Per-channel block constants (see the header comment): the own
-            // block's reference, exp of it from the chunk start and to the chunk
-            // end, and the factors exp(R_I - R_blk) of the later blocks' versions.
-            const float Rs = blk == 0 ? R[0] : blk == 1 ? R[1] : blk == 2 ? R[2] : R[3];
-            const float Rl = G[7];  // the same reference, relative to the block start
-            const float Ps = __expf(Rs), Ys = __expf(Gend - Rs);
+            // block's references, exp of the row one from the chunk start and
+            // of the column one to the chunk end, and the factors
+            // exp(Rr_I - Rc_blk) of the later blocks' versions (the own block's
+            // version: 1, or 0 in a steep item).
+            const float Rrs = blk == 0 ? Rr[0] : blk == 1 ? Rr[1] : blk == 2 ? Rr[2] : Rr[3];
+            const float Rcs = blk == 0 ? Rc[0] : blk == 1 ? Rc[1] : blk == 2 ? Rc[2] : Rc[3];
+            // The same references relative to the block start.
+            const float Rlr = steep ? 0.f : G[7], Rlc = steep ? G[15] : G[7];
+            const float Ps = __expf(Rrs), Ys = __expf(Gend - Rcs);
             float Xv[4];
 #pragma unroll
-            for (int I = 0; I < 4; ++I) Xv[I] = I > blk ? __expf(R[I] - Rs) : 1.f;
+            for (int I = 0; I < 4; ++I) Xv[I] = I > blk ? __expf(Rr[I] - Rcs) : (steep ? 0.f : 1.f);
             // A runtime loop over the two 8-token groups (one copy of the body
             // keeps the kernel within the instruction cache).
 #pragma unroll 1
@@ -361,9 +447,8 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                     kv[r] = in ? fk * __bfloat162float(ks[i * D + c]) : 0.f;
                     qv[r] = in ? fq * __bfloat162float(qs[i * D + c]) : 0.f;
-                    const float x = Gi[r] - Rl;
-                    E[r] = __expf(x);
-                    kF[r] = kv[r] * __expf(-x);
+                    E[r] = __expf(Gi[r] - Rlr);
+                    kF[r] = kv[r] * __expf(Rlc - Gi[r]);
                 }
                 // V^T needs no arithmetic: move the bf16 bits (zero past the end).
                 const unsigned short *vb = reinterpret_cast<const unsigned short *>(vs);
@@ -401,6 +486,16 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 st16(reg + TcRegion::A1 + mnmaj(i0, c, kA1Lbo, kA1Sbo), t8);
             }
             if (blk == 3) reinterpret_cast<float *>(reg + TcRegion::Gam)[c] = __expf(Gend);
+            if (steep) {
+                // Steep item: the in-block log-decay prefixes replace g in
+                // staging (each thread its own entries), then the diagonal
+                // blocks are formed directly.
+                float *gG = reinterpret_cast<float *>(sm + P1::g);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) gG[(16 * blk + t) * D + c] = G[t];
+                __syncthreads();
+                steep_diagonal_blocks(sm, tid, len, pro.l2norm, scale);
+            }
         }
         fence_async_smem();
         fence_before();
@@ -442,6 +537,14 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 tmem_wait_ld();
                 if (ver_I(vv) != Iblk) continue;
                 const int J = ver_J(vv);
+                if (steep && J == Iblk) {  // formed directly in the elementwise pass
+                    const float *src = reinterpret_cast<const float *>(sm + P1::dg) + (isH ? 64 * 16 : 0) + i * 16;
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const float4 d4 = *reinterpret_cast<const float4 *>(src + 4 * f);
+                        x[4 * f] = d4.x; x[4 * f + 1] = d4.y; x[4 * f + 2] = d4.z; x[4 * f + 3] = d4.w;
+                    }
+                }
                 if (!isH) {
 #pragma unroll
                     for (int f = 0; f < 4; ++f) {

@@ -248,3 +248,63 @@ def make_decode_opts(spec: DecodeSpec, opts: OptionsSpec):
     q, k, v, beta, g = _opt_inputs(gen, (s, N), H, d, _dtype(spec.dtype), opts)
     state0 = 0.1 * torch.randn((N, H, d, d), generator=gen)
     return dict(q=q, k=k, v=v, g=g, beta=beta, state0=state0, scale=d ** -0.5)
+
+
+# ---------------------------------------------------------------- edge cases
+# Heads of the edge-case inputs take, in turn (head h gets kind h mod 6):
+#   0 "steep":   g ~ U[-40, 0] per channel and token (decays far beyond what a
+#                factor spanning several tokens can carry in fp32)
+#   1 "beta0":   beta = 0 (no write: pure decay of the initial state)
+#   2 "beta1":   beta = 1 (the overwrite case: with a unit key the write
+#                replaces the value stored under that key)
+#   3 "nodecay": g = 0 (a = 1, DeltaNet)
+#   4 "mixed":   each token, with probability 1/2, g ~ U[-40, 0] per channel,
+#                else the base gate (steep and gentle blocks side by side)
+#   5 "base":    the base recipe
+EDGE_KINDS = ("steep", "beta0", "beta1", "nodecay", "mixed", "base")
+
+
+def _edge_override(gen, beta, g):
+    """Applies the per-head kinds above, in place, to beta [..., H] and g
+    [..., H, d] drawn by the base recipe (draw order: steep g, mixed mask,
+    mixed g)."""
+    H = beta.shape[-1]
+    steep = -40.0 * torch.rand(g.shape, generator=gen)
+    mask = torch.rand(g.shape[:-1] + (1,), generator=gen) < 0.5
+    steep2 = -40.0 * torch.rand(g.shape, generator=gen)
+    for h in range(H):
+        kind = EDGE_KINDS[h % len(EDGE_KINDS)]
+        if kind == "steep":
+            g[..., h, :] = steep[..., h, :]
+        elif kind == "beta0":
+            beta[..., h] = 0.0
+        elif kind == "beta1":
+            beta[..., h] = 1.0
+        elif kind == "nodecay":
+            g[..., h, :] = 0.0
+        elif kind == "mixed":
+            g[..., h, :] = torch.where(mask[..., h, :], steep2[..., h, :], g[..., h, :])
+
+
+def make_prefill_edge(spec: PrefillSpec):
+    """make_prefill, then the per-head edge-case kinds of EDGE_KINDS (the
+    base draws first, in the usual order, then the overrides)."""
+    inp = make_prefill(spec)
+    gen = torch.Generator().manual_seed(spec.seed + 1000)
+    _edge_override(gen, inp["beta"], inp["g"])
+    return inp
+
+
+def make_decode_edge(spec: DecodeSpec):
+    """make_decode, then the per-head edge-case kinds of EDGE_KINDS."""
+    inp = make_decode(spec)
+    gen = torch.Generator().manual_seed(spec.seed + 1000)
+    _edge_override(gen, inp["beta"], inp["g"])
+    return inp
+
+
+def steep_logits(spec_seed, shape):
+    """Gate logits z ~ N(-12, 8^2) (seeded): through the log-sigmoid gate they
+    give per-token log-decays from about -40 to 0, mostly steep."""
+    gen = torch.Generator().manual_seed(spec_seed + 2000)
+    return -12.0 + 8.0 * torch.randn(shape, generator=gen)
