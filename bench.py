@@ -284,6 +284,95 @@ def to_dev(inp, dev, keys):
     return {k: (None if inp[k] is None else inp[k].to(dev)) for k in keys}
 
 
+def prefill_workload_variant(spec, dev, K, world, peaks):
+    """Device-resident and end-to-end timings of one prefill workload."""
+    from kimi_delta_attention_17_gb300 import chunk_fwd, chunk_fwd_host, workspace_size
+    inp = kin.make_prefill(spec)
+    keys = ("q", "k", "v", "g", "beta", "init_state", "cu_seqlens")
+    d_in = to_dev(inp, dev, keys)
+    B, T, H, d = inp["q"].shape
+    N = len(inp["lengths"])
+    out = torch.empty((B, T, H, d), dtype=inp["q"].dtype, device=dev)
+    fin = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, workspace_size(B, T, H, d, d, N, inp["q"].dtype)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def run(ev=None):
+        chunk_fwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"], inp["scale"],
+                  d_in["init_state"], d_in["cu_seqlens"], out=out, final_state=fin, workspace=ws,
+                  phase_events=ev)
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    phase = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    v0 = torch.cuda.Event(enable_timing=True)
+    v1 = torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for s in range(K):
+        run(phase[s])
+    v1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    vms = max_over_ranks(v0.elapsed_time(v1), dev) / K
+    tokens = B * T
+    vbytes = prefill_bytes(spec, tokens, N, inp["init_state"] is not None)
+    names = ["chunk_table", "intra_chunk", "state_pass"]
+    phases = {n: statistics.mean(phase[s][i].elapsed_time(phase[s][i + 1]) for s in range(K))
+              for i, n in enumerate(names)}
+    flops = prefill_flops(spec, tokens)
+    # end to end: pinned host inputs through kda_chunk_fwd_host (host cu_seqlens)
+    h_in = {k: (None if inp[k] is None else inp[k].pin_memory()) for k in keys}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    scratch = {}
+
+    def e2e():
+        chunk_fwd_host(h_in["q"], h_in["k"], h_in["v"], h_in["g"], h_in["beta"], inp["scale"],
+                       h_in["init_state"], h_in["cu_seqlens"], out=h_out, final_state=h_fin,
+                       window_tokens=16384, scratch=scratch)
+    e2e()
+    torch.cuda.synchronize()
+    e_steps = max(1, min(K, 3))
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ems = max_over_ranks(e0.elapsed_time(e1), dev) / e_steps
+    h2d = sum(x.numel() * x.element_size() for n, x in h_in.items()
+              if x is not None and n != "cu_seqlens")
+    d2h = h_out.numel() * h_out.element_size() + h_fin.numel() * h_fin.element_size()
+    res = {
+        "metric": "KDA prefill tokens/s (%s)" % spec.name,
+        "value": units_for_world(tokens, world) / (vms / 1e3), "unit": "tokens/s",
+        "ms_per_step": vms,
+        "config": {"workload": spec.name, "B": B, "T": T, "H": H, "d_k": d, "d_v": d,
+                   "num_seqs": N, "lengths": inp["lengths"] if inp["cu_seqlens"] is not None else None,
+                   "init_state": inp["init_state"] is not None},
+        "roofline": {"bound": "hbm", "kernel": "kda_chunk_fwd (all phases)",
+                     "achieved": vbytes / (vms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": None, "algorithmic_bytes_per_launch": vbytes,
+                     "phases_ms": phases,
+                     "tensor_tflops": flops / (vms / 1e3) / 1e12,
+                     "tensor_frac": flops / (vms / 1e3) / 1e12 / peaks["bf16_tflops"]},
+        "e2e": {"value": units_for_world(tokens, world) / (ems / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "kda_chunk_fwd_host (C ABI): pinned host buffers, 16384-token windows, "
+                       "copies overlapped with the compute"},
+    }
+    del d_in, out, fin, ws, h_in, h_out, h_fin, scratch
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_ours(args):
     from kimi_delta_attention_17_gb300 import (build, chunk_fwd, chunk_fwd_host, decode_host,
                                                decode_step, workspace_size)
@@ -400,6 +489,15 @@ def bench_ours(args):
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
                          "algorithmic_bytes_per_launch": vbytes}}
+
+    # The other prefill workloads of the metric's shape (the two-sequence
+    # 4096-token batch on 16 heads and the 8 packed sequences of mixed lengths
+    # on 32 heads), each timed on the device and end to end through the
+    # host-buffer entry point, with per-phase times.
+    if not args.no_workload_variants:
+        for vname, vspec in (("prefill_b2_h16_t4096", kin.PREFILL_B2),
+                             ("prefill_varlen_8seq_h32", kin.VARLEN_8)):
+            variants[vname] = prefill_workload_variant(vspec, dev, K, world, peaks)
 
     # Few (sequence, head) chains: the first 4 heads of the same inputs (a
     # 4-head shard of the workload) with one serial state chain per head and
@@ -548,24 +646,16 @@ def bench_ours(args):
     h_in = {k: (None if inp[k] is None else inp[k].pin_memory()) for k in keys}
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in h_in.values() if t is not None)
+    h2d = sum(t.numel() * t.element_size() for n, t in h_in.items()
+              if t is not None and n != "cu_seqlens")
     d2h = h_out.numel() * h_out.element_size() + h_fin.numel() * h_fin.element_size()
     e2e_steps = max(1, min(K, 3))
-    fixed_len = inp["cu_seqlens"] is None
     host_scratch = {}
 
     def e2e_prefill():
-        if fixed_len:
-            chunk_fwd_host(h_in["q"], h_in["k"], h_in["v"], h_in["g"], h_in["beta"],
-                           inp["scale"], h_in["init_state"], out=h_out, final_state=h_fin,
-                           segment_tokens=16384, scratch=host_scratch)
-        else:  # packed sequences: whole-call copies
-            for k in keys:
-                if h_in[k] is not None:
-                    d_in[k].copy_(h_in[k], non_blocking=True)
-            prefill()
-            h_out.copy_(out, non_blocking=True)
-            h_fin.copy_(fin, non_blocking=True)
+        chunk_fwd_host(h_in["q"], h_in["k"], h_in["v"], h_in["g"], h_in["beta"],
+                       inp["scale"], h_in["init_state"], h_in["cu_seqlens"], out=h_out,
+                       final_state=h_fin, window_tokens=16384, scratch=host_scratch)
     e2e_prefill()  # first call sizes the segment buffers
     barrier()
     torch.cuda.synchronize()
@@ -646,8 +736,8 @@ def bench_ours(args):
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": e2e_tok_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "api": "chunk_fwd_host, 16384-token segments, copies overlapped"
-                    if fixed_len else "chunk_fwd with whole-call copies"},
+                    "api": "kda_chunk_fwd_host (C ABI): pinned host buffers, 16384-token "
+                           "windows, copies overlapped with the compute"},
             "gpu_launches": 3 * K + steps_total,
             "clocks": clocks,
             "variants": variants,
@@ -661,7 +751,8 @@ def bench_ours(args):
                              "algorithmic_bytes_per_launch": dbytes},
                 "e2e": {"value": world * dspec.steps / (de_ms / 1e3), "unit": "steps/s",
                         "h2d_bytes_per_step": d_h2d, "d2h_bytes_per_step": d_d2h,
-                        "api": "decode_host, copies overlapped with the steps"},
+                        "api": "kda_decode_host (C ABI): pinned host buffers, step t+1's "
+                               "inputs in and step t-1's outputs out while step t runs"},
                 "cpu_baseline": {"value": dcpu_val, "unit": "steps/s", "cores": dcores,
                                  "kind": "oracle", "sample": dsample},
             },
@@ -720,6 +811,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(PREFILL_WORKLOADS), default="long")
     ap.add_argument("--T", type=int, default=0, help="override the per-sequence length")
+    ap.add_argument("--no-workload-variants", action="store_true",
+                    help="skip the other prefill workloads (two-sequence and packed)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target duration of the oracle baseline sample")
     args = ap.parse_args(argv)

@@ -39,11 +39,11 @@
  *    printed. Argument checks happen on the host before any CUDA call; a
  *    launch failure returns KDA_ERR_CUDA (the CUDA error is left for the
  *    caller's cudaGetLastError()/cudaPeekAtLastError() to inspect).
- *  - Inputs are expected to satisfy g <= 0 (finite), beta in [0, 1]; the
- *    chunked prefill factors each pair decay through references at most
- *    eight tokens away, so a per-token log-decay below about -10 can
- *    overflow fp32 in the bf16 path. Values outside these ranges are not
- *    checked on the device.
+ *  - Inputs are expected to satisfy g <= 0 (finite), beta in [0, 1]. Every
+ *    decay a = exp(g) in (0, 1] is handled exactly, however steep (the bf16
+ *    prefill takes a slower exact form for any 64-token chunk in which some
+ *    key channel decays by more than 64 nats within 16 tokens). Values
+ *    outside these ranges are not checked on the device.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -222,6 +222,49 @@ kda_status kda_chunk_fwd_opt(const void *q, const void *k, const void *v, const 
                              cudaStream_t stream, cudaEvent_t *events);
 
 /*
+ * Bytes of device workspace kda_chunk_fwd_host needs: two windows of
+ * `window_tokens` tokens (inputs, outputs and up to 16 sequence states in and
+ * out each) and the prefill's own workspace for one window. window_tokens must
+ * be a positive multiple of 64; options as in kda_chunk_fwd_opt (NULL: the
+ * defaults; only the decay family changes the size). Returns 0 for invalid or
+ * unsupported sizes.
+ */
+size_t kda_chunk_fwd_host_workspace_size(int H, int dk, int dv, kda_dtype dtype,
+                                         const kda_options *options, int window_tokens);
+
+/*
+ * The chunkwise prefill with every tensor in HOST memory (the end-to-end form
+ * of kda_chunk_fwd_opt): q, k, v, g, beta, init_state (nullable), out and
+ * final_state (nullable) have kda_chunk_fwd's layouts but are host pointers,
+ * pinned for the copies to overlap (pageable memory works, serialised).
+ * cu_seqlens, when given, is a HOST int32 array of num_seqs + 1 offsets (B must
+ * be 1), checked here: rising from 0 to T, else KDA_ERR_INVALID_ARGUMENT.
+ *
+ * The sequences are cut into windows of at most `window_tokens` tokens and 16
+ * sequence pieces, each cut falling on a multiple of 64 tokens from its
+ * sequence's start, so that every chunk is the one the single device call
+ * forms; the fp32 state of a cut sequence crosses windows on the device. Each
+ * window is one kda_chunk_fwd_opt call (serial state pass) on `stream`, while
+ * two copy streams created for the call move the next window's inputs in and
+ * the previous window's outputs and finished sequences' final states out. The
+ * results are bit-identical to kda_chunk_fwd_opt with options->segments = 1 on
+ * the same data, and valid once `stream` reaches the end of the call; the host
+ * inputs must stay unchanged until then.
+ *
+ * workspace: device memory of kda_chunk_fwd_host_workspace_size(...) bytes,
+ * 256-byte aligned. The call allocates no device memory; it creates two streams
+ * and a few events and releases them before returning (their work completes
+ * asynchronously). Errors as kda_chunk_fwd; a zero-length sequence's final
+ * state (its initial state, or zeros) is written on the host during the call.
+ */
+kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v, const float *g,
+                              const float *beta, float scale, const float *init_state,
+                              const int32_t *cu_seqlens, void *out, float *final_state, int B,
+                              int T, int H, int dk, int dv, int num_seqs, kda_dtype dtype,
+                              const kda_options *options, int window_tokens, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Capacity, in bytes, of the scratch array kda_chunk_fwd_noalloc uses: 64 MiB.
  * A problem fits when kda_chunk_fwd_workspace_size(...) for its sizes is at
  * most this value.
@@ -240,21 +283,43 @@ kda_status kda_chunk_fwd_opt(const void *q, const void *k, const void *v, const 
  * KDA_NOALLOC_SCRATCH_BYTES inside libkda.so, which every GPU that loads the
  * library holds until the process exits. This call allocates nothing (no
  * cudaMalloc, cudaFree or allocating library routine).
- *  - Sizes whose kda_chunk_fwd_workspace_size exceeds KDA_NOALLOC_SCRATCH_BYTES
- *    are rejected with KDA_ERR_WORKSPACE before any CUDA call.
- *  - The first call on each device resolves the array's device address with
- *    cudaGetSymbolAddress (with that device current) and caches it; make that
- *    first call before any stream capture begins.
+ *  - The arguments are checked first, exactly as kda_chunk_fwd checks them
+ *    (same codes, same order); then sizes whose kda_chunk_fwd_workspace_size
+ *    exceeds KDA_NOALLOC_SCRATCH_BYTES are rejected with KDA_ERR_WORKSPACE.
+ *    Both happen before any CUDA call.
+ *  - Every call looks up the array's device address in the current context
+ *    with cudaGetSymbolAddress (with the target device current), so a context
+ *    created later on the same device, for instance after cudaDeviceReset,
+ *    gets its own array. The first call in a context also loads the
+ *    library's device code there: make it before any stream capture begins.
  *  - Every call, on every stream, shares the one array and it keeps the last
  *    call's contents. Nothing in it needs to start at zero (each call rebuilds
  *    everything it reads), but calls whose work overlaps on the GPU race on it:
  *    order them on one stream or synchronise between them.
+ *  - The device-side status word of kda_chunk_fwd (bad cu_seqlens, a bounded
+ *    wait that gave up) lives at the start of the array; read it with
+ *    kda_chunk_fwd_noalloc_status.
  */
 kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, float scale, const float *init_state,
                                  const int32_t *cu_seqlens, void *out, float *final_state, int B,
                                  int T, int H, int dk, int dv, int num_seqs, kda_dtype dtype,
                                  cudaStream_t stream);
+
+/*
+ * The device-side status word of the last kda_chunk_fwd_noalloc call on this
+ * device (see kda_chunk_fwd's "Device-side status"): KDA_OK, or
+ * KDA_ERR_INVALID_ARGUMENT when cu_seqlens failed its check (nothing was
+ * computed or written), or KDA_ERR_TIMEOUT. The paper has no counterpart.
+ *  status  host int (pageable or pinned) that receives the word.
+ *  stream  the stream of that call: one 4-byte device-to-host copy is queued
+ *          on it, so the word is that call's once the stream has reached the
+ *          copy (after cudaStreamSynchronize(stream), or at return when
+ *          `status` is pageable memory).
+ * Allocates nothing. Returns KDA_ERR_INVALID_ARGUMENT for a NULL status and
+ * KDA_ERR_CUDA if the copy cannot be queued.
+ */
+kda_status kda_chunk_fwd_noalloc_status(int *status, cudaStream_t stream);
 
 /*
  * One recurrent decode step for N independent sequences ("Kimi Delta
@@ -281,6 +346,32 @@ kda_status kda_decode_step_opt(const void *q, const void *k, const void *v, cons
                                const float *beta, float scale, float *state, void *out, int N,
                                int H, int dk, int dv, kda_dtype dtype, const kda_options *options,
                                cudaStream_t stream);
+
+/*
+ * Bytes of device workspace kda_decode_host needs for N sequences (two steps'
+ * inputs and outputs). Returns 0 for invalid or unsupported sizes.
+ */
+size_t kda_decode_host_workspace_size(int N, int H, int dk, int dv, kda_dtype dtype,
+                                      const kda_options *options);
+
+/*
+ * `steps` successive decode steps (kda_decode_step_opt) with the per-step
+ * tensors in HOST memory: q, k [steps][N][H][dk], v [steps][N][H][dv], g
+ * [steps][N][H][dk] (or [steps][N][H] with KDA_DECAY_SCALAR; unused with
+ * KDA_DECAY_NONE), beta [steps][N][H], out [steps][N][H][dv] (written), all
+ * host pointers (pinned for overlap). `state` [N][H][dk][dv] fp32 is DEVICE
+ * memory, updated in place by every step. Step t + 1's inputs are copied in
+ * and step t - 1's outputs copied out on two copy streams created for the call
+ * while step t runs on `stream`; results are bit-identical to the device
+ * steps and valid once `stream` reaches the end of the call.
+ * workspace: device memory of kda_decode_host_workspace_size(...) bytes,
+ * 256-byte aligned; nothing is allocated on the device.
+ */
+kda_status kda_decode_host(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float scale, float *state, void *out, int steps,
+                           int N, int H, int dk, int dv, kda_dtype dtype,
+                           const kda_options *options, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
 
 /*
  * Output gate and RMS normalisation of the attention outputs, per token and

@@ -34,6 +34,14 @@ _SIGNATURES = {
                             + [ctypes.c_int] * 7 + [_vp, ctypes.c_size_t, _vp, _vp], ctypes.c_int),
     "kda_chunk_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
                               + [ctypes.c_int] * 7 + [_vp], ctypes.c_int),
+    "kda_chunk_fwd_noalloc_status": ([_vp, _vp], ctypes.c_int),
+    "kda_chunk_fwd_host_workspace_size": ([ctypes.c_int] * 4 + [_vp, ctypes.c_int], ctypes.c_size_t),
+    "kda_chunk_fwd_host": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
+                           + [ctypes.c_int] * 7 + [_vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp],
+                           ctypes.c_int),
+    "kda_decode_host_workspace_size": ([ctypes.c_int] * 5 + [_vp], ctypes.c_size_t),
+    "kda_decode_host": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]
+                        + [ctypes.c_int] * 6 + [_vp, _vp, ctypes.c_size_t, _vp], ctypes.c_int),
     "kda_decode_step": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp]
                         + [ctypes.c_int] * 5 + [_vp], ctypes.c_int),
     "kda_chunk_fwd_opt": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]

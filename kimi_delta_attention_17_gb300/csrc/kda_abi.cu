@@ -203,12 +203,15 @@ bool g_ok(const float *g, const Prologue &p, bool required) {
     return (a & (p.decay == KDA_DECAY_CHANNEL ? 15u : 3u)) == 0;
 }
 
-kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g,
-                          const float *beta, float scale, const float *init_state,
-                          const int32_t *cu_seqlens, void *out, float *final_state, int B, int T,
-                          int H, int dk, int dv, int num_seqs, kda_dtype dtype,
-                          const kda_options *options, void *workspace, size_t workspace_bytes,
-                          cudaStream_t stream, cudaEvent_t *events) {
+}  // namespace
+
+// Every check of a prefill call's arguments except those of the workspace, in
+// the order kda_chunk_fwd applies them (host only, no CUDA call).
+kda_status kda::chunk_fwd_check(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, float scale, const float *init_state,
+                                const int32_t *cu_seqlens, void *out, float *final_state, int B,
+                                int T, int H, int dk, int dv, int num_seqs, kda_dtype dtype,
+                                const kda_options *options) {
     Prologue pro;
     if (!make_prologue(options, &pro)) return KDA_ERR_INVALID_ARGUMENT;
     if (dtype != KDA_DTYPE_F32 && dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARGUMENT;
@@ -228,6 +231,22 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
     if ((reinterpret_cast<uintptr_t>(beta) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
     if ((reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return KDA_ERR_INVALID_ARGUMENT;
     if (!dims_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+namespace {
+
+kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, float scale, const float *init_state,
+                          const int32_t *cu_seqlens, void *out, float *final_state, int B, int T,
+                          int H, int dk, int dv, int num_seqs, kda_dtype dtype,
+                          const kda_options *options, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream, cudaEvent_t *events) {
+    const kda_status chk = chunk_fwd_check(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
+                                           final_state, B, T, H, dk, dv, num_seqs, dtype, options);
+    if (chk != KDA_OK) return chk;
+    Prologue pro;
+    make_prologue(options, &pro);
     const size_t need = kda_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dtype);
     if (!workspace || workspace_bytes < need) return KDA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_WORKSPACE;

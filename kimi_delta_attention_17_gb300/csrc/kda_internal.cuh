@@ -110,6 +110,14 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(x);
 }
 
+// The argument checks of kda_chunk_fwd_opt other than the workspace's, in the
+// same order (host only; no CUDA call). KDA_OK when the call may proceed.
+kda_status chunk_fwd_check(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, float scale, const float *init_state,
+                           const int32_t *cu_seqlens, void *out, float *final_state, int B, int T,
+                           int H, int dk, int dv, int num_seqs, kda_dtype dtype,
+                           const kda_options *options);
+
 // Fills `table` and `seq_first_slot` from cu_seqlens (device) or, when
 // cu_seqlens is NULL, from num_seqs sequences of length T_fixed, and clears
 // the status word.

@@ -5,8 +5,6 @@
 // statically). Its scratch lives in one file-scope device array that the
 // module carries; nothing here calls cudaMalloc, cudaFree or any allocating
 // library routine.
-#include <atomic>
-
 #include "kda_internal.cuh"
 
 namespace {
@@ -17,22 +15,16 @@ namespace {
 // cudaGetSymbolAddress below and only that address is handed to kernels.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void *> g_scratch_addr[kMaxDevices];
-
-// Resolves (once per device, with that device current) the device address of
-// the scratch array.
+// The device address of the scratch array in the current context. It is
+// resolved on every call rather than cached: a context created after a
+// cudaDeviceReset (or any other context on the same device) gets its own copy
+// of the module, and a cached address would point into the old one. The
+// lookup allocates nothing; the first call in a context also loads the
+// library's module there.
 cudaError_t scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (err != cudaSuccess) return err;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (err != cudaSuccess) return err;
-        g_scratch_addr[dev].store(p, std::memory_order_release);
-    }
     *out = p;
     return cudaSuccess;
 }
@@ -45,17 +37,30 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
                                             void *out, float *final_state, int B, int T, int H,
                                             int dk, int dv, int num_seqs, kda_dtype dtype,
                                             cudaStream_t stream) {
+    // The arguments first, exactly as kda_chunk_fwd checks them, so that both
+    // entry points report the same error for the same bad call; then the
+    // capacity of the fixed scratch.
+    const kda_status chk = kda::chunk_fwd_check(q, k, v, g, beta, scale, init_state, cu_seqlens,
+                                                out, final_state, B, T, H, dk, dv, num_seqs, dtype,
+                                                nullptr);
+    if (chk != KDA_OK) return chk;
     const size_t need = kda_chunk_fwd_workspace_size(B, T, H, dk, dv, num_seqs, dtype);
-    if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
-    if (need == 0) {
-        // Invalid or unsupported sizes: let the regular entry point report
-        // which (it returns before touching the device for these).
-        return kda_chunk_fwd(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B,
-                             T, H, dk, dv, num_seqs, dtype, nullptr, 0, stream);
-    }
+    if (need == 0 || need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
     return kda_chunk_fwd(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B, T,
                          H, dk, dv, num_seqs, dtype, scratch, (size_t)KDA_NOALLOC_SCRATCH_BYTES,
                          stream);
+}
+
+extern "C" kda_status kda_chunk_fwd_noalloc_status(int *status, cudaStream_t stream) {
+    if (!status) return KDA_ERR_INVALID_ARGUMENT;
+    void *scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return KDA_ERR_CUDA;
+    // The status word is the first int of the scratch (the workspace layout of
+    // kda_chunk_fwd): one 4-byte copy on the caller's stream, nothing allocated.
+    return cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDeviceToHost, stream) ==
+                   cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
 }

@@ -196,151 +196,120 @@ def output_gate_rmsnorm(o, z, weight=None, eps=1e-6, *, out=None, stream=None):
     return out
 
 
-def chunk_fwd_host(q, k, v, g, beta, scale, init_state=None, *, out=None, final_state=None,
-                   segment_tokens=16384, scratch=None, device=None, **options):
-    """Prefill from pinned host tensors, for fixed-length batches (q, k, v
-    [B, T, H, d], g, beta as in chunk_fwd; no cu_seqlens). Each sequence is cut
-    into segments of ``segment_tokens`` tokens (a multiple of the 64-token
-    chunk, so the chunking is that of one call, and with a serial state pass,
-    segments=1, every result is bit-identical to one call's); segment
-    i + 1 is copied to the device while segment i runs, and segment i's outputs
-    are copied back while segment i + 1 runs. The state crosses segments in
-    fp32 through init_state / final_state. Returns host tensors
-    (out [B, T, H, dv], final_state [B, H, dk, dv]); ``out`` / ``final_state``
-    may be given (pinned). ``scratch``: a dict kept between calls for the
-    device buffers and streams. ``options`` as in chunk_fwd."""
-    if segment_tokens <= 0 or segment_tokens % 64:
-        raise ValueError("segment_tokens must be a positive multiple of 64")
-    if q.dim() != 4 or q.shape[1] == 0:
-        raise ValueError("q must be [B, T, H, d] with T > 0")
+def _host(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError("%s must be a host tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def host_workspace_size(H, dk, dv, dtype, window_tokens=16384, decay="channel"):
+    """Bytes of device workspace kda_chunk_fwd_host needs (include/kda.h)."""
+    opts = _lib.Options(_lib.DECAY[decay], 0, 0.0, 0, 0)
+    return int(_lib.lib().kda_chunk_fwd_host_workspace_size(H, dk, dv, _DTYPES[dtype],
+                                                            ctypes.byref(opts), window_tokens))
+
+
+def chunk_fwd_host(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=None,
+                   final_state=None, window_tokens=16384, workspace=None, scratch=None,
+                   device=None, stream=None, decay="channel", gate="log", gate_lower=-5.0,
+                   l2norm_qk=False):
+    """The prefill with every tensor in host memory (kda_chunk_fwd_host): q, k,
+    v [B, T, H, d], g, beta as in chunk_fwd, init_state [N, H, dk, dv] or None,
+    cu_seqlens an int32 HOST tensor [N + 1] or None, all pinned for the copies
+    to overlap with the compute. The library cuts the sequences into windows of
+    ``window_tokens`` tokens (whole 64-token chunks of each sequence; results
+    bit-identical to one chunk_fwd call with segments=1) and pipelines the
+    copies. Returns host tensors (out [B, T, H, dv], final_state [N, H, dk, dv]);
+    ``out`` / ``final_state`` may be given (pinned). ``workspace``: a device
+    uint8 tensor of host_workspace_size(...) bytes, or None (allocated here,
+    and kept in the ``scratch`` dict when one is given)."""
+    if window_tokens <= 0 or window_tokens % 64:
+        raise ValueError("window_tokens must be a positive multiple of 64")
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta")):
-        if t.is_cuda or not t.is_pinned():
-            raise ValueError("%s must be a pinned host tensor" % n)
+        _host(t, n)
+    if g is not None:
+        _host(g, "g", torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [B, T, H, d]")
+    dtype = q.dtype
+    if dtype not in _DTYPES:
+        raise ValueError("q/k/v must be bfloat16 or float32")
     B, T, H, dk = q.shape
     dv = v.shape[-1]
+    if cu_seqlens is not None:
+        _host(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if init_state is not None:
+        _host(init_state, "init_state", torch.float32)
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
-    sc = {} if scratch is None else scratch
-    seg = min(segment_tokens, max(T, 1))
-    key = (seg, H, dk, dv, q.dtype, None if g is None else tuple(g.shape[2:]))
-    if sc.get("key") != key:
-        sc.clear()
-        sc["key"] = key
-        sc["streams"] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))  # in, out copies
-        sc["bufs"] = []
-        for _ in range(2):  # double-buffered device segments
-            b = {n: torch.empty((1, seg) + tuple(t.shape[2:]), dtype=t.dtype, device=dev)
-                 for n, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g))
-                 if t is not None}
-            b["out"] = torch.empty((1, seg, H, dv), dtype=q.dtype, device=dev)
-            sc["bufs"].append(b)
-        sc["state"] = torch.empty((1, H, dk, dv), dtype=torch.float32, device=dev)
-        sc["ws"] = torch.empty(max(1, workspace_size(1, seg, H, dk, dv, 1, q.dtype)),
-                               dtype=torch.uint8, device=dev)
-    s_in, s_out = sc["streams"]
-    comp = torch.cuda.current_stream(dev)
     if out is None:
-        out = torch.empty((B, T, H, dv), dtype=q.dtype).pin_memory()
+        out = torch.empty((B, T, H, dv), dtype=dtype).pin_memory()
     if final_state is None:
-        final_state = torch.empty((B, H, dk, dv), dtype=torch.float32).pin_memory()
-    state = sc["state"]
-    jobs = [(b, t0, min(T, t0 + seg)) for b in range(B) for t0 in range(0, max(T, 1), seg)]
-    freed = [torch.cuda.Event(), torch.cuda.Event()]  # buffer i may be refilled
-    drained = [torch.cuda.Event(), torch.cuda.Event()]  # buffer i's outputs copied out
-    for i in range(2):
-        freed[i].record(comp)
-        drained[i].record(comp)
-    for j, (b, t0, t1) in enumerate(jobs):
-        buf = sc["bufs"][j % 2]
-        n = t1 - t0
-        loaded = torch.cuda.Event()
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(freed[j % 2])
-            for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
-                if t is not None:
-                    buf[name][:, :n].copy_(t[b:b + 1, t0:t1], non_blocking=True)
-            loaded.record(s_in)
-        comp.wait_event(loaded)
-        comp.wait_event(drained[j % 2])
-        first = t0 == 0
-        if first and init_state is not None:
-            state.copy_(init_state[b:b + 1], non_blocking=True)
-        # [:, :n] of a (1, seg, ...) buffer is contiguous: the short last
-        # segment runs in place.
-        qd, kd, vd, bd = (buf[nm][:, :n] for nm in ("q", "k", "v", "beta"))
-        chunk_fwd(qd, kd, vd, None if g is None else buf["g"][:, :n], bd, scale,
-                  None if (first and init_state is None) else state, out=buf["out"][:, :n],
-                  final_state=state, workspace=sc["ws"], **options)
-        freed[j % 2].record(comp)
-        done = torch.cuda.Event()
-        done.record(comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(done)
-            out[b:b + 1, t0:t1].copy_(buf["out"][:, :n], non_blocking=True)
-            if t1 == T:
-                final_state[b:b + 1].copy_(state, non_blocking=True)
-            drained[j % 2].record(s_out)
-        if t1 == T:
-            # the next sequence's first segment must not overwrite this state early
-            comp.wait_stream(s_out)
-    comp.wait_stream(s_out)
+        final_state = torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory()
+    opts = _options(decay, gate, gate_lower, l2norm_qk, 1)
+    need = int(_lib.lib().kda_chunk_fwd_host_workspace_size(H, dk, dv, _DTYPES[dtype],
+                                                            ctypes.byref(opts), window_tokens))
+    if workspace is None:
+        sc = {} if scratch is None else scratch
+        key = ("prefill", need, dev)
+        if sc.get("key") != key:
+            sc.clear()
+            sc["key"] = key
+            sc["ws"] = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        workspace = sc["ws"]
+    _need(workspace, "workspace", torch.uint8, 1)
+    _lib.check("kda_chunk_fwd_host", _lib.lib().kda_chunk_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(init_state),
+        _ptr(cu_seqlens), _ptr(out), _ptr(final_state), B, T, H, dk, dv, N, _DTYPES[dtype],
+        ctypes.byref(opts), int(window_tokens), _ptr(workspace), workspace.numel(),
+        _stream_ptr(stream)))
     return out, final_state
 
 
-def decode_host(q, k, v, g, beta, scale, state, *, out=None, scratch=None, **options):
-    """``steps`` successive decode steps from pinned host tensors q, k [steps,
-    N, H, dk], v [steps, N, H, dv], g [steps, N, H, dk] (or per the decay
-    option), beta [steps, N, H]; ``state`` [N, H, dk, dv] fp32 stays on the
-    device and is updated in place. Step t + 1's inputs are copied in while
-    step t runs, and step t's outputs are copied back while step t + 1 runs.
+def decode_host(q, k, v, g, beta, scale, state, *, out=None, workspace=None, scratch=None,
+                stream=None, decay="channel", gate="log", gate_lower=-5.0, l2norm_qk=False):
+    """``steps`` successive decode steps with the per-step tensors in host
+    memory (kda_decode_host): q, k [steps, N, H, dk], v [steps, N, H, dv], g
+    [steps, N, H, dk] (or per the decay option), beta [steps, N, H], pinned;
+    ``state`` [N, H, dk, dv] fp32 stays on the device and is updated in place.
     Returns the host outputs [steps, N, H, dv] (``out``, pinned, may be given).
-    ``scratch``: a dict kept between calls for the device buffers and streams.
-    ``options`` as in decode_step."""
+    ``workspace``: a device uint8 tensor, or None (allocated here, and kept in
+    the ``scratch`` dict when one is given)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta")):
-        if t.is_cuda or not t.is_pinned():
-            raise ValueError("%s must be a pinned host tensor" % n)
-    steps = q.shape[0]
-    dev = state.device
-    sc = {} if scratch is None else scratch
-    key = (tuple(q.shape[1:]), tuple(v.shape[1:]), q.dtype, None if g is None else tuple(g.shape[1:]))
-    if sc.get("key") != key:
-        sc.clear()
-        sc["key"] = key
-        sc["streams"] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
-        sc["bufs"] = [{n: torch.empty(tuple(t.shape[1:]), dtype=t.dtype, device=dev)
-                       for n, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g))
-                       if t is not None} for _ in range(2)]
-        for b in sc["bufs"]:
-            b["out"] = torch.empty(tuple(v.shape[1:]), dtype=q.dtype, device=dev)
-    s_in, s_out = sc["streams"]
-    comp = torch.cuda.current_stream(dev)
+        _host(t, n)
+    if g is not None:
+        _host(g, "g", torch.float32)
+    if q.dim() != 4:
+        raise ValueError("q must be [steps, N, H, dk]")
+    _need(state, "state", torch.float32, 4)
+    dtype = q.dtype
+    if dtype not in _DTYPES:
+        raise ValueError("q/k/v must be bfloat16 or float32")
+    steps, N, H, dk = q.shape
+    dv = v.shape[-1]
     if out is None:
-        out = torch.empty(tuple(v.shape), dtype=q.dtype).pin_memory()
-    freed = [torch.cuda.Event(), torch.cuda.Event()]
-    drained = [torch.cuda.Event(), torch.cuda.Event()]
-    for i in range(2):
-        freed[i].record(comp)
-        drained[i].record(comp)
-    for t in range(steps):
-        buf = sc["bufs"][t % 2]
-        loaded = torch.cuda.Event()
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(freed[t % 2])
-            for name, x in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g)):
-                if x is not None:
-                    buf[name].copy_(x[t], non_blocking=True)
-            loaded.record(s_in)
-        comp.wait_event(loaded)
-        comp.wait_event(drained[t % 2])
-        decode_step(buf["q"], buf["k"], buf["v"], buf.get("g"), buf["beta"], scale, state,
-                    out=buf["out"], **options)
-        freed[t % 2].record(comp)
-        done = torch.cuda.Event()
-        done.record(comp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(done)
-            out[t].copy_(buf["out"], non_blocking=True)
-            drained[t % 2].record(s_out)
-    comp.wait_stream(s_out)
+        out = torch.empty(tuple(v.shape), dtype=dtype).pin_memory()
+    opts = _options(decay, gate, gate_lower, l2norm_qk, 0)
+    optp = None if opts is None else ctypes.byref(opts)
+    need = int(_lib.lib().kda_decode_host_workspace_size(N, H, dk, dv, _DTYPES[dtype], optp))
+    if workspace is None:
+        sc = {} if scratch is None else scratch
+        key = ("decode", need, state.device)
+        if sc.get("key") != key:
+            sc.clear()
+            sc["key"] = key
+            sc["ws"] = torch.empty(max(need, 1), dtype=torch.uint8, device=state.device)
+        workspace = sc["ws"]
+    _need(workspace, "workspace", torch.uint8, 1)
+    _lib.check("kda_decode_host", _lib.lib().kda_decode_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state), _ptr(out),
+        steps, N, H, dk, dv, _DTYPES[dtype], optp, _ptr(workspace), workspace.numel(),
+        _stream_ptr(stream)))
     return out
 
 

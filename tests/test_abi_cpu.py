@@ -174,3 +174,40 @@ def test_selftest_validation(L):
     assert f(FAKE + 2, 100, None) == INVALID
     assert f(FAKE, 0, None) == INVALID
     assert f(FAKE, (1 << 22) + 1, None) == INVALID
+
+
+def test_host_entry_points_check_arguments_before_any_cuda_call(L):
+    """kda_chunk_fwd_host / kda_decode_host validate on the host: window size,
+    workspace, host cu_seqlens (read here), sizes (runs without a GPU)."""
+    from kimi_delta_attention_17_gb300 import _lib as lib_mod
+    vp = ctypes.c_void_p
+    opts = lib_mod.Options(0, 0, 0.0, 0, 0)
+    hsz = L.kda_chunk_fwd_host_workspace_size
+    assert hsz(2, 128, 128, 1, None, 16384) > 0
+    assert hsz(2, 128, 128, 1, ctypes.byref(opts), 100) == 0     # window not a multiple of 64
+    assert hsz(2, 96, 96, 1, None, 64) == 0                       # unsupported head size
+    need = hsz(2, 64, 64, 1, None, 128)
+
+    def host(cu=None, N=1, B=1, T=64, window=128, wsb=None, dk=64):
+        return L.kda_chunk_fwd_host(FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, None, cu, FAKE, FAKE, B, T, 2,
+                                    dk, dk, N, 1, None, window, FAKE,
+                                    need if wsb is None else wsb, None)
+    assert host(window=100) == INVALID
+    assert host(wsb=need - 1) == WORKSPACE
+    assert host(dk=96) == UNSUPPORTED
+    bad = (ctypes.c_int32 * 3)(0, 40, 30)                          # decreasing offsets
+    assert host(cu=bad, N=2, T=30) == INVALID
+    short = (ctypes.c_int32 * 3)(0, 20, 50)                        # ends before T
+    assert host(cu=short, N=2, T=64) == INVALID
+    assert host(cu=short, N=2, B=2, T=25) == INVALID               # packed needs B == 1
+    dsz = L.kda_decode_host_workspace_size
+    assert dsz(4, 2, 128, 128, 1, None) > 0 and dsz(0, 2, 128, 128, 1, None) == 0
+    dneed = dsz(4, 2, 64, 64, 1, None)
+
+    def dec(steps=3, N=4, wsb=None, g=FAKE):
+        return L.kda_decode_host(FAKE, FAKE, FAKE, g, FAKE, 0.1, FAKE, FAKE, steps, N, 2, 64, 64, 1,
+                                 None, FAKE, dneed if wsb is None else wsb, None)
+    assert dec(steps=-1) == INVALID
+    assert dec(steps=0) == 0                                       # nothing to do
+    assert dec(wsb=dneed - 1) == WORKSPACE
+    assert dec(g=None) == INVALID

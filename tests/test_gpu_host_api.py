@@ -1,6 +1,8 @@
-"""The host-buffer APIs (chunk_fwd_host, decode_host) pipeline copies with the
-compute; their results are bit-identical to the device-tensor calls: segments
-are whole 64-token chunks and the fp32 state crosses them unchanged."""
+"""The host-buffer entry points of the C ABI (kda_chunk_fwd_host,
+kda_decode_host, through their thin Python wrappers) pipeline copies with the
+compute; their results are bit-identical to the device-tensor calls: windows
+cut sequences only at whole 64-token chunks and the fp32 state crosses them
+unchanged."""
 import pytest
 import torch
 
@@ -30,15 +32,38 @@ def test_chunk_fwd_host_matches_device_call(dtype, d):
     h = _pin(inp, ("q", "k", "v", "g", "beta", "init_state"))
     scratch = {}
     out_h, fin_h = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
-                                  h["init_state"], segment_tokens=128, scratch=scratch)
+                                  h["init_state"], window_tokens=128, scratch=scratch)
     out_h2, _ = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
-                               h["init_state"], segment_tokens=128, scratch=scratch)
+                               h["init_state"], window_tokens=128, scratch=scratch)
     torch.cuda.synchronize()
     out_d, fin_d = chunk_fwd(*(inp[n].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"],
-                             inp["init_state"].cuda())
+                             inp["init_state"].cuda(), segments=1)
     torch.cuda.synchronize()
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(fin_h, fin_d.cpu())
     assert torch.equal(out_h2, out_h)
+
+
+@pytest.mark.parametrize("window", [64, 192, 16384])
+@pytest.mark.parametrize("with_init", [True, False])
+def test_chunk_fwd_host_packed_sequences(window, with_init):
+    """Packed sequences (empty ones, ones shorter than a chunk, ones crossing
+    several windows, more pieces than a window holds) through host cu_seqlens:
+    bit-identical to one packed device call."""
+    lengths = (0, 1, 63, 64, 65, 130, 0, 200, 17) + (5,) * 20 + (300,)
+    spec = PrefillSpec("host packed", H=2, d=128, fixed_lengths=lengths, dtype="bf16",
+                       init="normal0.1" if with_init else "zero", seed=23)
+    inp = make_prefill(spec)
+    h = _pin(inp, ("q", "k", "v", "g", "beta", "init_state"))
+    cu_h = inp["cu_seqlens"].clone()
+    out_h, fin_h = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
+                                  h["init_state"], cu_h, window_tokens=window)
+    torch.cuda.synchronize()
+    init_d = None if inp["init_state"] is None else inp["init_state"].cuda()
+    out_d, fin_d = chunk_fwd(*(inp[n].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"],
+                             init_d, inp["cu_seqlens"].cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu())
+    assert torch.equal(fin_h, fin_d.cpu())
 
 
 def test_chunk_fwd_host_with_options():
@@ -46,10 +71,10 @@ def test_chunk_fwd_host_with_options():
     inp = make_prefill_opts(PrefillSpec("host-opt", H=2, d=128, B=1, T=200, seed=20), opts)
     h = _pin(inp, ("q", "k", "v", "g", "beta"))
     out_h, fin_h = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
-                                  segment_tokens=64, **opts.kwargs())
+                                  window_tokens=64, **opts.kwargs())
     torch.cuda.synchronize()
     out_d, fin_d = chunk_fwd(*(inp[n].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"],
-                             **opts.kwargs())
+                             segments=1, **opts.kwargs())
     torch.cuda.synchronize()
     assert torch.equal(out_h, out_d.cpu()) and torch.equal(fin_h, fin_d.cpu())
 
@@ -70,15 +95,16 @@ def test_decode_host_matches_device_steps():
 @pytest.mark.slow
 def test_chunk_fwd_host_full_size_matches_device_call():
     """The benchmark's end-to-end call at its size: the 131072-token, 32-head
-    prefill through pinned host buffers in 16384-token segments equals one
+    prefill through pinned host buffers in 16384-token windows equals one
     device call bit for bit."""
     from kimi_delta_attention_17_gb300.inputs import LONG_128K
     inp = make_prefill(LONG_128K)
     h = _pin(inp, ("q", "k", "v", "g", "beta"))
     out_h, fin_h = chunk_fwd_host(h["q"], h["k"], h["v"], h["g"], h["beta"], inp["scale"],
-                                  segment_tokens=16384)
+                                  window_tokens=16384)
     torch.cuda.synchronize()
-    out_d, fin_d = chunk_fwd(*(h[n].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"])
+    out_d, fin_d = chunk_fwd(*(h[n].cuda() for n in ("q", "k", "v", "g", "beta")), inp["scale"],
+                             segments=1)
     torch.cuda.synchronize()
     assert torch.equal(fin_h, fin_d.cpu())
     assert torch.equal(out_h, out_d.cpu())

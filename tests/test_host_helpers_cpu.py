@@ -16,21 +16,23 @@ def test_chunk_fwd_host_rejects_bad_arguments():
     beta = _host(1, 128, 2, dtype=torch.float32)
     g = _host(1, 128, 2, 64, dtype=torch.float32)
     with pytest.raises(ValueError, match="multiple of 64"):
-        chunk_fwd_host(q, q, q, g, beta, 0.125, segment_tokens=100)
+        chunk_fwd_host(q, q, q, g, beta, 0.125, window_tokens=100)
     with pytest.raises(ValueError, match="multiple of 64"):
-        chunk_fwd_host(q, q, q, g, beta, 0.125, segment_tokens=0)
-    with pytest.raises(ValueError, match="T > 0"):
-        chunk_fwd_host(_host(1, 0, 2, 64), q, q, g, beta, 0.125)
-    with pytest.raises(ValueError, match="pinned host tensor"):
-        chunk_fwd_host(q, q, q, g, beta, 0.125)
+        chunk_fwd_host(q, q, q, g, beta, 0.125, window_tokens=0)
+    with pytest.raises(ValueError, match="host tensor"):
+        chunk_fwd_host(q, q, q, g, beta.to("meta"), 0.125)
+    with pytest.raises(ValueError, match="cu_seqlens must be torch.int32"):
+        chunk_fwd_host(q, q, q, g, beta, 0.125, cu_seqlens=torch.zeros(2, dtype=torch.int64))
 
 
-def test_decode_host_rejects_pageable_inputs():
+def test_decode_host_rejects_bad_arguments():
     q = _host(3, 2, 2, 64)
     beta = _host(3, 2, 2, dtype=torch.float32)
     state = torch.zeros(2, 2, 64, 64)
-    with pytest.raises(ValueError, match="pinned host tensor"):
-        decode_host(q, q, q, None, beta, 0.125, state)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        decode_host(q, q, q, None, beta, 0.125, state)  # the state lives on the device
+    with pytest.raises(ValueError, match="steps, N, H, dk"):
+        decode_host(_host(2, 2, 64), q, q, None, beta, 0.125, state.to("meta"))
 
 
 def test_decode_graph_rejects_bad_shapes():

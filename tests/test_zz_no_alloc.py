@@ -18,6 +18,7 @@ from kimi_delta_attention_17_gb300.inputs import PrefillSpec, make_prefill
 from tests.helpers import assert_parity, f64
 
 KDA_NOALLOC_SCRATCH_BYTES = 64 << 20
+KDA_ERR_INVALID_ARGUMENT = 1
 KDA_ERR_WORKSPACE = 3
 
 
@@ -39,6 +40,51 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     st = L.kda_chunk_fwd_noalloc(fake, fake, fake, fake, fake, 0.1, None, None, fake, fake,
                                  B, T, H, d, d, 1, 1, None)
     assert st == KDA_ERR_WORKSPACE
+
+
+def test_noalloc_checks_arguments_before_capacity():
+    """A bad argument is reported as kda_chunk_fwd reports it, whatever the
+    size: a misaligned q with a problem too large for the scratch gives
+    KDA_ERR_INVALID_ARGUMENT from both entry points (runs without a GPU)."""
+    build.build()
+    L = _lib.lib()
+    B, T, H, d = 1, 1 << 20, 32, 128
+    fake, bad = 1 << 20, (1 << 20) + 4
+    args = (bad, fake, fake, fake, fake, 0.1, None, None, fake, fake, B, T, H, d, d, 1, 1)
+    assert L.kda_chunk_fwd_noalloc(*args, None) == KDA_ERR_INVALID_ARGUMENT
+    assert L.kda_chunk_fwd(*args, fake, 1 << 40, None) == KDA_ERR_INVALID_ARGUMENT
+    assert L.kda_chunk_fwd_noalloc_status(None, None) == KDA_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_bad_offsets_through_its_status_word():
+    """Decreasing packed offsets: the call returns KDA_OK (the offsets live on
+    the device), computes nothing, and the status word read through
+    kda_chunk_fwd_noalloc_status says KDA_ERR_INVALID_ARGUMENT; a good call
+    afterwards reads KDA_OK."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    L = _lib.lib()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    inp = make_prefill(PrefillSpec("noalloc status", H=2, d=128, fixed_lengths=(70, 50, 30),
+                                   dtype="bf16", init="normal0.1", seed=33))
+    B, T, H, d = inp["q"].shape
+    t = {n: inp[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    t["init"] = inp["init_state"].to(dev)
+    t["out"] = torch.zeros_like(t["v"])
+    t["fin"] = torch.zeros_like(t["init"])
+    word = ctypes.c_int(-1)
+    for cu, want in (([0, 70, 60, 150], KDA_ERR_INVALID_ARGUMENT), ([0, 70, 120, 150], 0)):
+        t["cu"] = torch.tensor(cu, dtype=torch.int32, device=dev)
+        st = _noalloc(L, t, inp["scale"], B, T, H, d, 3, _lib.DTYPE_BF16, stream.cuda_stream)
+        assert st == 0, _lib.STATUS_NAMES.get(st, st)
+        assert L.kda_chunk_fwd_noalloc_status(ctypes.byref(word), stream.cuda_stream) == 0
+        torch.cuda.synchronize()
+        assert word.value == want
+        if want:
+            assert not t["out"].any() and not t["fin"].any()  # nothing written
 
 
 @pytest.mark.gpu
