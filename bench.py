@@ -564,7 +564,36 @@ def bench_ours(args):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": ebytes / (ems / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
                      "algorithmic_bytes_per_launch": ebytes}}
-    del zgate, eout
+    # The same gate fused into the prefill (kda_chunk_fwd_gated): the outputs
+    # leave the state pass gated and normalised, so o is written once and
+    # never re-read.
+    fout = torch.empty_like(out)
+
+    def fused_prefill():
+        chunk_fwd(d_in["q"], d_in["k"], d_in["v"], d_in["g"], d_in["beta"], inp["scale"],
+                  d_in["init_state"], d_in["cu_seqlens"], out=fout, final_state=fin, workspace=ws,
+                  out_gate=zgate, norm_weight=wnorm)
+    fused_prefill()
+    torch.cuda.synchronize()
+    v0 = torch.cuda.Event(enable_timing=True)
+    v1 = torch.cuda.Event(enable_timing=True)
+    v0.record(stream)
+    for _ in range(K):
+        fused_prefill()
+    v1.record(stream)
+    torch.cuda.synchronize()
+    fms = max_over_ranks(v0.elapsed_time(v1), dev) / K
+    fbytes = prefill_bytes(spec, tokens, N, inp["init_state"] is not None) + \
+        out.numel() * out.element_size() + wnorm.numel() * 4   # + z read
+    variants["prefill_fused_gate_rmsnorm"] = {
+        "metric": "KDA prefill with fused output gate + RMSNorm, tokens/s (%s)" % spec.name,
+        "value": units_for_world(tokens, world) / (fms / 1e3), "unit": "tokens/s",
+        "ms_per_step": fms,
+        "roofline": {"bound": "hbm", "achieved": fbytes / (fms / 1e3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": fbytes / (fms / 1e3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                     "algorithmic_bytes_per_launch": fbytes}}
+    del zgate, eout, fout
 
     def decode_fused():
         for t in range(dspec.steps):

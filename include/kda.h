@@ -265,6 +265,36 @@ kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v, const
                               size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * kda_chunk_fwd_opt whose outputs leave through the output gate and RMS
+ * normalisation of the module around the scan ("Understanding Kimi Delta
+ * Attention", closing remarks: output gating and RMS normalisation):
+ *
+ *     out_t = w o (o_t / sqrt(mean_c o_t,c^2 + eps)) o sigmoid(z_t)
+ *
+ * per token and head over the dv channels, o_t the scan's output. Same
+ * arguments as kda_chunk_fwd_opt plus
+ *  z       [tokens][H][dv], dtype: gate logits (16-byte aligned; not read when
+ *          there are no tokens)
+ *  weight  [dv] fp32 per-channel scale shared by the heads, or NULL (ones)
+ *  eps     finite, > 0 (1e-6 is customary)
+ * On the tensor-core path (bf16, d = 128) the gate is applied inside the state
+ * pass, from the fp32 outputs, before the single write of `out`: the four
+ * CTAs that hold a head's 128 output columns form a thread-block cluster and
+ * exchange per-row sums of squares through distributed shared memory. The
+ * state then crosses chunks in one serial chain (options->segments is
+ * ignored). On the fp32 path the gate is a pass over the written outputs
+ * (kda_output_gate_rmsnorm in place). The ungated outputs are not kept.
+ * Workspace and errors as kda_chunk_fwd; eps, z and weight are checked first.
+ */
+kda_status kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const float *g,
+                               const float *beta, float scale, const float *init_state,
+                               const int32_t *cu_seqlens, const void *z, const float *weight,
+                               float eps, void *out, float *final_state, int B, int T, int H,
+                               int dk, int dv, int num_seqs, kda_dtype dtype,
+                               const kda_options *options, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream, cudaEvent_t *events);
+
+/*
  * Capacity, in bytes, of the scratch array kda_chunk_fwd_noalloc uses: 64 MiB.
  * A problem fits when kda_chunk_fwd_workspace_size(...) for its sizes is at
  * most this value.

@@ -35,6 +35,9 @@ _SIGNATURES = {
     "kda_chunk_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
                               + [ctypes.c_int] * 7 + [_vp], ctypes.c_int),
     "kda_chunk_fwd_noalloc_status": ([_vp, _vp], ctypes.c_int),
+    "kda_chunk_fwd_gated": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp,
+                             ctypes.c_float, _vp, _vp] + [ctypes.c_int] * 7
+                            + [_vp, _vp, ctypes.c_size_t, _vp, _vp], ctypes.c_int),
     "kda_chunk_fwd_host_workspace_size": ([ctypes.c_int] * 4 + [_vp, ctypes.c_int], ctypes.c_size_t),
     "kda_chunk_fwd_host": ([_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _vp, _vp]
                            + [ctypes.c_int] * 7 + [_vp, ctypes.c_int, _vp, ctypes.c_size_t, _vp],

@@ -241,7 +241,8 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
                           const int32_t *cu_seqlens, void *out, float *final_state, int B, int T,
                           int H, int dk, int dv, int num_seqs, kda_dtype dtype,
                           const kda_options *options, void *workspace, size_t workspace_bytes,
-                          cudaStream_t stream, cudaEvent_t *events) {
+                          cudaStream_t stream, cudaEvent_t *events,
+                          const GateParams &gate = GateParams{nullptr, nullptr, 0.f}) {
     const kda_status chk = chunk_fwd_check(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
                                            final_state, B, T, H, dk, dv, num_seqs, dtype, options);
     if (chk != KDA_OK) return chk;
@@ -275,12 +276,18 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
         err = launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
                                 T_fixed, (long long)B * T, H, num_seqs, slots, table, seq_first_slot,
                                 reinterpret_cast<unsigned char *>(region), status, pro,
-                                options ? options->segments : 0, seg_max, seg_ws, stream, events);
-    else
+                                options ? options->segments : 0, seg_max, seg_ws, gate, stream,
+                                events);
+    else {
         err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
                                   final_state, T_fixed, H, dk, num_seqs, dtype, slots, table,
                                   seq_first_slot, reinterpret_cast<float *>(region), status, pro,
                                   stream, events);
+        // The fp32 path applies the output gate as a pass over its outputs.
+        if (err == cudaSuccess && gate.z)
+            err = launch_output_gate_rmsnorm(out, gate.z, gate.w, gate.eps, out, (long long)B * T * H,
+                                             dv, dtype, stream);
+    }
     return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -320,6 +327,25 @@ extern "C" kda_status kda_chunk_fwd_opt(const void *q, const void *k, const void
     return chunk_fwd_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B, T,
                           H, dk, dv, num_seqs, dtype, options, workspace, workspace_bytes, stream,
                           events);
+}
+
+extern "C" kda_status kda_chunk_fwd_gated(const void *q, const void *k, const void *v,
+                                          const float *g, const float *beta, float scale,
+                                          const float *init_state, const int32_t *cu_seqlens,
+                                          const void *z, const float *weight, float eps, void *out,
+                                          float *final_state, int B, int T, int H, int dk, int dv,
+                                          int num_seqs, kda_dtype dtype,
+                                          const kda_options *options, void *workspace,
+                                          size_t workspace_bytes, cudaStream_t stream,
+                                          cudaEvent_t *events) {
+    if (!(eps > 0.f) || !isfinite(eps)) return KDA_ERR_INVALID_ARGUMENT;
+    if ((long long)B * T > 0 && !z) return KDA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(z) || (reinterpret_cast<uintptr_t>(weight) & 3u) != 0)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if ((long long)B * T <= 0) z = nullptr;  // nothing to gate
+    return chunk_fwd_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state, B, T,
+                          H, dk, dv, num_seqs, dtype, options, workspace, workspace_bytes, stream,
+                          events, GateParams{z, weight, eps});
 }
 
 namespace {

@@ -135,6 +135,14 @@ cudaError_t launch_prefill_simt(const void *q, const void *k, const void *v, con
                                 const int *seq_first_slot, float *region, const int *status,
                                 const Prologue &pro, cudaStream_t stream, cudaEvent_t *events);
 
+// Output gate and RMS normalisation applied to the prefill's outputs (z NULL:
+// none): out = w o / sqrt(mean(o^2) + eps) sigmoid(z) per (token, head).
+struct GateParams {
+    const void *z;   // gate logits [tokens][H][dv], storage dtype
+    const float *w;  // [dv] or NULL
+    float eps;
+};
+
 // Tensor-core prefill (bf16 storage, d = 128).
 size_t tc_region_bytes();
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
@@ -143,8 +151,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               int T_fixed, long long tokens, int H, int num_seqs, long long slots,
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, const Prologue &pro,
-                              int segments, int seg_max, float *seg_ws, cudaStream_t stream,
-                              cudaEvent_t *events);
+                              int segments, int seg_max, float *seg_ws, const GateParams &gate,
+                              cudaStream_t stream, cudaEvent_t *events);
 
 // Records events[i] (when non-NULL) on the stream: the prefill marks the
 // start (0), the end of the chunk table (1), of the intra-chunk phase (2) and

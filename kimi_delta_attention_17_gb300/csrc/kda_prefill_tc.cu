@@ -855,7 +855,23 @@ constexpr int kP2Bar = kP2B2 + 8192;
 constexpr int kP2NBar = 2 * kP2Bufs + 3;
 constexpr int kP2Tmem = kP2Bar + 8 * kP2NBar;
 constexpr int kP2Err = kP2Tmem + 4;
-constexpr int kP2Smem = kP2Err + 4;
+// Fused output gate (4-CTA cluster): three mbarriers (the partial sums of a
+// chunk's rows from the four CTAs have arrived, one per chunk parity; the
+// chunk's gate logits have landed), this CTA's per-row partials of its four
+// column groups, the four CTAs' per-row partials (two chunk parities), and the
+// gate logits of this CTA's 32 columns for one chunk (bf16 [64 tokens][32],
+// a tensor-map tile: global loads would hold the output warps at their next
+// named barrier until they return).
+constexpr int kP2RedBar = kP2Err + 4;
+constexpr int kP2Loc = kP2RedBar + 32;   // fp32 [4 column groups][64 rows]
+constexpr int kP2Red = kP2Loc + 1024;    // fp32 [2 parities][4 CTAs][64 rows]
+constexpr int kP2Z = (kP2Red + 2048 + 127) / 128 * 128;
+constexpr uint32_t kZBytes = C * kTN * 2;
+constexpr int kP2Smem = kP2Z + (int)kZBytes;
+static_assert(kP2RedBar % 8 == 0, "mbarriers must be 8-byte aligned");
+constexpr int kBarO = 3;                 // named barrier of the output warps
+constexpr uint32_t kRedBytes = (D / kTN) * 64 * 4;  // row partials a CTA receives per chunk
+constexpr int kGateCluster = D / kTN;    // CTAs of a head's state = the cluster
 static_assert(kBufBytes % 1024 == 0 && kP2B1 % 1024 == 0, "operand tiles must stay 1 KiB aligned");
 static_assert(kP2Smem <= 232448, "phase-2 shared memory exceeds 227 KiB");
 constexpr uint32_t kB1Lbo = 128, kB1Sbo = 2048;
@@ -876,6 +892,25 @@ constexpr int kD2Col = 128;
 //    outputs, into xfer;
 //  * final (segments 1 .. P-1), after seg_combine: each segment runs from the
 //    state entering it, with outputs; the last one writes the final state.
+// sigmoid(z) = (1 + tanh(z / 2)) / 2 with the hardware tanh approximation
+// (one transcendental instead of an exponential and a reciprocal; its error,
+// below 1e-3 relative, is far inside the bf16 output's rounding).
+__device__ __forceinline__ float sigmoid_fast(float z) {
+    float th;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(0.5f * z));
+    return fmaf(0.5f, th, 0.5f);
+}
+
+// The output gate and RMS normalisation fused into the state pass's output
+// write (z == NULL: plain outputs): out = w o / sqrt(mean(o^2) + eps) sigmoid(z)
+// per (token, head) over the d_v channels ("Understanding Kimi Delta
+// Attention", closing remarks: output gating and RMS normalisation).
+struct OutGate {
+    const __nv_bfloat16 *z;  // gate logits [tokens][H][D], or NULL (read through tm_z)
+    const float *w;          // [D] per-channel weight, or NULL (ones)
+    float eps;
+};
+
 struct SegPass {
     int L;         // chunks per segment
     int P;         // segments per sequence (1: the serial pass)
@@ -889,11 +924,16 @@ __global__ void __launch_bounds__(kP2Threads, 1)
 tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
               const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens,
               int T_fixed, const float *init_state, __nv_bfloat16 *__restrict__ out,
-              float *final_state, int H, int *__restrict__ status, const SegPass sp) {
+              float *final_state, int H, int *__restrict__ status, const SegPass sp,
+              const OutGate og, const __grid_constant__ CUtensorMap tm_z) {
     extern __shared__ __align__(1024) unsigned char sm[];
+    const bool gated = og.z != nullptr;
     // A call whose chunk table was refused (or that already failed) does
-    // nothing; the decision is taken once for the whole CTA.
-    if (__syncthreads_or(threadIdx.x == 0 && *status != 0)) return;
+    // nothing; the decision is taken once for the whole CTA. With the fused
+    // output gate the CTA is one of a cluster and stays for the cluster
+    // barriers, walking no chunk.
+    const bool refused = __syncthreads_or(threadIdx.x == 0 && *status != 0) != 0;
+    if (refused && !gated) return;
     // 1-D grid, sequences slowest in seq_order (longest first), then heads,
     // then segments, then the column tiles of one head and segment (adjacent:
     // they read the same tiles). A transfer launch has 2 D / kTN tiles: the
@@ -922,7 +962,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     }
     const int all_chunks = (len + C - 1) / C;
     const int c0 = (int)min((long long)all_chunks, (long long)p * sp.L);
-    const int nchunks = min(all_chunks - c0, sp.L);  // this segment's chunks
+    const int nchunks = refused ? 0 : min(all_chunks - c0, sp.L);  // this segment's chunks
     const int slot0 = seq_first_slot[n] + c0;
     // Where the state comes from and where it goes, row r, columns j0 + js:
     const size_t nh = (size_t)n * H + h;
@@ -951,6 +991,10 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     uint64_t *bar_m1 = bar_fr + kP2Bufs;                            // first product done
     uint64_t *bar_m2 = bar_m1 + 1;                                  // second product done
     uint64_t *bar_m3 = bar_m2 + 1;                                  // H Z product done
+    uint64_t *red_full = reinterpret_cast<uint64_t *>(sm + kP2RedBar);  // [2] row partials arrived
+    uint64_t *z_full = red_full + 2;                                    // gate logits landed
+    float *loc = reinterpret_cast<float *>(sm + kP2Loc);
+    float *red = reinterpret_cast<float *>(sm + kP2Red);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kP2Tmem);
     volatile int *err = reinterpret_cast<volatile int *>(sm + kP2Err);
     // Bounded waits. A phase that has completed returns at once; otherwise the
@@ -1001,6 +1045,13 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     if (warp == 0) tmem_alloc<256>(tslot);
     if (tid == 0) {
         for (int i = 0; i < kP2NBar; ++i) mbar_init(bar_ld + i, 1);
+        // every output thread of the four CTAs arrives once per chunk
+        if (gated) {
+            // Each chunk's phase: one local arrival (with the expected bytes,
+            // 4 CTAs x 64 rows x 4 B) and the peers' asynchronous stores.
+            for (int i = 0; i < 2; ++i) mbar_init(red_full + i, 1);
+            mbar_init(z_full, 1);
+        }
         *err = 0;
         mbar_fence_init();
     }
@@ -1008,6 +1059,11 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     fence_before();
     __syncthreads();
     fence_after();
+    // The first two chunks' phases expect their bytes, and the peers' barriers
+    // are initialised, before anyone sends.
+    if (gated && tid == 0)
+        for (int i = 0; i < 2 && i < nchunks && !refused; ++i) mbar_expect_tx(red_full + i, kRedBytes);
+    if (gated) cluster_sync();
     const uint32_t tmem = *tslot;
 
     // Chunk ch lives in buffer ch % 3 and is that buffer's (ch / 3)-th use: its
@@ -1104,21 +1160,119 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         __syncwarp();
     } else {
         uint32_t p1 = 0, p2 = 0, p3 = 0;  // phases of the three product barriers
+        uint32_t rph = 0;                 // phases of the two row-partial barriers (bit per parity)
         const bool zrow = r >= 64;
-        // Token outputs of chunk `ch` (rows 0-63 of its D1): s Qbar S + H Z.
-        auto put_outputs = [&](int ch) {  // ch counts this segment's chunks
-            const int clen = min(C, len - (c0 + ch) * C);
+        float wv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wv[j] = gated && og.w ? og.w[j0 + js + j] : 1.f;
+        const uint32_t crank = gated ? cluster_rank() : 0u;
+        // Token outputs of chunk `ch` (rows 0-63 of its D1): s Qbar S + H Z,
+        // or with the fused gate w o / rms(o) sigmoid(z), the mean of squares
+        // over all D columns: this CTA's 32 are summed through shared memory,
+        // then every CTA of the cluster sends its row sums to all four.
+        // The gate logits of chunk ch: one tensor-map tile (32 columns x 64
+        // tokens) into the slot, issued by thread 0 once every output thread
+        // has read the previous chunk's.
+        const __nv_bfloat16 *zslot = reinterpret_cast<const __nv_bfloat16 *>(sm + kP2Z);
+        auto issue_z = [&](int ch) {
+            if (tid != 0 || ch >= nchunks) return;
+            mbar_expect_tx(z_full, kZBytes);
+            tma_load_3d(sm + kP2Z, &tm_z, j0, h, bos + (c0 + ch) * C, z_full);
+        };
+        uint32_t zph = 0;
+        int z_issued = 0;  // tiles issued (tid 0)
+        if (gated && outputs) {
+            issue_z(0);
+            z_issued = nchunks > 0 ? 1 : 0;
+        }
+        // Plain outputs are stored as soon as they are read. With the gate, part
+        // one (before this chunk's Z barrier) reads the outputs and sends their
+        // row sums of squares to the cluster; part two (while the second
+        // product runs) forms w sigmoid(z), takes the four CTAs' sums,
+        // normalises and stores.
+        float o8[8];
+        uint4 zr = make_uint4(0u, 0u, 0u, 0u);
+        auto put_outputs_a = [&](int ch) {  // ch counts this segment's chunks
             const uint32_t d1 = tmem + lane_base + 64 * (ch & 1);
+            if (gated) {
+                if (!mbar_test(z_full, zph) && !*err && !mbar_wait(z_full, zph)) {
+                    *err = 1;
+                    atomicExch(status, (int)KDA_ERR_TIMEOUT);
+                }
+                zph ^= 1;
+                zr = *reinterpret_cast<const uint4 *>(zslot + r * kTN + js);
+            }
             float hi[8], lo[8];
             tmem_ld8(d1 + js, hi);
             tmem_ld8(d1 + kTN + js, lo);
             tmem_wait_ld();
-            if (r < clen) {
-                float o8[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) o8[j] = hi[j] + lo[j];
-                *reinterpret_cast<uint4 *>(out + ((size_t)(bos + (c0 + ch) * C + r) * H + h) * D + j0 + js) = pack8(o8);
+            for (int j = 0; j < 8; ++j) o8[j] = hi[j] + lo[j];
+            if (!gated) {
+                const int clen = min(C, len - (c0 + ch) * C);
+                if (r < clen)
+                    *reinterpret_cast<uint4 *>(out + ((size_t)(bos + (c0 + ch) * C + r) * H + h) * D + j0 + js) =
+                        pack8(o8);
+            } else {
+                const int par = ch & 1;
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ss += o8[j] * o8[j];
+                loc[(js >> 3) * 64 + r] = ss;
+                // Every output thread has read its z (the slot is free) and has
+                // finished the previous chunk, whose row sums it read: that
+                // barrier's next phase (chunk ch + 1) may now expect its bytes,
+                // before this CTA sends anything a peer could answer with them.
+                bar_sync(kBarO, 256);
+                if (ch + 1 < nchunks) {
+                    issue_z(ch + 1);
+                    z_issued = ch + 2;
+                }
+                if (tid == 0 && ch >= 1 && ch + 1 < nchunks) mbar_expect_tx(red_full + (par ^ 1), kRedBytes);
+                if (tid < 16) {
+                    // Rows 4 tid .. 4 tid + 3: this CTA's sums, 16 bytes to each CTA.
+                    float4 pr;
+                    float *pp = reinterpret_cast<float *>(&pr);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = 4 * tid + i;
+                        pp[i] = loc[row] + loc[64 + row] + loc[128 + row] + loc[192 + row];
+                    }
+                    float *slot = red + (par * kGateCluster + (int)crank) * 64 + 4 * tid;
+#pragma unroll
+                    for (uint32_t dst = 0; dst < (uint32_t)kGateCluster; ++dst)
+                        st_async_cluster_v4(cluster_addr(slot, dst), pr, cluster_addr(red_full + par, dst));
+                }
             }
+        };
+        auto put_outputs_b = [&](int ch) {
+            if (!gated) return;  // stored by part one
+            const int clen = min(C, len - (c0 + ch) * C);
+            const size_t orow = ((size_t)(bos + (c0 + ch) * C + r) * H + h) * D + j0 + js;
+            {
+                const int par = ch & 1;
+                float gz[8];
+                const uint32_t zu[4] = {zr.x, zr.y, zr.z, zr.w};
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float zj = __uint_as_float((j & 1) ? (zu[j >> 1] & 0xFFFF0000u) : (zu[j >> 1] << 16));
+                    gz[j] = wv[j] * sigmoid_fast(zj);
+                }
+                if (!mbar_test_cluster(red_full + par, (rph >> par) & 1u) && !*err &&
+                    !mbar_wait_cluster(red_full + par, (rph >> par) & 1u)) {
+                    *err = 1;
+                    atomicExch(status, (int)KDA_ERR_TIMEOUT);
+                }
+                rph ^= 1u << par;
+                const float *rp = red + par * kGateCluster * 64 + r;
+                float tot = 0.f;
+#pragma unroll
+                for (int q = 0; q < kGateCluster; ++q) tot += rp[q * 64];
+                const float rs = rsqrtf(tot * (1.f / D) + og.eps);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) o8[j] *= gz[j] * rs;
+            }
+            if (r < clen) *reinterpret_cast<uint4 *>(out + orow) = pack8(o8);
         };
         for (int ch = 0; ch < nchunks; ++ch) {
             const int b = ch % kP2Bufs;
@@ -1137,11 +1291,11 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             }
             if (!zrow && outputs && ch > 0) {
                 // The previous chunk's outputs, complete once its H Z product is:
-                // written while this chunk's first product runs.
+                // read while this chunk's first product runs.
                 wait(bar_m3, p3);
                 p3 ^= 1;
                 fence_after();
-                put_outputs(ch - 1);
+                put_outputs_a(ch - 1);
             }
             spin(bar_m1, p1);
             p1 ^= 1;
@@ -1165,6 +1319,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             fence_async_smem();
             fence_before();
             bar_arrive(kBarZ, kP2Sync);
+            if (!zrow && outputs && ch > 0) put_outputs_b(ch - 1);  // while the second product runs
             spin(bar_m2, p2);
             p2 ^= 1;
             fence_after();
@@ -1188,9 +1343,13 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         if (nchunks > 0 && !zrow && outputs) {
             wait(bar_m3, p3);
             fence_after();
-            put_outputs(nchunks - 1);
+            put_outputs_a(nchunks - 1);
+            put_outputs_b(nchunks - 1);
         }
-        if (st_dst && !*err) {
+        // Every z tile lands before the CTA exits (bounded; the output threads
+        // waited for each one unless an error made them skip).
+        if (gated && tid == 0 && z_issued > 0) mbar_wait(z_full, (uint32_t)(z_issued - 1) & 1u);
+        if (st_dst && !refused && !*err) {
             float *dst = st_dst + (size_t)r * dst_row + j0 + js;
             *reinterpret_cast<float4 *>(dst) = make_float4(S[0], S[1], S[2], S[3]);
             *reinterpret_cast<float4 *>(dst + 4) = make_float4(S[4], S[5], S[6], S[7]);
@@ -1198,6 +1357,8 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     }
     fence_before();
     __syncthreads();
+    // No CTA leaves while a peer may still write into its shared memory.
+    if (gated) cluster_sync();
     if (warp == 0) tmem_dealloc<256>(tmem);
 }
 
@@ -1300,6 +1461,22 @@ cudaError_t token_rows_map(CUtensorMap *m, const void *base, CUtensorMapDataType
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The gate logits [tokens][H][128] bf16 seen as 3-D (channel, head, token)
+// with boxes of one state-pass CTA's 32 columns x 1 head x 64 tokens.
+cudaError_t gate_rows_map(CUtensorMap *m, const void *base, int H, long long tokens) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kTN, 1u, (cuuint32_t)C};
+    const cuuint32_t unit[3] = {1u, 1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                           strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Segments of the state pass for the `segments` option (0: automatic, 1: the
 // serial chain, k: k segments), at most seg_max (the workspace's bound) and
 // one per chunk. Automatic: as many as keep the transfer launch within one
@@ -1326,8 +1503,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               int T_fixed, long long tokens, int H, int num_seqs, long long slots,
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, const Prologue &pro,
-                              int segments, int seg_max, float *seg_ws, cudaStream_t stream,
-                              cudaEvent_t *events) {
+                              int segments, int seg_max, float *seg_ws, const GateParams &gate,
+                              cudaStream_t stream, cudaEvent_t *events) {
     // Per device, once: the SM count (phase 1 runs one persistent CTA per SM)
     // and the dynamic shared-memory opt-ins. Repeating this is idempotent.
     static int sm_counts[64];
@@ -1405,12 +1582,38 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         constexpr int kTiles = D / kTN;
         const int *order = seq_first_slot + num_seqs + 1;
         const int nch = (T_fixed + C - 1) / C;
-        const int P = state_segments(segments, seg_max, nch, (long long)num_seqs * H, sm_count);
-        if (P <= 1) {
+        // The fused output gate runs on the serial chain (its clusters are the
+        // four column tiles of one sequence and head).
+        const OutGate og{static_cast<const __nv_bfloat16 *>(gate.z), gate.w, gate.eps};
+        CUtensorMap tz;
+        memset(&tz, 0, sizeof(tz));  // read only by the fused gate
+        if (og.z && (err = gate_rows_map(&tz, og.z, H, tokens)) != cudaSuccess) return err;
+        const int P = og.z ? 1 : state_segments(segments, seg_max, nch, (long long)num_seqs * H, sm_count);
+        if (P <= 1 && og.z) {
+            static_assert(kGateCluster == kTiles, "a cluster holds the column tiles of one head");
+            const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)num_seqs * H * kTiles);
+            cfg.blockDim = dim3(kP2Threads);
+            cfg.dynamicSmemBytes = kP2Smem;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = kGateCluster;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if ((err = cudaLaunchKernelEx(&cfg, tc_state_pass, (const unsigned char *)region,
+                                          seq_first_slot, order, cu_seqlens, T_fixed, init_state,
+                                          static_cast<__nv_bfloat16 *>(out), final_state, H, status,
+                                          sp, og, tz)) != cudaSuccess)
+                return err;
+        } else if (P <= 1) {
             const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
             tc_state_pass<<<(unsigned)num_seqs * H * kTiles, kP2Threads, kP2Smem, stream>>>(
                 region, seq_first_slot, order, cu_seqlens, T_fixed, init_state,
-                static_cast<__nv_bfloat16 *>(out), final_state, H, status, sp);
+                static_cast<__nv_bfloat16 *>(out), final_state, H, status, sp, og, tz);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         } else {
             const int L = (nch + P - 1) / P;
@@ -1421,7 +1624,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * 2 * kTiles, kP2Threads, kP2Smem,
                             stream>>>(region, seq_first_slot, order, cu_seqlens, T_fixed,
                                       init_state, static_cast<__nv_bfloat16 *>(out), final_state,
-                                      H, status, sa);
+                                      H, status, sa, og, tz);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
             if (Pn > 2) {
                 seg_combine<<<(unsigned)num_seqs * H * (D / kCombCols), kCombThreads, kCombSmem,
@@ -1432,7 +1635,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * kTiles, kP2Threads, kP2Smem,
                             stream>>>(region, seq_first_slot, order, cu_seqlens, T_fixed,
                                       init_state, static_cast<__nv_bfloat16 *>(out), final_state,
-                                      H, status, sc);
+                                      H, status, sc, og, tz);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     }

@@ -212,6 +212,81 @@ __device__ __forceinline__ bool mbar_spin(uint64_t *mbar, uint32_t parity) {
     return mbar_wait(mbar, parity);
 }
 
+// ---- thread-block clusters (distributed shared memory; no multicast)
+
+// This CTA's rank within its cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of the variable at `p` (this CTA's shared
+// memory) in the CTA of rank `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Asynchronous 4-byte store into the shared memory of a CTA of the cluster
+// (cluster addresses), completing 4 transaction bytes on that CTA's mbarrier;
+// no fence: the mbarrier's phase completion publishes the value.
+__device__ __forceinline__ void st_async_cluster_f32(uint32_t addr, float v, uint32_t mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
+                     addr),
+                 "f"(v), "r"(mbar)
+                 : "memory");
+}
+// The same for 16 bytes (four consecutive floats; addr 16-byte aligned).
+__device__ __forceinline__ void st_async_cluster_v4(uint32_t addr, float4 v, uint32_t mbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            addr),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(mbar)
+        : "memory");
+}
+// Arrives once on the mbarrier at cluster address `addr`, releasing this
+// thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+                 : "memory");
+}
+// Bounded wait on a local mbarrier whose arrivals come from other CTAs of the
+// cluster (acquire at cluster scope). Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *mbar, uint32_t parity,
+                                                  uint32_t limit = 1u << 22) {
+    const uint32_t a = smem_u32(mbar);
+    for (uint32_t it = 0; it < limit; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{.reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+            "selp.u32 %0, 1, 0, p;}"
+            : "=r"(ok)
+            : "r"(a), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+// One non-blocking test of such a barrier (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t *mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{.reg .pred p; mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+        "selp.u32 %0, 1, 0, p;}"
+        : "=r"(done)
+        : "r"(smem_u32(mbar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Barrier over every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` transactions on mbar.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

@@ -73,7 +73,7 @@ def _check_g(g, decay, nd):
 def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=None,
               final_state=None, workspace=None, output_final_state=True, stream=None,
               phase_events=None, decay="channel", gate="log", gate_lower=-5.0, l2norm_qk=False,
-              segments=0):
+              segments=0, out_gate=None, norm_weight=None, norm_eps=1e-6):
     """Chunkwise prefill. q, k [B, T, H, dk]; v [B, T, H, dv] (bf16 or fp32);
     g [B, T, H, dk] fp32; beta [B, T, H] fp32; init_state [N, H, dk, dv] fp32
     or None; cu_seqlens int32 [N+1] (device) or None (then N = B).
@@ -87,7 +87,11 @@ def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=
     gate_lower * sigmoid(g)); ``l2norm_qk`` normalises q and k in the kernel;
     ``segments`` how the state crosses the chunks on the tensor-core path (0
     automatic, 1 one serial chain, k up to k segments composed as affine maps;
-    kda_options.segments)."""
+    kda_options.segments).
+    ``out_gate`` (gate logits z, q's dtype and v's shape) makes ``out`` the
+    gated, RMS-normalised output w * o / sqrt(mean(o^2) + norm_eps) *
+    sigmoid(z), with ``norm_weight`` [dv] fp32 or None (kda_chunk_fwd_gated;
+    fused into the state pass on the tensor-core path)."""
     _need(q, "q", ndim=4)
     dtype = q.dtype
     if dtype not in _DTYPES:
@@ -128,7 +132,18 @@ def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=
             raise ValueError("phase_events needs 4 events")
         handles = (ctypes.c_void_p * 4)(*[None if e is None else _event_handle(e)
                                           for e in phase_events])
-    if opts is not None:
+    if out_gate is not None:
+        _need(out_gate, "out_gate", dtype, 4)
+        if out_gate.shape != v.shape:
+            raise ValueError("out_gate must have v's shape")
+        if norm_weight is not None:
+            _need(norm_weight, "norm_weight", torch.float32, 1)
+        if opts is None:
+            opts = _lib.Options(_lib.DECAY["channel"], _lib.GATE["log"], 0.0, 0, 0)
+        _lib.check("kda_chunk_fwd_gated", _lib.lib().kda_chunk_fwd_gated(
+            *head[:8], _ptr(out_gate), _ptr(norm_weight), float(norm_eps), *head[8:],
+            ctypes.byref(opts), *tail, handles))
+    elif opts is not None:
         _lib.check("kda_chunk_fwd_opt",
                    _lib.lib().kda_chunk_fwd_opt(*head, ctypes.byref(opts), *tail, handles))
     elif handles is None:

@@ -99,3 +99,28 @@ def test_four_head_shard_parallel_prefix():
     es = assert_parity(fin_h, ref_fin, spec.dtype, "final state")
     print("\n%s, parallel prefix: O max|err| %.3g rel %.3g; final state max|err| %.3g rel %.3g"
           % (spec.name, eo[0], eo[1], es[0], es[1]))
+
+
+def test_varlen_workload_every_head():
+    """The 8-sequence packed prefill (mixture gates: half the key channels with
+    half-lives of hundreds of tokens; nonzero initial states), where the bf16
+    error budget is tightest: all 32 heads against the oracle, and each head on
+    its own within the bounds. Prints the worst head's errors."""
+    spec = VARLEN_8
+    inp = make_prefill(spec)
+    out, fin = gpu_prefill(inp)
+    out64, fin64 = f64(out), f64(fin)
+    del out, fin
+    ref_out, ref_fin = oracle_prefill(inp)
+    assert_parity(out64, ref_out, spec.dtype, "O")
+    assert_parity(fin64, ref_fin, spec.dtype, "final state")
+    worst = {}
+    for h in range(spec.H):
+        for what, got, ref in (("O", out64[:, :, h], ref_out[:, :, h]),
+                               ("final state", fin64[:, h], ref_fin[:, h])):
+            m, r = assert_parity(got, ref, spec.dtype, "%s, head %d" % (what, h))
+            if r > worst.get(what, (0, 0.0, 0.0))[2]:
+                worst[what] = (h, m, r)
+    for what, (h, m, r) in worst.items():
+        print("\n%s, every head: worst %s is head %d: max|err| %.3g rel %.3g"
+              % (spec.name, what, h, m, r))
