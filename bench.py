@@ -455,6 +455,59 @@ def bench_ours(args):
         decode_ms = d_start.elapsed_time(d_end)
     clocks = clk.summary()
 
+    # ---------------- end to end through host buffers (pinned), prefill: the C entry
+    # kda_chunk_fwd_host (through chunk_fwd_host), which copies each 16384-token
+    # window in while the previous one runs and its outputs back while the next
+    # runs. Timed before the variants allocate and free their own buffers.
+    h_in = {k: (None if inp[k] is None else inp[k].pin_memory()) for k in keys}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for n, t in h_in.items()
+              if t is not None and n != "cu_seqlens")
+    d2h = h_out.numel() * h_out.element_size() + h_fin.numel() * h_fin.element_size()
+    e2e_steps = max(1, min(K, 3))
+    host_scratch = {}
+
+    def e2e_prefill():
+        chunk_fwd_host(h_in["q"], h_in["k"], h_in["v"], h_in["g"], h_in["beta"],
+                       inp["scale"], h_in["init_state"], h_in["cu_seqlens"], out=h_out,
+                       final_state=h_fin, window_tokens=16384, scratch=host_scratch)
+    e2e_prefill()  # first call sizes the segment buffers
+    barrier()
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        e2e_prefill()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
+    e2e_tok_s = units_for_world(tokens, world) * e2e_steps / (e2e_ms / 1e3)
+
+    # ---------------- end to end, decode: the public host-buffer call (decode_host),
+    # step t + 1's inputs copied in while step t runs
+    hd = {k: dinp[k].pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    h_dout = torch.empty((dspec.steps,) + tuple(dout.shape), dtype=dout.dtype).pin_memory()
+    d_h2d = sum(hd[k][0].numel() * hd[k][0].element_size() for k in hd)
+    d_d2h = dout.numel() * dout.element_size()
+    dec_scratch = {}
+    decode_host(hd["q"], hd["k"], hd["v"], hd["g"], hd["beta"], dinp["scale"], state,
+                out=h_dout, scratch=dec_scratch)
+    barrier()
+    torch.cuda.synchronize()
+    de_start = torch.cuda.Event(enable_timing=True)
+    de_end = torch.cuda.Event(enable_timing=True)
+    de_start.record(stream)
+    decode_host(hd["q"], hd["k"], hd["v"], hd["g"], hd["beta"], dinp["scale"], state,
+                out=h_dout, scratch=dec_scratch)
+    de_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    de_ms = max_over_ranks(de_start.elapsed_time(de_end), dev)
+    del h_in, h_out, h_fin, hd, h_dout, host_scratch, dec_scratch
+
     # ---------------- variants: the options of kda_chunk_fwd_opt / kda_decode_step_opt on the
     # same resident inputs (one channel of g as the per-head decay; g as gate logits)
     g_head = d_in["g"][..., 0].contiguous()
@@ -668,57 +721,6 @@ def bench_ours(args):
     tok_per_s = units_for_world(tokens, world) * K / (prefill_ms / 1e3)
     pbytes = prefill_bytes(spec, tokens, N, inp["init_state"] is not None)
     dominant = max(phase_ms, key=phase_ms.get)
-
-    # ---------------- end to end through host buffers (pinned), prefill: the public
-    # host-buffer call (chunk_fwd_host), which copies each 16384-token segment in
-    # while the previous one runs and copies outputs back while the next runs
-    h_in = {k: (None if inp[k] is None else inp[k].pin_memory()) for k in keys}
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for n, t in h_in.items()
-              if t is not None and n != "cu_seqlens")
-    d2h = h_out.numel() * h_out.element_size() + h_fin.numel() * h_fin.element_size()
-    e2e_steps = max(1, min(K, 3))
-    host_scratch = {}
-
-    def e2e_prefill():
-        chunk_fwd_host(h_in["q"], h_in["k"], h_in["v"], h_in["g"], h_in["beta"],
-                       inp["scale"], h_in["init_state"], h_in["cu_seqlens"], out=h_out,
-                       final_state=h_fin, window_tokens=16384, scratch=host_scratch)
-    e2e_prefill()  # first call sizes the segment buffers
-    barrier()
-    torch.cuda.synchronize()
-    e_start = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
-    e_start.record(stream)
-    for _ in range(e2e_steps):
-        e2e_prefill()
-    e_end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end), dev)
-    e2e_tok_s = units_for_world(tokens, world) * e2e_steps / (e2e_ms / 1e3)
-
-    # ---------------- end to end, decode: the public host-buffer call (decode_host),
-    # step t + 1's inputs copied in while step t runs
-    hd = {k: dinp[k].pin_memory() for k in ("q", "k", "v", "g", "beta")}
-    h_dout = torch.empty((dspec.steps,) + tuple(dout.shape), dtype=dout.dtype).pin_memory()
-    d_h2d = sum(hd[k][0].numel() * hd[k][0].element_size() for k in hd)
-    d_d2h = dout.numel() * dout.element_size()
-    dec_scratch = {}
-    decode_host(hd["q"], hd["k"], hd["v"], hd["g"], hd["beta"], dinp["scale"], state,
-                out=h_dout, scratch=dec_scratch)
-    barrier()
-    torch.cuda.synchronize()
-    de_start = torch.cuda.Event(enable_timing=True)
-    de_end = torch.cuda.Event(enable_timing=True)
-    de_start.record(stream)
-    decode_host(hd["q"], hd["k"], hd["v"], hd["g"], hd["beta"], dinp["scale"], state,
-                out=h_dout, scratch=dec_scratch)
-    de_end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    de_ms = max_over_ranks(de_start.elapsed_time(de_end), dev)
 
     steps_total = dspec.steps * K
     dec_steps_s = world * steps_total / (decode_ms / 1e3)
