@@ -8,10 +8,11 @@
 //     G      in-chunk cumulative log-decay (registers, one thread per channel)
 //     A, H   decay-gated K K^T and Q K^T, from ONE tcgen05.mma (below)
 //     T      (I - A)^{-1}: blocked forward substitution in fp32 shared memory
-//     W = (T B) L,  U = (T B) V                 one MMA pair, B = Diag(beta)
+//     W = (T B) L                               one MMA, B = Diag(beta)
 //     s Qbar, Kbar^T, exp(G_n)                  elementwise
 //   phase 2 (one CTA per sequence, head and 32-column slab of the state,
 //   chunks in order, state in registers, warp-specialised):
+//     U = (T B) V                               one MMA, a chunk ahead
 //     [s Qbar S; W S] = [s Qbar; W] S           one MMA, M = 128
 //     Z = U - W S                               elementwise
 //     S <- Diag(exp(G_n)) S + Kbar^T Z          one MMA
@@ -54,45 +55,38 @@ constexpr int D = 128;   // d_k = d_v on this path
 constexpr int C = kChunk;
 constexpr int kTN = 32;  // state columns per phase-2 CTA
 
-// Workspace region of one (chunk slot, head), byte offsets. Everything every
-// state-pass CTA of the head needs comes first, contiguous, so that it moves
-// in one bulk copy; each CTA's U slab follows. (An SM completes about one bulk
-// copy per 900 cycles whatever its size, up to 64 KiB: copies must be few and large.)
+// Workspace region of one (chunk slot, head), byte offsets. Everything a
+// state-pass CTA needs from it is shared by the head's four CTAs and moves in
+// one bulk copy (an SM completes about one bulk copy per 900 cycles whatever
+// its size, up to 64 KiB: copies must be few and large); each CTA forms its
+// own 32-column slab of U = (T B) V from (T B) here and the value rows it
+// loads itself.
 struct TcRegion {
     static constexpr size_t A1 = 0;        // [s Qbar; W] bf16, MN-major, 128 tokens x 128 ch
     static constexpr size_t A2 = 32768;    // Kbar^T bf16, K-major, 128 ch x 64 tokens
-    static constexpr size_t Hm = 49152;    // H bf16, K-major [token i][token j] (LBO 1024, SBO 128)
-    static constexpr size_t Gam = 57344;   // fp32 [128] exp(G_n)
-    static constexpr size_t shared = 57856;  // bytes of the part above
-    static constexpr size_t U = 57856;     // fp32 [4 slabs][64 tokens][32 columns], rows swizzled
-    static constexpr size_t bytes = 90624;
+    static constexpr size_t HT = 49152;    // [H; T B] bf16, K-major [row][token j] (LBO 2048, SBO 128)
+    static constexpr size_t Gam = 65536;   // fp32 [128] exp(G_n)
+    static constexpr size_t shared = 66048;  // bytes of the part above
+    static constexpr size_t bytes = 66048;
 };
-static_assert(TcRegion::U + 4 * 64 * 32 * 4 == TcRegion::bytes, "region layout");
-// Element (token i, column j of a 32-column slab) of a U slab: the float4
-// groups of a row are XOR-swizzled by (i & 7), so the phase-2 thread that owns
-// row i reads it without bank conflicts, while phase 1 (one thread per column)
-// still writes each row with one coalesced 128-byte store per warp.
-__host__ __device__ constexpr int slab_idx(int i, int j) {
-    return i * 32 + ((((j >> 2) ^ (i & 7))) << 2) + (j & 3);
-}
+static_assert(TcRegion::bytes % 256 == 0, "regions stay 256-byte aligned");
 // Descriptor strides of the workspace tiles (and of their shared-memory copies).
 constexpr uint32_t kA1Lbo = 128, kA1Sbo = 2048;  // MN-major: channel cores adjacent
 constexpr uint32_t kA2Lbo = 2048, kA2Sbo = 128;  // K-major: channel groups adjacent
 
 // ---------------------------------------------------------------- phase 1
 // Persistent: one CTA of 16 warps per SM walks the (chunk slot, head) items,
-// heads fastest. The raw rows of the next item (q, k, v bf16 and g fp32: four
+// heads fastest. The raw rows of the next item (q, k bf16 and g fp32: three
 // tensor-map tiles) stream into the staging area while the current item runs
 // its MMAs, solve and stores. Thread (c, blk) owns key/value channel c and the
 // 16-token block blk in the elementwise pass; for TMEM read-back thread t owns
 // lane t mod 128, the four warps of a lane quadrant splitting the columns.
 constexpr int kP1Threads = 512;
 struct P1 {  // shared-memory offsets, bytes
-    static constexpr int q = 0, k = 16384, v = 32768, g = 49152;  // staging rows of one chunk
+    static constexpr int q = 0, k = 16384, g = 49152;  // staging rows of one chunk
     static constexpr int am = 81920;    // [Ktilde; s Qtilde] bf16, MN-major 128 x 128
     static constexpr int bm = 114688;   // column versions bf16, MN-major 160 x 128
     static constexpr int lt = 155648;   // L^T bf16, K-major [channel][token]
-    static constexpr int vt = 172032;   // V^T bf16, K-major [channel][token]
     static constexpr int beta = 188416; // 64 floats
     static constexpr int bar = 188672;  // mbarriers: staging loaded, MMA done
     static constexpr int tmem = 188688;
@@ -198,7 +192,7 @@ constexpr int kVarChannel = 0, kVarRuntime = 1, kVarScalar = 2, kVarNone = 3, kV
 template <int kVar>
 __global__ void __launch_bounds__(kP1Threads, 1)
 tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+               const __grid_constant__ CUtensorMap tm_g,
                const float *__restrict__ g_head, Prologue pro,
                const float *__restrict__ beta, float scale, const ChunkEntry *__restrict__ table,
                const int *__restrict__ used_slots, long long nslots, int H,
@@ -242,7 +236,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint64_t d_am = desc(smem_u32(sm + P1::am), kA1Lbo, kA1Sbo);
     const uint64_t d_bm = desc(smem_u32(sm + P1::bm), kA1Lbo, kA1Sbo);
     const uint64_t d_lt = desc(smem_u32(sm + P1::lt), kA2Lbo, kA2Sbo);
-    const uint64_t d_vt = desc(smem_u32(sm + P1::vt), kA2Lbo, kA2Sbo);
     const uint64_t d_tb = desc(smem_u32(sm + P1::TBs), 1024, 128);
 
     // One thread fetches an item: four 3-D TMA tiles (128 channels x 1 head x
@@ -255,10 +248,9 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const bool g_tile = pro.decay == KDA_DECAY_CHANNEL;  // g arrives as a tile only per channel
     auto issue = [&](int hh, const ChunkEntry e) {
         if (tid != 0) return;
-        mbar_expect_tx(bar_ld, 64u * (3u * 256u + (g_tile ? 512u : 0u)));
+        mbar_expect_tx(bar_ld, 64u * (2u * 256u + (g_tile ? 512u : 0u)));
         tma_load_3d(sm + P1::q, &tm_q, 0, hh, e.bos, bar_ld);
         tma_load_3d(sm + P1::k, &tm_k, 0, hh, e.bos, bar_ld);
-        tma_load_3d(sm + P1::v, &tm_v, 0, hh, e.bos, bar_ld);
         if (g_tile) tma_load_3d(sm + P1::g, &tm_g, 0, hh, e.bos, bar_ld);
     };
 
@@ -306,7 +298,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const float *gs = reinterpret_cast<const float *>(sm + P1::g);
             const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::q);
             const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::k);
-            const __nv_bfloat16 *vs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::v);
             // Cumulative log-decay of channel c: each thread sums its own block,
             // keeping the 16 in-block prefixes; block totals and in-block
             // references (token 7 of each block) are exchanged so that every
@@ -433,7 +424,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             for (int ig = 0; ig < 2; ++ig) {
                 const int i0 = 16 * blk + 8 * ig;  // first token of the group
                 float kv[8], qv[8], E[8], kF[8], t8[8], Gi[8];
-                uint32_t vraw[4];
 #pragma unroll
                 for (int r = 0; r < 8; ++r) Gi[r] = ig ? G[8 + r] : G[r];
 #pragma unroll
@@ -449,14 +439,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     qv[r] = in ? fq * __bfloat162float(qs[i * D + c]) : 0.f;
                     E[r] = __expf(Gi[r] - Rlr);
                     kF[r] = kv[r] * __expf(Rlc - Gi[r]);
-                }
-                // V^T needs no arithmetic: move the bf16 bits (zero past the end).
-                const unsigned short *vb = reinterpret_cast<const unsigned short *>(vs);
-#pragma unroll
-                for (int r = 0; r < 8; r += 2) {
-                    const uint32_t lo = i0 + r < len ? vb[(i0 + r) * D + c] : 0u;
-                    const uint32_t hi = i0 + r + 1 < len ? vb[(i0 + r + 1) * D + c] : 0u;
-                    vraw[r >> 1] = lo | (hi << 16);
                 }
 #pragma unroll
                 for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r];
@@ -478,8 +460,6 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r] * Ps;
                 st16(sm + P1::lt + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
-                *reinterpret_cast<uint4 *>(sm + P1::vt + kmaj(c, i0, kA2Lbo, kA2Sbo)) =
-                    make_uint4(vraw[0], vraw[1], vraw[2], vraw[3]);
                 // s Qbar, rows 0-63 of the state-pass operand [s Qbar; W].
 #pragma unroll
                 for (int r = 0; r < 8; ++r) t8[r] = qv[r] * E[r] * Ps;
@@ -518,7 +498,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!ok) break;
         {
             float *As = reinterpret_cast<float *>(sm + P1::As);
-            unsigned char *Hs = reg + TcRegion::Hm;  // H goes straight to the workspace
+            unsigned char *Hs = reg + TcRegion::HT;  // H goes straight to the workspace (rows 0-63)
             const int lr = tid & 127, i = lr & 63, Iblk = i >> 4;
             const bool isH = lr >= 64;
             const int grp = warp >> 2;           // which of the quadrant's four warps
@@ -563,7 +543,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                         float t8[8];
 #pragma unroll
                         for (int r = 0; r < 8; ++r) t8[r] = (16 * J + 8 * hf + r <= i) ? x[8 * hf + r] : 0.f;
-                        st16(Hs + kmaj(i, 16 * J + 8 * hf, 1024, 128), t8);
+                        st16(Hs + kmaj(i, 16 * J + 8 * hf, kA2Lbo, kA2Sbo), t8);
                     }
                 }
             }
@@ -578,8 +558,8 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 make_float4(0.f, 0.f, 0.f, 0.f);
                     } else {
                         const uint4 z = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J, 1024, 128)) = z;
-                        *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J + 8, 1024, 128)) = z;
+                        *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J, kA2Lbo, kA2Sbo)) = z;
+                        *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J + 8, kA2Lbo, kA2Sbo)) = z;
                     }
                 }
             }
@@ -748,6 +728,9 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
                 st16(sm + P1::TBs + kmaj(i, jb, 1024, 128), t8);
+                // and rows 64-127 of the workspace's [H; T B], from which each
+                // state-pass CTA forms its slab of U = (T B) V
+                st16(reg + TcRegion::HT + kmaj(64 + i, jb, kA2Lbo, kA2Sbo), t8);
             }
         }
         fence_async_smem();
@@ -755,15 +738,12 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         __syncthreads();
         fence_after();
 
-        // ================= W = (T B) L, U = (T B) V
+        // ================= W = (T B) L
         if (tid == 0) {
             const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
-            for (int s = 0; s < C / 16; ++s) {
-                const uint64_t b = d_tb + s * (2 * 1024 >> 4);
-                mma_bf16(tmem + 0, d_lt + s * (2 * kA2Lbo >> 4), b, id, s > 0);
-                mma_bf16(tmem + 64, d_vt + s * (2 * kA2Lbo >> 4), b, id, s > 0);
-            }
+            for (int s = 0; s < C / 16; ++s)
+                mma_bf16(tmem + 0, d_lt + s * (2 * kA2Lbo >> 4), d_tb + s * (2 * 1024 >> 4), id, s > 0);
             commit(bar_mma);
         }
         ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
@@ -771,24 +751,13 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         fence_after();
         if (!ok) break;
         {
-            // W -> rows 64-127 of [s Qbar; W] (column groups 0, 1); U -> its slab
-            // (groups 2, 3); each thread reads two 16-token parts of its lane.
-            const int side = blk >> 1;
-            float *slab = reinterpret_cast<float *>(reg + TcRegion::U) + (size_t)(c >> 5) * (C * 32);
-#pragma unroll
-            for (int pp = 0; pp < 2; ++pp) {
-                const int part = 2 * (blk & 1) + pp;
-                float x[16];
-                tmem_ld16(tmem + lane_base + 64 * side + 16 * part, x);
-                tmem_wait_ld();
-                if (side == 0) {
-                    st16(reg + TcRegion::A1 + mnmaj(64 + 16 * part, c, kA1Lbo, kA1Sbo), x);
-                    st16(reg + TcRegion::A1 + mnmaj(64 + 16 * part + 8, c, kA1Lbo, kA1Sbo), x + 8);
-                } else {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) slab[slab_idx(16 * part + r, c & 31)] = x[r];
-                }
-            }
+            // W^T (lane = channel c, column = token) -> rows 64-127 of [s Qbar; W];
+            // thread (c, blk) writes tokens 16 blk .. 16 blk + 15 of its channel.
+            float x[16];
+            tmem_ld16(tmem + lane_base + 16 * blk, x);
+            tmem_wait_ld();
+            st16(reg + TcRegion::A1 + mnmaj(64 + 16 * blk, c, kA1Lbo, kA1Sbo), x);
+            st16(reg + TcRegion::A1 + mnmaj(64 + 16 * blk + 8, c, kA1Lbo, kA1Sbo), x + 8);
         }
         // The next item's per-head log-decays (this item read its own before
         // its exchange barrier; the next item's load barrier orders these).
@@ -827,32 +796,53 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 //   round trip 2:  D2 = Kbar^T Z,  D1[0:64] += H Z
 //                  S <- Diag(exp G_n) S + D2,  O = D1[0:64] = s Qbar S + H Z
 // ("Understanding Kimi Delta Attention", "The token outputs" and "One state
-// crosses the chunk boundary"). S and Z enter the MMAs as bf16 hi + lo pairs.
-// Warp roles: warps 0-15 compute; warp 16 issues the MMAs; warp 17's lane 0
-// issues every bulk copy of the chunk tiles (a copy's issue can hold its
-// thread for a hundred cycles or more).
+// crosses the chunk boundary"), with U = (T B) V formed a chunk ahead. S and
+// Z enter the MMAs as bf16 hi + lo pairs.
+// Warp roles: warps 0-15 compute; warp 16 issues the two products on the
+// chain of dependent steps and keeps the named barriers with the compute
+// warps; warp 18 issues the products off that chain (U, H Z), paced by
+// mbarriers alone: an MMA's issue holds its thread while the tensor pipe is
+// busy (about 100 cycles per M = 128, K = 16 step here), which must not delay
+// a barrier. Warp 17 issues the copies of the chunk tiles (a bulk copy's
+// issue can hold its thread for a hundred cycles or more).
 constexpr int kP2Compute = 512;
 constexpr int kP2MmaWarp = kP2Compute / 32;
 constexpr int kP2ProdWarp = kP2MmaWarp + 1;
-constexpr int kP2Threads = kP2Compute + 64;
+constexpr int kP2SideWarp = kP2MmaWarp + 2;
+constexpr int kP2Threads = kP2Compute + 96;
 constexpr int kP2Sync = kP2Compute + 32;  // compute warps + MMA warp
 constexpr int kBarZ = 1, kBarS = 2;       // named barriers: Z written, state written
-constexpr int kP2Bufs = 3;        // chunk buffers: loads run ahead of use
-// One chunk's buffer: the region's shared part (A1, A2, H, gamma) at the same
-// offsets as in the workspace, then this CTA's U slab. Two bulk copies fill it;
-// it is free again once the chunk that last used it has finished its H Z product.
-constexpr int kBufA2 = (int)TcRegion::A2, kBufH = (int)TcRegion::Hm, kBufGam = (int)TcRegion::Gam;
-constexpr int kBufU = (int)TcRegion::shared;
-constexpr int kBufBytes = 66560;  // 65 KiB
-constexpr uint32_t kSlabBytes = kTN * C * 4;
-constexpr uint32_t kLoadBytes = (uint32_t)TcRegion::shared + kSlabBytes;
-static_assert(kBufU + (int)kSlabBytes <= kBufBytes, "chunk buffer too small");
-constexpr int kP2B1 = kP2Bufs * kBufBytes;      // S (hi | lo) bf16, MN-major [K = ch][N = 64]
-constexpr int kP2B2 = kP2B1 + 16384;            // [Z_hi | Z_lo] bf16, MN-major [K = token][N = 64]
-// mbarriers: loaded[3], free[3], first product, second product, H Z product;
-// then the TMEM base and the error flag.
+// A chunk's tiles sit in two rings, by when they are consumed. Ring X holds
+// [s Qbar; W] (the A operand of the first product, free again once that
+// product completes), two chunks deep; ring Y holds the rest of the region
+// (Kbar^T, [H; T B], gamma, at their workspace offsets less A2) and this CTA's
+// 32 columns of the chunk's value rows, bf16 MN-major (K = token, N =
+// column), the B operand of U = (T B) V, three chunks deep: free once the
+// chunk's last product (H Z) completes, and wanted a chunk early (U is formed
+// one chunk ahead). One bulk copy fills an X slot; one bulk copy and 32 lanes
+// of 16-byte cp.async a Y slot.
+constexpr int kXBufs = 2, kYBufs = 3;
+constexpr int kXBytes = (int)TcRegion::A2;                           // 32 KiB
+constexpr uint32_t kYCopy = (uint32_t)(TcRegion::shared - TcRegion::A2);  // bulk part of a Y slot
+constexpr int kYA2 = 0, kYHT = (int)(TcRegion::HT - TcRegion::A2), kYGam = (int)(TcRegion::Gam - TcRegion::A2);
+constexpr int kYV = (int)kYCopy;
+constexpr uint32_t kVBytes = C * kTN * 2;
+constexpr int kYBytes = (kYV + (int)kVBytes + 1023) / 1024 * 1024;   // 37 KiB
+static_assert(kYV % 16 == 0 && kYCopy % 16 == 0, "bulk copies move 16-byte units");
+constexpr uint32_t kBvLbo = 128, kBvSbo = 1024;  // value rows as an MN-major B operand
+constexpr int kP2Y = kXBufs * kXBytes;
+constexpr int kP2B1 = kP2Y + kYBufs * kYBytes;   // S (hi | lo) bf16, MN-major [K = ch][N = 64]
+constexpr int kP2B2 = kP2B1 + 16384;             // [Z_hi | Z_lo] bf16, MN-major [K = token][N = 64]
+// mbarriers: X landed[2], X free[2] (tensor-core commits), Y landed[3] (the
+// bulk copy's bytes plus one arrival per copy-warp lane for its cp.async),
+// Y free[3], first product, second product, H Z product, U product[2] (by
+// chunk parity: U of the next chunk can complete before a compute thread
+// waits for this chunk's), and the first product as the off-chain issuing
+// warp sees it (two arrivals: the product's commit and that warp's own, made
+// once it has seen the phase before, so the barrier never runs a phase ahead
+// of the warp); then the TMEM base and the error flag.
 constexpr int kP2Bar = kP2B2 + 8192;
-constexpr int kP2NBar = 2 * kP2Bufs + 3;
+constexpr int kP2NBar = 2 * kXBufs + 2 * kYBufs + 6;
 constexpr int kP2Tmem = kP2Bar + 8 * kP2NBar;
 constexpr int kP2Err = kP2Tmem + 4;
 // Fused output gate (4-CTA cluster): three mbarriers (the partial sums of a
@@ -862,9 +852,10 @@ constexpr int kP2Err = kP2Tmem + 4;
 // gate logits of this CTA's 32 columns for one chunk (bf16 [64 tokens][32],
 // a tensor-map tile: global loads would hold the output warps at their next
 // named barrier until they return).
-constexpr int kP2RedBar = kP2Err + 4;
-constexpr int kP2Loc = kP2RedBar + 32;   // fp32 [4 column groups][64 rows]
+constexpr int kP2RedBar = (kP2Err + 4 + 7) / 8 * 8;
+constexpr int kP2Loc = (kP2RedBar + 24 + 15) / 16 * 16;  // fp32 [4 column groups][64 rows]
 constexpr int kP2Red = kP2Loc + 1024;    // fp32 [2 parities][4 CTAs][64 rows]
+static_assert(kP2Red % 16 == 0, "the row partials arrive as 16-byte asynchronous stores");
 constexpr int kP2Z = (kP2Red + 2048 + 127) / 128 * 128;
 constexpr uint32_t kZBytes = C * kTN * 2;
 constexpr int kP2Smem = kP2Z + (int)kZBytes;
@@ -872,13 +863,15 @@ static_assert(kP2RedBar % 8 == 0, "mbarriers must be 8-byte aligned");
 constexpr int kBarO = 3;                 // named barrier of the output warps
 constexpr uint32_t kRedBytes = (D / kTN) * 64 * 4;  // row partials a CTA receives per chunk
 constexpr int kGateCluster = D / kTN;    // CTAs of a head's state = the cluster
-static_assert(kBufBytes % 1024 == 0 && kP2B1 % 1024 == 0, "operand tiles must stay 1 KiB aligned");
+static_assert(kXBytes % 1024 == 0 && kYBytes % 1024 == 0 && kP2Y % 1024 == 0 && kP2B1 % 1024 == 0,
+              "operand tiles must stay 1 KiB aligned");
+constexpr int kUCol = 192;  // TMEM columns of U: [192, 224) and [224, 256), by chunk parity
 static_assert(kP2Smem <= 232448, "phase-2 shared memory exceeds 227 KiB");
 constexpr uint32_t kB1Lbo = 128, kB1Sbo = 2048;
 constexpr uint32_t kB2Lbo = 128, kB2Sbo = 1024;
 // TMEM columns: D1 alternates between [0, 64) and [64, 128) from chunk to
 // chunk (the token outputs of chunk n are read while chunk n + 1's first
-// product runs); D2 = Kbar^T Z at [128, 192).
+// product runs); D2 = Kbar^T Z at [128, 192); U at [192, 256) (kUCol).
 constexpr int kD2Col = 128;
 
 // Which chunks a state-pass launch walks. The serial pass is one segment of
@@ -925,7 +918,8 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
               const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens,
               int T_fixed, const float *init_state, __nv_bfloat16 *__restrict__ out,
               float *final_state, int H, int *__restrict__ status, const SegPass sp,
-              const OutGate og, const __grid_constant__ CUtensorMap tm_z) {
+              const OutGate og, const __grid_constant__ CUtensorMap tm_z,
+              const __nv_bfloat16 *__restrict__ vin) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const bool gated = og.z != nullptr;
     // A call whose chunk table was refused (or that already failed) does
@@ -986,11 +980,15 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     }
     unsigned char *B1 = sm + kP2B1;
     unsigned char *B2 = sm + kP2B2;
-    uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + kP2Bar);  // [kP2Bufs] tiles landed
-    uint64_t *bar_fr = bar_ld + kP2Bufs;                            // [kP2Bufs] tiles consumed
-    uint64_t *bar_m1 = bar_fr + kP2Bufs;                            // first product done
+    uint64_t *bar_xl = reinterpret_cast<uint64_t *>(sm + kP2Bar);  // [kXBufs] X tiles landed
+    uint64_t *bar_xf = bar_xl + kXBufs;                             // [kXBufs] X tiles consumed
+    uint64_t *bar_yl = bar_xf + kXBufs;                             // [kYBufs] Y tiles landed
+    uint64_t *bar_yf = bar_yl + kYBufs;                             // [kYBufs] Y tiles consumed
+    uint64_t *bar_m1 = bar_yf + kYBufs;                             // first product done
     uint64_t *bar_m2 = bar_m1 + 1;                                  // second product done
     uint64_t *bar_m3 = bar_m2 + 1;                                  // H Z product done
+    uint64_t *bar_u = bar_m3 + 1;                                   // [2] U product done
+    uint64_t *bar_m1s = bar_u + 2;                                  // first product, off-chain warp
     uint64_t *red_full = reinterpret_cast<uint64_t *>(sm + kP2RedBar);  // [2] row partials arrived
     uint64_t *z_full = red_full + 2;                                    // gate logits landed
     float *loc = reinterpret_cast<float *>(sm + kP2Loc);
@@ -1044,7 +1042,10 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     }
     if (warp == 0) tmem_alloc<256>(tslot);
     if (tid == 0) {
-        for (int i = 0; i < kP2NBar; ++i) mbar_init(bar_ld + i, 1);
+        // Y landed: the bulk copy's arrival and one per copy-warp lane.
+        for (int i = 0; i < kP2NBar; ++i)
+            mbar_init(bar_xl + i, i >= 2 * kXBufs && i < 2 * kXBufs + kYBufs ? 33 : 1);
+        mbar_init(bar_m1s, 2);
         // every output thread of the four CTAs arrives once per chunk
         if (gated) {
             // Each chunk's phase: one local arrival (with the expected bytes,
@@ -1066,96 +1067,178 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     if (gated) cluster_sync();
     const uint32_t tmem = *tslot;
 
-    // Chunk ch lives in buffer ch % 3 and is that buffer's (ch / 3)-th use: its
-    // loads complete the phase of parity (ch / 3) & 1 of the buffer's "landed"
-    // barrier, and its release the phase of the same parity of the "free" one.
+    // Chunk ch lives in X slot ch % kXBufs and Y slot ch % kYBufs, the
+    // (ch / kXBufs)-th and (ch / kYBufs)-th use of each: its loads complete the
+    // phase of that parity of the slot's "landed" barrier, and its release
+    // the phase of the same parity of the "free" one.
     if (warp == kP2ProdWarp) {
-        if (lane == 0) {
-            int issued = 0;
-            for (int ch = 0; ch < nchunks && !*err; ++ch) {
-                const int b = ch % kP2Bufs;
-                if (ch >= kP2Bufs) wait(bar_fr + b, (uint32_t)(ch / kP2Bufs - 1) & 1);
-                if (*err) break;
-                const unsigned char *rg = ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes;
-                unsigned char *dst = sm + b * kBufBytes;
-                // Identity tiles take U = 0: no slab.
-                mbar_expect_tx(bar_ld + b, ident ? (uint32_t)TcRegion::shared : kLoadBytes);
-                bulk_g2s(dst, rg, (uint32_t)TcRegion::shared, bar_ld + b);
-                if (!ident)
-                    bulk_g2s(dst + kBufU, rg + TcRegion::U + (size_t)jt * kSlabBytes, kSlabBytes,
-                             bar_ld + b);
-                issued = ch + 1;
+        // Chunk c's copies go out as their slots free, in the order the slots
+        // free: Y (its chunk c - 3 finished) before X (the first product of
+        // chunk c - 2 finished). Lane 0 waits and issues the bulk copies; in a
+        // Y slot, lane l copies the value rows' 16-byte pieces l, l + 32, ...
+        // straight into the MN-major operand layout (tokens past the sequence
+        // read as zeros), and every lane arrives once its copies have landed.
+        int nx = 0, ny = 0;  // copies issued
+        for (int ch = 0; ch < nchunks; ++ch) {
+            bool go = true;
+            if (lane == 0) go = ch < kYBufs || wait(bar_yf + ch % kYBufs, (uint32_t)(ch / kYBufs - 1) & 1);
+            go = __shfl_sync(0xffffffffu, go, 0) != 0;
+            if (!go) break;
+            const unsigned char *rg = ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes;
+            {
+                unsigned char *dst = sm + kP2Y + (ch % kYBufs) * kYBytes;
+                uint64_t *bar = bar_yl + ch % kYBufs;
+                if (lane == 0) {
+                    mbar_expect_tx(bar, kYCopy);
+                    bulk_g2s(dst, rg + TcRegion::A2, kYCopy, bar);
+                }
+                if (!ident) {
+                    const int tok0 = (c0 + ch) * C;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const int idx = lane + 32 * m, kk = idx >> 2, gi = idx & 3;
+                        const bool in = tok0 + kk < len;
+                        const __nv_bfloat16 *src =
+                            in ? vin + ((size_t)(bos + tok0 + kk) * H + h) * D + j0 + 8 * gi : vin;
+                        cp_async16(dst + kYV + gi * kBvSbo + (kk >> 3) * kBvLbo + (kk & 7) * 16, src,
+                                   in ? 16u : 0u);
+                    }
+                }
+                cp_async_mbar_arrive(bar);
+                ny = ch + 1;
             }
-            // Every copy lands before the CTA exits (bounded waits; a buffer's
-            // last use is the newest phase of its barrier).
-            for (int cc = issued > kP2Bufs ? issued - kP2Bufs : 0; cc < issued; ++cc)
-                mbar_wait(bar_ld + cc % kP2Bufs, (uint32_t)(cc / kP2Bufs) & 1);
+            if (lane == 0) go = ch < kXBufs || wait(bar_xf + ch % kXBufs, (uint32_t)(ch / kXBufs - 1) & 1);
+            go = __shfl_sync(0xffffffffu, go, 0) != 0;
+            if (!go) break;
+            if (lane == 0) {
+                uint64_t *bar = bar_xl + ch % kXBufs;
+                mbar_expect_tx(bar, (uint32_t)kXBytes);
+                bulk_g2s(sm + (ch % kXBufs) * kXBytes, rg, (uint32_t)kXBytes, bar);
+            }
+            nx = ch + 1;
+        }
+        // Every copy lands before the CTA exits (bounded; a slot's last use
+        // is the newest phase of its barrier).
+        cp_async_wait_all();
+        if (lane == 0) {
+            for (int cc = nx > kXBufs ? nx - kXBufs : 0; cc < nx; ++cc)
+                mbar_wait(bar_xl + cc % kXBufs, (uint32_t)(cc / kXBufs) & 1);
+            for (int cc = ny > kYBufs ? ny - kYBufs : 0; cc < ny; ++cc)
+                mbar_wait(bar_yl + cc % kYBufs, (uint32_t)(cc / kYBufs) & 1);
         }
         __syncwarp();
     } else if (warp == kP2MmaWarp) {
         // One lane issues; the whole warp keeps the named-barrier protocol, so
         // the compute warps never wait on a barrier that cannot complete.
-        // Descriptors of buffer 0's tiles and of the state-side operands are
-        // built once; a chunk adds its buffer's offset and a K step a constant
+        // Descriptors of slot 0's tiles and of the state-side operands are
+        // built once; a chunk adds its slot's offset and a K step a constant
         // (the address field is the byte address / 16).
         const uint64_t d_a1 = desc(smem_u32(sm), kA1Lbo, kA1Sbo);
-        const uint64_t d_a2 = desc(smem_u32(sm + kBufA2), kA2Lbo, kA2Sbo);
-        const uint64_t d_h = desc(smem_u32(sm + kBufH), 1024, 128);
+        const uint64_t d_a2 = desc(smem_u32(sm + kP2Y + kYA2), kA2Lbo, kA2Sbo);
         const uint64_t d_b1 = desc(smem_u32(B1), kB1Lbo, kB1Sbo);
         const uint64_t d_b2 = desc(smem_u32(B2), kB2Lbo, kB2Sbo);
         const uint32_t id1 = idesc_bf16(128, 2 * kTN, 1, 1), id2 = idesc_bf16(128, 2 * kTN, 0, 1);
-        // Chunk ch's tiles are waited for before its first product: chunk 0's
-        // here, every later one while the compute warps update the state of
-        // the chunk before it (off the chain of dependent steps).
-        bool ok_ld = true;
-        if (lane == 0 && nchunks > 0) ok_ld = wait(bar_ld, 0);
+        bool ok = true;  // lane 0: every wait so far succeeded
         for (int ch = 0; ch < nchunks; ++ch) {
-            const int b = ch % kP2Bufs;
-            const uint64_t boff = (uint64_t)b * (kBufBytes >> 4);
+            const uint64_t xo = (uint64_t)(ch % kXBufs) * (kXBytes >> 4);
+            const uint64_t yo = (uint64_t)(ch % kYBufs) * (kYBytes >> 4);
             const uint32_t d1 = tmem + 64 * (ch & 1);
-            if (lane == 0 && ok_ld) {
-                // [s Qbar S; W S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
-                fence_after();
+            if (lane == 0) {
+                // Chunk 0's tiles; a later chunk's were waited for before the
+                // state barrier (off the chain of dependent steps).
+                if (ch == 0) ok = ok && wait(bar_xl, 0);
+                if (ok) {
+                    // [s Qbar S; W S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
+                    fence_after();
 #pragma unroll
-                for (int s = 0; s < D / 16; ++s)
-                    mma_bf16(d1, d_a1 + boff + s * (2 * kA1Lbo >> 4), d_b1 + s * (2 * kB1Lbo >> 4),
-                             id1, s > 0);
-                commit(bar_m1);
+                    for (int s = 0; s < D / 16; ++s)
+                        mma_bf16(d1, d_a1 + xo + s * (2 * kA1Lbo >> 4), d_b1 + s * (2 * kB1Lbo >> 4),
+                                 id1, s > 0);
+                    commit(bar_m1);
+                    commit(bar_m1s);
+                }
+                // The X slot is free once everything issued so far has completed.
+                commit(bar_xf + ch % kXBufs);
+                // The second product reads the Y tiles (landed long ago: U of
+                // this chunk was formed from them).
+                ok = ok && wait(bar_yl + ch % kYBufs, (uint32_t)(ch / kYBufs) & 1);
             }
             __syncwarp();
             bar_sync(kBarZ, kP2Sync);  // Z of this chunk is in B2
             fence_after();
             if (lane == 0) {
-                if (ok_ld) {
-                    // D2 = Kbar^T [Z_hi | Z_lo] (N = 64); then D1 += H [Z_hi | Z_lo], which
-                    // adds H Z to the s Qbar S rows 0-63 (rows 64-127 take products of
-                    // whatever follows H in shared memory; W S there is consumed).
+                if (ok) {
+                    // D2 = Kbar^T [Z_hi | Z_lo] (N = 64).
 #pragma unroll
                     for (int s = 0; s < C / 16; ++s)
-                        mma_bf16(tmem + kD2Col, d_a2 + boff + s * (2 * kA2Lbo >> 4),
+                        mma_bf16(tmem + kD2Col, d_a2 + yo + s * (2 * kA2Lbo >> 4),
                                  d_b2 + s * (2 * kB2Lbo >> 4), id2, s > 0);
                     commit(bar_m2);
                 }
-                // The compute warps saw this chunk's first product complete, and
-                // with it every product of the previous chunk: its buffer is free.
-                // Then the next chunk's tiles; both while the products run, before
-                // the H Z issue below, which holds this thread until the tensor
-                // pipe has taken it.
-                if (ch > 0) mbar_arrive(bar_fr + (ch - 1) % kP2Bufs);
-                const bool ok_next = ch + 1 >= nchunks || !ok_ld ||
-                                     wait(bar_ld + (ch + 1) % kP2Bufs, (uint32_t)((ch + 1) / kP2Bufs) & 1);
-                if (ok_ld && outputs) {
-#pragma unroll
-                    for (int s = 0; s < C / 16; ++s)
-                        mma_bf16(d1, d_h + boff + s * (2 * 1024 >> 4), d_b2 + s * (2 * kB2Lbo >> 4),
-                                 id2, 1);
-                    commit(bar_m3);
-                }
-                ok_ld = ok_ld && ok_next;
+                // Without outputs this is the Y slot's last reader; with them
+                // the other issuing warp releases it after H Z.
+                if (!outputs) commit(bar_yf + ch % kYBufs);
+                if (ch + 1 < nchunks)
+                    ok = ok && wait(bar_xl + (ch + 1) % kXBufs, (uint32_t)((ch + 1) / kXBufs) & 1);
             }
             __syncwarp();
             bar_sync(kBarS, kP2Sync);  // the new state is in B1
             fence_after();
+        }
+        __syncwarp();
+    } else if (warp == kP2SideWarp) {
+        // U of chunk ch + 1 = [H; T B] times its value rows (rows 64-127 of the
+        // product; the H rows give nothing used), into TMEM columns by chunk
+        // parity, once chunk ch's first product has completed (the pipe runs it
+        // while the compute warps form Z); chunk 0's first. Then, with
+        // outputs, D1 += [H; T B] [Z_hi | Z_lo] once the second product has
+        // completed, which adds H Z to the s Qbar S rows 0-63 (rows 64-127
+        // take (T B) Z; W S there is consumed). The value rows were written by
+        // cp.async (generic proxy): a proxy fence after the landed barrier's
+        // wait hands them to the tensor core.
+        // Phases stay in step: the first product's barrier here completes a
+        // phase only with this warp's arrival; chunk ch + 1's second product
+        // needs the outputs of chunk ch read, hence H Z of chunk ch issued
+        // after this warp saw chunk ch's second product.
+        if (lane == 0 && (outputs || !ident)) {
+            const uint64_t d_ht = desc(smem_u32(sm + kP2Y + kYHT), kA2Lbo, kA2Sbo);
+            const uint64_t d_v = desc(smem_u32(sm + kP2Y + kYV), kBvLbo, kBvSbo);
+            const uint64_t d_b2 = desc(smem_u32(B2), kB2Lbo, kB2Sbo);
+            const uint32_t id2 = idesc_bf16(128, 2 * kTN, 0, 1), idu = idesc_bf16(128, kTN, 0, 1);
+            bool ok = true;
+            auto issue_u = [&](int ch) {
+                ok = ok && wait(bar_yl + ch % kYBufs, (uint32_t)(ch / kYBufs) & 1);
+                if (!ok) return;
+                const uint64_t yo = (uint64_t)(ch % kYBufs) * (kYBytes >> 4);
+                fence_async_smem();
+                fence_after();
+#pragma unroll
+                for (int s = 0; s < C / 16; ++s)
+                    mma_bf16(tmem + kUCol + kTN * (ch & 1), d_ht + yo + s * (2 * kA2Lbo >> 4),
+                             d_v + yo + s * (2 * kBvLbo >> 4), idu, s > 0);
+                commit(bar_u + (ch & 1));
+            };
+            if (!ident && nchunks > 0) issue_u(0);
+            mbar_arrive(bar_m1s);  // chunk 0's phase
+            for (int ch = 0; ch < nchunks && ok; ++ch) {
+                if (!ident && ch + 1 < nchunks) {
+                    spin(bar_m1s, (uint32_t)ch & 1);
+                    mbar_arrive(bar_m1s);  // chunk ch + 1's phase
+                    issue_u(ch + 1);
+                }
+                if (outputs && ok) {
+                    spin(bar_m2, (uint32_t)ch & 1);
+                    if (*err) break;
+                    fence_after();
+                    const uint64_t yo = (uint64_t)(ch % kYBufs) * (kYBytes >> 4);
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        mma_bf16(tmem + 64 * (ch & 1), d_ht + yo + s * (2 * kA2Lbo >> 4),
+                                 d_b2 + s * (2 * kB2Lbo >> 4), id2, 1);
+                    commit(bar_m3);
+                    commit(bar_yf + ch % kYBufs);
+                }
+            }
         }
         __syncwarp();
     } else {
@@ -1275,19 +1358,18 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             if (r < clen) *reinterpret_cast<uint4 *>(out + orow) = pack8(o8);
         };
         for (int ch = 0; ch < nchunks; ++ch) {
-            const int b = ch % kP2Bufs;
-            unsigned char *buf = sm + b * kBufBytes;
             const uint32_t d1 = tmem + 64 * (ch & 1);
-            // The tiles landed long ago (the first product used them); this
-            // thread's own wait makes the copied U and gamma visible to it.
-            wait(bar_ld + b, (uint32_t)(ch / kP2Bufs) & 1);
-            // This chunk's U row and decay, read while the first product runs.
-            const float gam = reinterpret_cast<const float *>(buf + kBufGam)[r];
-            float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f), u1 = u0;
+            // The Y tiles landed before this chunk's U was formed; this
+            // thread's own wait makes the copied decay visible to it.
+            wait(bar_yl + ch % kYBufs, (uint32_t)(ch / kYBufs) & 1);
+            const float gam =
+                reinterpret_cast<const float *>(sm + kP2Y + (ch % kYBufs) * kYBytes + kYGam)[r];
+            // This chunk's U row (formed while the previous state was updated).
+            float uv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (zrow && !ident) {
-                const float *Us = reinterpret_cast<const float *>(buf + kBufU);
-                u0 = *reinterpret_cast<const float4 *>(Us + slab_idx(r - 64, js));
-                u1 = *reinterpret_cast<const float4 *>(Us + slab_idx(r - 64, js + 4));
+                spin(bar_u + (ch & 1), (uint32_t)(ch >> 1) & 1);
+                fence_after();
+                tmem_ld8(tmem + lane_base + kUCol + kTN * (ch & 1) + js, uv);
             }
             if (!zrow && outputs && ch > 0) {
                 // The previous chunk's outputs, complete once its H Z product is:
@@ -1296,6 +1378,13 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 p3 ^= 1;
                 fence_after();
                 put_outputs_a(ch - 1);
+            }
+            if (zrow && outputs && ch > 0) {
+                // The previous chunk's H Z product reads B2, which this chunk's
+                // Z overwrites (it is issued by another thread than the first
+                // product, whose completion therefore does not imply its own).
+                wait(bar_m3, p3);
+                p3 ^= 1;
             }
             spin(bar_m1, p1);
             p1 ^= 1;
@@ -1307,7 +1396,6 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 tmem_ld8(d1 + lane_base + js, hi);
                 tmem_ld8(d1 + lane_base + kTN + js, lo);
                 tmem_wait_ld();
-                const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
                 float z[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) z[j] = uv[j] - (hi[j] + lo[j]);
@@ -1542,11 +1630,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const int sm_count = sm_counts[dev];
     if ((err = mark(events, 1, stream)) != cudaSuccess) return err;
     if (slots > 0 && tokens > 0) {
-        CUtensorMap tq, tk, tv, tg;
+        CUtensorMap tq, tk, tg;
         memset(&tg, 0, sizeof(tg));  // read only with a per-channel g
         if ((err = token_rows_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
-            (err = token_rows_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
-            (err = token_rows_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess)
+            (err = token_rows_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess)
             return err;
         if (pro.decay == KDA_DECAY_CHANNEL &&
             (err = token_rows_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tokens)) != cudaSuccess)
@@ -1564,7 +1651,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         }
         const int *used = seq_first_slot + num_seqs;
 #define KDA_P1_LAUNCH(V)                                                                        \
-    tc_intra_chunk<V><<<grid, kP1Threads, P1::bytes, stream>>>(tq, tk, tv, tg, g, pro, beta, scale, \
+    tc_intra_chunk<V><<<grid, kP1Threads, P1::bytes, stream>>>(tq, tk, tg, g, pro, beta, scale,     \
                                                                table, used, slots, H, region, status)
         switch (var) {
             case kVarChannel: KDA_P1_LAUNCH(kVarChannel); break;
@@ -1585,6 +1672,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         // The fused output gate runs on the serial chain (its clusters are the
         // four column tiles of one sequence and head).
         const OutGate og{static_cast<const __nv_bfloat16 *>(gate.z), gate.w, gate.eps};
+        const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(v);
         CUtensorMap tz;
         memset(&tz, 0, sizeof(tz));  // read only by the fused gate
         if (og.z && (err = gate_rows_map(&tz, og.z, H, tokens)) != cudaSuccess) return err;
@@ -1607,13 +1695,13 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             if ((err = cudaLaunchKernelEx(&cfg, tc_state_pass, (const unsigned char *)region,
                                           seq_first_slot, order, cu_seqlens, T_fixed, init_state,
                                           static_cast<__nv_bfloat16 *>(out), final_state, H, status,
-                                          sp, og, tz)) != cudaSuccess)
+                                          sp, og, tz, vin)) != cudaSuccess)
                 return err;
         } else if (P <= 1) {
             const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
             tc_state_pass<<<(unsigned)num_seqs * H * kTiles, kP2Threads, kP2Smem, stream>>>(
                 region, seq_first_slot, order, cu_seqlens, T_fixed, init_state,
-                static_cast<__nv_bfloat16 *>(out), final_state, H, status, sp, og, tz);
+                static_cast<__nv_bfloat16 *>(out), final_state, H, status, sp, og, tz, vin);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         } else {
             const int L = (nch + P - 1) / P;
@@ -1624,7 +1712,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * 2 * kTiles, kP2Threads, kP2Smem,
                             stream>>>(region, seq_first_slot, order, cu_seqlens, T_fixed,
                                       init_state, static_cast<__nv_bfloat16 *>(out), final_state,
-                                      H, status, sa, og, tz);
+                                      H, status, sa, og, tz, vin);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
             if (Pn > 2) {
                 seg_combine<<<(unsigned)num_seqs * H * (D / kCombCols), kCombThreads, kCombSmem,
@@ -1635,7 +1723,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * kTiles, kP2Threads, kP2Smem,
                             stream>>>(region, seq_first_slot, order, cu_seqlens, T_fixed,
                                       init_state, static_cast<__nv_bfloat16 *>(out), final_state,
-                                      H, status, sc, og, tz);
+                                      H, status, sc, og, tz, vin);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     }

@@ -287,6 +287,21 @@ __device__ __forceinline__ void cluster_sync() {
                      : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async); with src_bytes < 16
+// the rest of the 16 bytes is filled with zeros (src_bytes = 0: zeros only).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// An arrival on mbar once every earlier cp.async of this thread has landed
+// (the arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *mbar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(mbar))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // 1-D bulk copy global -> shared, completing `bytes` transactions on mbar.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
