@@ -98,8 +98,8 @@ typedef enum {
 
 /*
  * Options of kda_chunk_fwd_opt and kda_decode_step_opt. A NULL pointer means
- * {KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0, 0, 0}, the behaviour of kda_chunk_fwd and
- * kda_decode_step.
+ * {KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0, 0, 0, 0}, the behaviour of kda_chunk_fwd
+ * and kda_decode_step.
  *  decay       layout of g (above)
  *  gate        meaning of g's values (above); ignored with KDA_DECAY_NONE
  *  gate_lower  KDA_GATE_BOUNDED only: the lower bound of log a_t, finite and
@@ -124,6 +124,17 @@ typedef enum {
  *              chains leave most of the GPU idle and T >= 2048, else 1.
  *              Results equal the serial chain's up to fp32 rounding. Must be
  *              >= 0; ignored by the decode step and the fp32 SIMT path.
+ *  fused       prefill only, tensor-core path: 0 (the default) lets the call
+ *              run phase 1 and the state pass as ONE cooperative launch when
+ *              that is expected to be faster: a serial chain (segments
+ *              resolves to 1), fixed-length batches or a single packed
+ *              sequence, and few enough (sequence, head) chains that the
+ *              state pass (two CTAs per chain) leaves SMs to phase 1, which
+ *              hands each chunk over through a ready flag in the workspace.
+ *              1: the fused launch whenever those conditions (all but the
+ *              expected speed) hold. -1: always the two launches. Results
+ *              equal the two launches' up to fp32 rounding. Other values are
+ *              rejected.
  */
 typedef struct {
     kda_decay decay;
@@ -131,6 +142,7 @@ typedef struct {
     float gate_lower;
     int l2norm_qk;
     int segments;
+    int fused;
 } kda_options;
 
 /* Human-readable name of a status code (static storage; never NULL). */
@@ -277,13 +289,15 @@ kda_status kda_chunk_fwd_host(const void *q, const void *k, const void *v, const
  *          there are no tokens)
  *  weight  [dv] fp32 per-channel scale shared by the heads, or NULL (ones)
  *  eps     finite, > 0 (1e-6 is customary)
- * On the tensor-core path (bf16, d = 128) the gate is applied inside the state
- * pass, from the fp32 outputs, before the single write of `out`: the four
- * CTAs that hold a head's 128 output columns form a thread-block cluster and
- * exchange per-row sums of squares through distributed shared memory. The
- * state then crosses chunks in one serial chain (options->segments is
- * ignored). On the fp32 path the gate is a pass over the written outputs
- * (kda_output_gate_rmsnorm in place). The ungated outputs are not kept.
+ * On the tensor-core path (bf16, d = 128) the state crosses chunks in one
+ * serial chain (options->segments is ignored). Where the fused single launch
+ * applies (see kda_options.fused) the call runs it with plain outputs and
+ * then the gate as a pass over them (kda_output_gate_rmsnorm in place);
+ * otherwise the gate is applied inside the state pass, from the fp32 outputs,
+ * before the single write of `out`: the four CTAs that hold a head's 128
+ * output columns form a thread-block cluster and exchange per-row sums of
+ * squares through distributed shared memory. On the fp32 path the gate is a
+ * pass over the written outputs. The ungated outputs are not kept.
  * Workspace and errors as kda_chunk_fwd; eps, z and weight are checked first.
  */
 kda_status kda_chunk_fwd_gated(const void *q, const void *k, const void *v, const float *g,

@@ -21,7 +21,7 @@ GATE = {"log": 0, "logsigmoid": 1, "bounded": 2}          # kda_gate
 class Options(ctypes.Structure):
     """kda_options of include/kda.h."""
     _fields_ = [("decay", ctypes.c_int), ("gate", ctypes.c_int), ("gate_lower", ctypes.c_float),
-                ("l2norm_qk", ctypes.c_int), ("segments", ctypes.c_int)]
+                ("l2norm_qk", ctypes.c_int), ("segments", ctypes.c_int), ("fused", ctypes.c_int)]
 
 
 _vp = ctypes.c_void_p

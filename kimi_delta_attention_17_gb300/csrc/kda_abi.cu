@@ -189,6 +189,7 @@ bool make_prologue(const kda_options *o, Prologue *p) {
         return false;
     if (o->gate == KDA_GATE_BOUNDED && !(o->gate_lower >= -10.f && o->gate_lower < 0.f)) return false;
     if (o->segments < 0) return false;
+    if (o->fused < -1 || o->fused > 1) return false;
     *p = Prologue{(int)o->decay, (int)o->gate, o->gate == KDA_GATE_BOUNDED ? o->gate_lower : 0.f,
                   o->l2norm_qk ? 1 : 0};
     return true;
@@ -276,8 +277,8 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const flo
         err = launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
                                 T_fixed, (long long)B * T, H, num_seqs, slots, table, seq_first_slot,
                                 reinterpret_cast<unsigned char *>(region), status, pro,
-                                options ? options->segments : 0, seg_max, seg_ws, gate, stream,
-                                events);
+                                options ? options->segments : 0, seg_max, seg_ws, gate,
+                                options ? options->fused : 0, stream, events);
     else {
         err = launch_prefill_simt(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
                                   final_state, T_fixed, H, dk, num_seqs, dtype, slots, table,

@@ -152,7 +152,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, const Prologue &pro,
                               int segments, int seg_max, float *seg_ws, const GateParams &gate,
-                              cudaStream_t stream, cudaEvent_t *events);
+                              int fused, cudaStream_t stream, cudaEvent_t *events);
 
 // Records events[i] (when non-NULL) on the stream: the prefill marks the
 // start (0), the end of the chunk table (1), of the intra-chunk phase (2) and

@@ -64,9 +64,8 @@ constexpr int kTN = 32;  // state columns per phase-2 CTA
 struct TcRegion {
     static constexpr size_t A1 = 0;        // [s Qbar; W] bf16, MN-major, 128 tokens x 128 ch
     static constexpr size_t A2 = 32768;    // Kbar^T bf16, K-major, 128 ch x 64 tokens
-    static constexpr size_t HT = 49152;    // [H; T B] bf16, K-major [row][token j] (LBO 2048, SBO 128)
-    static constexpr size_t Gam = 65536;   // fp32 [128] exp(G_n)
-    static constexpr size_t shared = 66048;  // bytes of the part above
+    static constexpr size_t Gam = 49152;   // fp32 [128] exp(G_n)
+    static constexpr size_t HT = 49664;    // [H; T B] bf16, K-major [row][token j] (LBO 2048, SBO 128)
     static constexpr size_t bytes = 66048;
 };
 static_assert(TcRegion::bytes % 256 == 0, "regions stay 256-byte aligned");
@@ -189,14 +188,26 @@ __device__ __noinline__ void steep_diagonal_blocks(unsigned char *sm, int tid, i
 // through the log-sigmoid with q and k normalised (the KDA layer's own
 // prologue); 1 takes every option at run time.
 constexpr int kVarChannel = 0, kVarRuntime = 1, kVarScalar = 2, kVarNone = 3, kVarGated = 4;
+// How a phase-1 CTA walks the items: its rank among the phase-1 CTAs and
+// their count; in the fused prefill also the ready flags it sets and the item
+// order (ilv > 1: chunk-major over ilv fixed-length sequences of nch chunks
+// each, so that chunk c of every sequence is ready at about the same time).
+struct P1Walk {
+    int rank, count;
+    int *ready;  // [slot][H]: 1 once the item's region is written; NULL: no flags
+    int ilv, nch;
+};
+
+// Phase 1 for the threads 0 .. kP1Threads - 1 of a CTA (its barriers count
+// exactly those threads, so a larger CTA may run it with the rest idle).
 template <int kVar>
-__global__ void __launch_bounds__(kP1Threads, 1)
-tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_g,
-               const float *__restrict__ g_head, Prologue pro,
-               const float *__restrict__ beta, float scale, const ChunkEntry *__restrict__ table,
-               const int *__restrict__ used_slots, long long nslots, int H,
-               unsigned char *__restrict__ ws, int *__restrict__ status) {
+__device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                                                 const CUtensorMap *tm_g, const float *__restrict__ g_head,
+                                                 Prologue pro, const float *__restrict__ beta, float scale,
+                                                 const ChunkEntry *__restrict__ table,
+                                                 const int *__restrict__ used_slots, long long nslots,
+                                                 int H, unsigned char *__restrict__ ws,
+                                                 int *__restrict__ status, const P1Walk wk) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
     const int c = tid & 127, blk = tid >> 7;  // channel; 16-token block / column group
@@ -209,7 +220,9 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // Items are (slot, head) pairs, heads fastest; CTA b takes items b, b + grid,
     // ...: stepping by the grid in (slot, head) form keeps 64-bit divisions off
     // the item path.
-    const int step_s = (int)(gridDim.x / H), step_h = (int)(gridDim.x % H);
+    const int step_s = (int)(wk.count / H), step_h = (int)(wk.count % H);
+    // The table slot of the item order's slot index.
+    auto phys = [&](int s) { return wk.ilv > 1 ? (s % wk.ilv) * wk.nch + s / wk.ilv : s; };
     auto advance = [&](int &sl, int &hh) {
         sl += step_s;
         hh += step_h;
@@ -226,7 +239,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_fence_init();
     }
     fence_before();
-    __syncthreads();
+    bar_sync(0, kP1Threads);
     fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -249,9 +262,9 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     auto issue = [&](int hh, const ChunkEntry e) {
         if (tid != 0) return;
         mbar_expect_tx(bar_ld, 64u * (2u * 256u + (g_tile ? 512u : 0u)));
-        tma_load_3d(sm + P1::q, &tm_q, 0, hh, e.bos, bar_ld);
-        tma_load_3d(sm + P1::k, &tm_k, 0, hh, e.bos, bar_ld);
-        if (g_tile) tma_load_3d(sm + P1::g, &tm_g, 0, hh, e.bos, bar_ld);
+        tma_load_3d(sm + P1::q, tm_q, 0, hh, e.bos, bar_ld);
+        tma_load_3d(sm + P1::k, tm_k, 0, hh, e.bos, bar_ld);
+        if (g_tile) tma_load_3d(sm + P1::g, tm_g, 0, hh, e.bos, bar_ld);
     };
 
     // Each item's table entry and beta values are read one item ahead, so
@@ -266,11 +279,11 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                    ? g_head[(size_t)(e.bos + tid) * H + hh]
                    : 0.f;
     };
-    int sl = (int)(blockIdx.x / H), hc = (int)(blockIdx.x % H);  // this item
+    int sl = (int)(wk.rank / H), hc = (int)(wk.rank % H);  // this item
     ChunkEntry ce{};
     float bcur = 0.f;
     if (sl < used) {
-        ce = table[sl];
+        ce = table[phys(sl)];
         issue(hc, ce);
         bcur = beta_of(hc, ce);
         if (pro.decay == KDA_DECAY_SCALAR && tid < C)
@@ -279,7 +292,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     int sn = sl, hn = hc;  // the next item
     advance(sn, hn);
-    ChunkEntry en = sn < used ? table[sn] : ce;
+    ChunkEntry en = sn < used ? table[phys(sn)] : ce;
     uint32_t ld_phase = 0, mma_phase = 0;
     bool ok = true;
     bool steep = false;  // this item takes the steep-decay form
@@ -288,8 +301,8 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         int snn = sn, hnn = hn;  // the item after next
         ChunkEntry enn;
         float bn, gn;
-        unsigned char *reg = ws + ((size_t)sl * H + hc) * TcRegion::bytes;
-        ok = __syncthreads_and(mbar_wait(bar_ld, ld_phase));
+        unsigned char *reg = ws + ((size_t)phys(sl) * H + hc) * TcRegion::bytes;
+        ok = bar_and(0, kP1Threads, mbar_wait(bar_ld, ld_phase));
         ld_phase ^= 1;
         if (!ok) break;
 
@@ -380,12 +393,12 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // (the log-decay is non-increasing within the block); over
             // kSteepNats anywhere, the whole item takes the steep-decay form
             // (the decision is CTA-uniform).
-            steep = __syncthreads_or(acc < -kSteepNats) != 0;
+            steep = bar_or(0, kP1Threads, acc < -kSteepNats) != 0;
             // The table entry of the item after next and the next item's beta,
             // read here: a CTA barrier waits for its threads' loads, and the next
             // one is the whole elementwise pass away.
             advance(snn, hnn);
-            enn = snn < used ? table[snn] : en;
+            enn = snn < used ? table[phys(snn)] : en;
             bn = sn < used ? beta_of(hn, en) : 0.f;
             gn = sn < used ? ghead_of(hn, en) : 0.f;
             // References of every block for this channel, as cumulative
@@ -473,13 +486,13 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 float *gG = reinterpret_cast<float *>(sm + P1::g);
 #pragma unroll
                 for (int t = 0; t < 16; ++t) gG[(16 * blk + t) * D + c] = G[t];
-                __syncthreads();
+                bar_sync(0, kP1Threads);
                 steep_diagonal_blocks(sm, tid, len, pro.l2norm, scale);
             }
         }
         fence_async_smem();
         fence_before();
-        __syncthreads();
+        bar_sync(0, kP1Threads);
         fence_after();
 
         // ================= A / H = gated K K^T and Q K^T (M=128, N=160, K=128)
@@ -492,7 +505,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         // The staging rows are consumed: fetch the next item's while this one runs.
         if (sn < used) issue(hn, en);
-        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
+        ok = bar_and(0, kP1Threads, mbar_wait(bar_mma, mma_phase));
         mma_phase ^= 1;
         fence_after();
         if (!ok) break;
@@ -565,7 +578,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
         }
         fence_before();
-        __syncthreads();
+        bar_sync(0, kP1Threads);
 
         // ================= T = (I - A)^{-1}, then T Diag(beta) as a bf16 operand.
         {
@@ -633,7 +646,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     *reinterpret_cast<float2 *>(dst) = make_float2(x0[q], x1[q]);
                 }
             }
-            __syncthreads();
+            bar_sync(0, kP1Threads);
             // Off-diagonal blocks: with M_IK = T_II A_IK (K < I), block row I of
             // (I - A) T = I gives T_IJ = sum_{K = J}^{I - 1} M_IK T_KJ. The
             // substitution above formed the six M blocks; stage 2 forms the first
@@ -711,7 +724,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     const float4 a0 = init ? *reinterpret_cast<const float4 *>(init + r * kMS + 4 * cg) : z4;
                     put(dst, ds, r, cg, prod(a0, P, ps, Q, qs, r, cg));
                 }
-                __syncthreads();
+                bar_sync(0, kP1Threads);
             }
             {
                 // Row i, columns jb .. jb + 7 of T Diag(beta): one 16-byte run per thread.
@@ -735,7 +748,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         fence_async_smem();
         fence_before();
-        __syncthreads();
+        bar_sync(0, kP1Threads);
         fence_after();
 
         // ================= W = (T B) L
@@ -746,7 +759,7 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 mma_bf16(tmem + 0, d_lt + s * (2 * kA2Lbo >> 4), d_tb + s * (2 * 1024 >> 4), id, s > 0);
             commit(bar_mma);
         }
-        ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase));
+        ok = bar_and(0, kP1Threads, mbar_wait(bar_mma, mma_phase));
         mma_phase ^= 1;
         fence_after();
         if (!ok) break;
@@ -765,8 +778,11 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             reinterpret_cast<float *>(sm + P1::gsc)[tid] =
                 sn < used && tid < en.len ? log_decay(gn, pro) : 0.f;
         fence_before();
-        __syncthreads();
+        bar_sync(0, kP1Threads);
         fence_after();
+        // Every thread's region writes precede the barrier: the release makes
+        // them visible before the flag that hands the item to the state pass.
+        if (wk.ready && tid == 0) st_release_gpu(wk.ready + (size_t)phys(sl) * H + hc, 1);
         sl = sn;
         hc = hn;
         ce = en;
@@ -782,97 +798,116 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_wait(bar_mma, mma_phase);
     }
     fence_before();
-    __syncthreads();
+    bar_sync(0, kP1Threads);
     if (warp == 0) tmem_dealloc<256>(tmem);
 }
 
+template <int kVar>
+__global__ void __launch_bounds__(kP1Threads, 1)
+tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_g, const float *__restrict__ g_head, Prologue pro,
+               const float *__restrict__ beta, float scale, const ChunkEntry *__restrict__ table,
+               const int *__restrict__ used_slots, long long nslots, int H,
+               unsigned char *__restrict__ ws, int *__restrict__ status) {
+    intra_chunk_body<kVar>(&tm_q, &tm_k, &tm_g, g_head, pro, beta, scale, table, used_slots, nslots, H,
+                           ws, status, P1Walk{(int)blockIdx.x, (int)gridDim.x, nullptr, 1, 0});
+}
+
 // ---------------------------------------------------------------- phase 2
-// One CTA of 576 threads per (sequence, head, 32-column slab) and, with the
-// segmented pass, per segment. Compute thread t owns TMEM lane / state row
-// 32 (w % 4) + (t % 32) of warp w = t / 32 and slab columns 8 (w / 4) .. + 7.
+// One CTA of 576 threads per (sequence, head, TN-column slab of the state)
+// and, with the segmented pass, per segment: TN = 32 (four CTAs per head) in
+// the two-launch prefill, TN = 64 (two) in the fused one. Compute thread t
+// owns TMEM lane / state row 32 (w % 4) + (t % 32) of warp w = t / 32 and the
+// TN / 4 slab columns from (TN / 4) (w / 4).
 // Per chunk, with S the state entering it:
+//                  U  = (T B) V                 (formed a chunk ahead)
 //   round trip 1:  D1 = [s Qbar; W] S          (rows 0-63: Qbar S, 64-127: W S)
 //                  Z  = U - W S                 (lanes 64-127)
 //   round trip 2:  D2 = Kbar^T Z,  D1[0:64] += H Z
 //                  S <- Diag(exp G_n) S + D2,  O = D1[0:64] = s Qbar S + H Z
 // ("Understanding Kimi Delta Attention", "The token outputs" and "One state
-// crosses the chunk boundary"), with U = (T B) V formed a chunk ahead. S and
-// Z enter the MMAs as bf16 hi + lo pairs.
-// Warp roles: warps 0-15 compute; warp 16 issues the two products on the
-// chain of dependent steps and keeps the named barriers with the compute
-// warps; warp 18 issues the products off that chain (U, H Z), paced by
-// mbarriers alone: an MMA's issue holds its thread while the tensor pipe is
-// busy (about 100 cycles per M = 128, K = 16 step here), which must not delay
-// a barrier. Warp 17 issues the copies of the chunk tiles (a bulk copy's
-// issue can hold its thread for a hundred cycles or more).
+// crosses the chunk boundary"). S and Z enter the MMAs as bf16 hi + lo pairs.
+// Warp roles: warps 0-15 compute. Warp 16's lane 0 issues the two products on
+// the chain of dependent steps, and the warp keeps the named barriers with
+// the compute warps. Warp 17's lane 0 issues the copies of the chunk tiles and
+// warp 18's lane 0 the products off the chain (U a chunk ahead, H Z), both
+// paced by mbarriers alone: an MMA's issue holds its thread while the tensor
+// pipe is busy (about 60 cycles per M = 128, K = 16 step), and a bulk copy's
+// issue can too, which must not delay a named barrier. (Two roles in one warp
+// would stall each other: a suspended wait holds the whole warp.)
 constexpr int kP2Compute = 512;
 constexpr int kP2MmaWarp = kP2Compute / 32;
-constexpr int kP2ProdWarp = kP2MmaWarp + 1;
+constexpr int kP2CopyWarp = kP2MmaWarp + 1;
 constexpr int kP2SideWarp = kP2MmaWarp + 2;
 constexpr int kP2Threads = kP2Compute + 96;
 constexpr int kP2Sync = kP2Compute + 32;  // compute warps + MMA warp
 constexpr int kBarZ = 1, kBarS = 2;       // named barriers: Z written, state written
-// A chunk's tiles sit in two rings, by when they are consumed. Ring X holds
-// [s Qbar; W] (the A operand of the first product, free again once that
-// product completes), two chunks deep; ring Y holds the rest of the region
-// (Kbar^T, [H; T B], gamma, at their workspace offsets less A2) and this CTA's
-// 32 columns of the chunk's value rows, bf16 MN-major (K = token, N =
-// column), the B operand of U = (T B) V, three chunks deep: free once the
-// chunk's last product (H Z) completes, and wanted a chunk early (U is formed
-// one chunk ahead). One bulk copy fills an X slot; one bulk copy and 32 lanes
-// of 16-byte cp.async a Y slot.
-constexpr int kXBufs = 2, kYBufs = 3;
-constexpr int kXBytes = (int)TcRegion::A2;                           // 32 KiB
-constexpr uint32_t kYCopy = (uint32_t)(TcRegion::shared - TcRegion::A2);  // bulk part of a Y slot
-constexpr int kYA2 = 0, kYHT = (int)(TcRegion::HT - TcRegion::A2), kYGam = (int)(TcRegion::Gam - TcRegion::A2);
-constexpr int kYV = (int)kYCopy;
-constexpr uint32_t kVBytes = C * kTN * 2;
-constexpr int kYBytes = (kYV + (int)kVBytes + 1023) / 1024 * 1024;   // 37 KiB
-static_assert(kYV % 16 == 0 && kYCopy % 16 == 0, "bulk copies move 16-byte units");
+constexpr int kBarO = 3;                  // named barrier of the output warps (fused gate)
+// A chunk's tiles sit in three rings, by lifetime:
+//   X  [s Qbar; W], the first product's A operand: free once it completes; 2 deep.
+//   K  Kbar^T and gamma: free once the second product completes; 2 deep.
+//   H  [H; T B] and this CTA's TN columns of the chunk's value rows (bf16
+//      MN-major, K = token, N = column: the B operand of U), wanted a chunk
+//      early (U is formed a chunk ahead) and free once H Z (without outputs:
+//      U) completes; 3 deep.
+// A bulk copy fills an X or K slot; a bulk copy and a tensor-map copy an H slot.
+constexpr int kXBufs = 2, kKBufs = 2, kHBufs = 3;
+constexpr int kXBytes = (int)TcRegion::A2;                                 // 32 KiB
+constexpr uint32_t kKCopy = (uint32_t)(TcRegion::HT - TcRegion::A2);      // Kbar^T, gamma
+constexpr int kKGam = (int)(TcRegion::Gam - TcRegion::A2);
+constexpr int kKBytes = ((int)kKCopy + 1023) / 1024 * 1024;              // 17 KiB
+constexpr uint32_t kHTBytes = (uint32_t)(TcRegion::bytes - TcRegion::HT);  // 16 KiB
+static_assert(kKCopy % 16 == 0 && kHTBytes % 16 == 0 && TcRegion::HT % 16 == 0,
+              "bulk copies move 16-byte units from 16-byte boundaries");
 constexpr uint32_t kBvLbo = 128, kBvSbo = 1024;  // value rows as an MN-major B operand
-constexpr int kP2Y = kXBufs * kXBytes;
-constexpr int kP2B1 = kP2Y + kYBufs * kYBytes;   // S (hi | lo) bf16, MN-major [K = ch][N = 64]
-constexpr int kP2B2 = kP2B1 + 16384;             // [Z_hi | Z_lo] bf16, MN-major [K = token][N = 64]
-// mbarriers: X landed[2], X free[2] (tensor-core commits), Y landed[3] (the
-// bulk copy's bytes plus one arrival per copy-warp lane for its cp.async),
-// Y free[3], first product, second product, H Z product, U product[2] (by
-// chunk parity: U of the next chunk can complete before a compute thread
-// waits for this chunk's), and the first product as the off-chain issuing
-// warp sees it (two arrivals: the product's commit and that warp's own, made
-// once it has seen the phase before, so the barrier never runs a phase ahead
-// of the warp); then the TMEM base and the error flag.
-constexpr int kP2Bar = kP2B2 + 8192;
-constexpr int kP2NBar = 2 * kXBufs + 2 * kYBufs + 6;
-constexpr int kP2Tmem = kP2Bar + 8 * kP2NBar;
-constexpr int kP2Err = kP2Tmem + 4;
-// Fused output gate (4-CTA cluster): three mbarriers (the partial sums of a
-// chunk's rows from the four CTAs have arrived, one per chunk parity; the
-// chunk's gate logits have landed), this CTA's per-row partials of its four
-// column groups, the four CTAs' per-row partials (two chunk parities), and the
-// gate logits of this CTA's 32 columns for one chunk (bf16 [64 tokens][32],
-// a tensor-map tile: global loads would hold the output warps at their next
-// named barrier until they return).
-constexpr int kP2RedBar = (kP2Err + 4 + 7) / 8 * 8;
-constexpr int kP2Loc = (kP2RedBar + 24 + 15) / 16 * 16;  // fp32 [4 column groups][64 rows]
-constexpr int kP2Red = kP2Loc + 1024;    // fp32 [2 parities][4 CTAs][64 rows]
-static_assert(kP2Red % 16 == 0, "the row partials arrive as 16-byte asynchronous stores");
-constexpr int kP2Z = (kP2Red + 2048 + 127) / 128 * 128;
-constexpr uint32_t kZBytes = C * kTN * 2;
-constexpr int kP2Smem = kP2Z + (int)kZBytes;
-static_assert(kP2RedBar % 8 == 0, "mbarriers must be 8-byte aligned");
-constexpr int kBarO = 3;                 // named barrier of the output warps
-constexpr uint32_t kRedBytes = (D / kTN) * 64 * 4;  // row partials a CTA receives per chunk
-constexpr int kGateCluster = D / kTN;    // CTAs of a head's state = the cluster
-static_assert(kXBytes % 1024 == 0 && kYBytes % 1024 == 0 && kP2Y % 1024 == 0 && kP2B1 % 1024 == 0,
-              "operand tiles must stay 1 KiB aligned");
-constexpr int kUCol = 192;  // TMEM columns of U: [192, 224) and [224, 256), by chunk parity
-static_assert(kP2Smem <= 232448, "phase-2 shared memory exceeds 227 KiB");
 constexpr uint32_t kB1Lbo = 128, kB1Sbo = 2048;
 constexpr uint32_t kB2Lbo = 128, kB2Sbo = 1024;
-// TMEM columns: D1 alternates between [0, 64) and [64, 128) from chunk to
-// chunk (the token outputs of chunk n are read while chunk n + 1's first
-// product runs); D2 = Kbar^T Z at [128, 192); U at [192, 256) (kUCol).
-constexpr int kD2Col = 128;
+// mbarriers: X landed[2] and free[2], K landed[2] and free[2], H landed[3] and
+// free[3]; first product, second product, H Z product, U product[2] (by chunk
+// parity: U of the next chunk can complete before a compute thread waits for
+// this chunk's), and the first product as the off-chain warp sees it (two
+// arrivals: the product's commit and that lane's own, made once it has seen
+// the phase before, so the barrier never runs a phase ahead of the lane).
+constexpr int kP2NBar = 2 * (kXBufs + kKBufs + kHBufs) + 6;
+
+// Shared memory and TMEM of the TN-column state pass (byte offsets; operand
+// tiles 1 KiB aligned).
+template <int TN>
+struct P2L {
+    static constexpr uint32_t kVBytes = C * TN * 2;
+    static constexpr int kHBytes = (int)((kHTBytes + kVBytes + 1023) / 1024 * 1024);
+    static constexpr int kK = kXBufs * kXBytes;
+    static constexpr int kH = kK + kKBufs * kKBytes;
+    static constexpr int kB1 = kH + kHBufs * kHBytes;  // S (hi | lo) bf16, MN-major [K = ch][N = 2 TN]
+    static constexpr int kB2 = kB1 + D * 2 * TN * 2;   // [Z_hi | Z_lo] bf16, MN-major [K = token][N = 2 TN]
+    static constexpr int kBar = kB2 + C * 2 * TN * 2;
+    static constexpr int kTmem = kBar + 8 * kP2NBar;
+    static constexpr int kErr = kTmem + 4;
+    // Fused output gate (TN = 32 only, a 4-CTA cluster): three mbarriers (the
+    // partial sums of a chunk's rows from the four CTAs have arrived, one per
+    // chunk parity; the chunk's gate logits have landed), this CTA's per-row
+    // partials of its four column groups, the four CTAs' per-row partials (two
+    // chunk parities), and the gate logits of this CTA's columns for one chunk
+    // (bf16 [64 tokens][TN], a tensor-map tile: global loads would hold the
+    // output warps at their next named barrier until they return).
+    static constexpr int kRedBar = (kErr + 4 + 7) / 8 * 8;
+    static constexpr int kLoc = (kRedBar + 24 + 15) / 16 * 16;  // fp32 [4 column groups][64 rows]
+    static constexpr int kRed = kLoc + 1024;                    // fp32 [2 parities][D / TN CTAs][64 rows]
+    static constexpr int kZ = (kRed + 2 * (D / TN) * 64 * 4 + 127) / 128 * 128;
+    static constexpr uint32_t kZBytes = C * TN * 2;
+    static constexpr int kSmem = TN == 32 ? kZ + (int)kZBytes : kErr + 4;
+    // TMEM columns: D1 alternates between [0, 2 TN) and [2 TN, 4 TN) from
+    // chunk to chunk (the token outputs of chunk n are read while chunk n + 1's
+    // first product runs); D2 = Kbar^T Z at [4 TN, 6 TN); U at [6 TN, 8 TN),
+    // by chunk parity.
+    static constexpr int kD2Col = 4 * TN, kUCol = 6 * TN, kCols = 8 * TN;
+    static_assert(kB1 % 1024 == 0 && kB2 % 1024 == 0 && kHBytes % 1024 == 0, "operand tiles 1 KiB aligned");
+    static_assert(kRedBar % 8 == 0 && kRed % 16 == 0 && kZ % 128 == 0, "gate buffers misaligned");
+    static_assert(kSmem <= 232448, "phase-2 shared memory exceeds 227 KiB");
+};
+static_assert(kKBytes % 1024 == 0 && kXBytes % 1024 == 0, "operand tiles 1 KiB aligned");
+constexpr uint32_t kRedBytes = (D / kTN) * 64 * 4;  // row partials a CTA receives per chunk (TN = 32)
+constexpr int kGateCluster = D / kTN;                // CTAs of a head's state = the cluster
 
 // Which chunks a state-pass launch walks. The serial pass is one segment of
 // every chunk. The segmented pass (a chunk-level parallel prefix over the
@@ -913,14 +948,20 @@ struct SegPass {
     float *enter;  // [seq][H][P][D][D]: the state entering segment p
 };
 
-__global__ void __launch_bounds__(kP2Threads, 1)
-tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
-              const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens,
-              int T_fixed, const float *init_state, __nv_bfloat16 *__restrict__ out,
-              float *final_state, int H, int *__restrict__ status, const SegPass sp,
-              const OutGate og, const __grid_constant__ CUtensorMap tm_z,
-              const __nv_bfloat16 *__restrict__ vin) {
+// The state pass for one CTA: vblock is its index in the launch's grid order;
+// `ready` (fused prefill) holds the flags phase 1 sets once a (slot, head)
+// region is written, NULL when phase 1 has finished before the launch.
+template <int TN>
+__device__ __forceinline__ void state_pass_body(
+    const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
+    const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens, int T_fixed,
+    const float *init_state, __nv_bfloat16 *__restrict__ out, float *final_state, int H,
+    int *__restrict__ status, const SegPass sp, const OutGate og_in, const CUtensorMap *tm_z,
+    const CUtensorMap *tm_v, int vblock, const int *ready) {
+    using L = P2L<TN>;
+    constexpr int NJ = TN / 4;  // slab columns per compute thread
     extern __shared__ __align__(1024) unsigned char sm[];
+    const OutGate og = TN == kTN ? og_in : OutGate{nullptr, nullptr, 0.f};
     const bool gated = og.z != nullptr;
     // A call whose chunk table was refused (or that already failed) does
     // nothing; the decision is taken once for the whole CTA. With the fused
@@ -930,20 +971,22 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     if (refused && !gated) return;
     // 1-D grid, sequences slowest in seq_order (longest first), then heads,
     // then segments, then the column tiles of one head and segment (adjacent:
-    // they read the same tiles). A transfer launch has 2 D / kTN tiles: the
+    // they read the same tiles). A transfer launch has 2 D / TN tiles: the
     // d_v tiles, then the identity tiles.
-    constexpr int kTiles = D / kTN;
+    constexpr int kTiles = D / TN;
     const int tiles = sp.transfer ? 2 * kTiles : kTiles;
     const int per_h = sp.np * tiles, per_seq = H * per_h;
-    const int rank = (int)blockIdx.x / per_seq, rem = (int)blockIdx.x - rank * per_seq;
+    const int rank = vblock / per_seq, rem = vblock - rank * per_seq;
     const int h = rem / per_h, rem2 = rem - h * per_h;
     const int p = sp.p_lo + rem2 / tiles, jt = rem2 - (rem2 / tiles) * tiles;
     const bool ident = jt >= kTiles;
-    const int j0 = (ident ? jt - kTiles : jt) * kTN;
+    const int j0 = (ident ? jt - kTiles : jt) * TN;
     // Segment 0 of a transfer launch starts from the true initial state: it
     // needs no map, so its identity tiles have nothing to do.
     if (sp.transfer && p == 0 && ident) return;
     const bool outputs = !sp.transfer || p == 0;
+    // The H ring is read by U (not in identity tiles) and by H Z (with outputs).
+    const bool has_h = outputs || !ident;
     const int n = seq_order[rank];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int bos, len;
@@ -978,23 +1021,25 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     } else if (p == sp.P - 1 && final_state) {
         st_dst = final_state + nh * D * D;
     }
-    unsigned char *B1 = sm + kP2B1;
-    unsigned char *B2 = sm + kP2B2;
-    uint64_t *bar_xl = reinterpret_cast<uint64_t *>(sm + kP2Bar);  // [kXBufs] X tiles landed
-    uint64_t *bar_xf = bar_xl + kXBufs;                             // [kXBufs] X tiles consumed
-    uint64_t *bar_yl = bar_xf + kXBufs;                             // [kYBufs] Y tiles landed
-    uint64_t *bar_yf = bar_yl + kYBufs;                             // [kYBufs] Y tiles consumed
-    uint64_t *bar_m1 = bar_yf + kYBufs;                             // first product done
-    uint64_t *bar_m2 = bar_m1 + 1;                                  // second product done
-    uint64_t *bar_m3 = bar_m2 + 1;                                  // H Z product done
-    uint64_t *bar_u = bar_m3 + 1;                                   // [2] U product done
-    uint64_t *bar_m1s = bar_u + 2;                                  // first product, off-chain warp
-    uint64_t *red_full = reinterpret_cast<uint64_t *>(sm + kP2RedBar);  // [2] row partials arrived
-    uint64_t *z_full = red_full + 2;                                    // gate logits landed
-    float *loc = reinterpret_cast<float *>(sm + kP2Loc);
-    float *red = reinterpret_cast<float *>(sm + kP2Red);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + kP2Tmem);
-    volatile int *err = reinterpret_cast<volatile int *>(sm + kP2Err);
+    unsigned char *B1 = sm + L::kB1;
+    unsigned char *B2 = sm + L::kB2;
+    uint64_t *bar_xl = reinterpret_cast<uint64_t *>(sm + L::kBar);  // [kXBufs] X tiles landed
+    uint64_t *bar_xf = bar_xl + kXBufs;                              // [kXBufs] X tiles consumed
+    uint64_t *bar_kl = bar_xf + kXBufs;                              // [kKBufs] K tiles landed
+    uint64_t *bar_kf = bar_kl + kKBufs;                              // [kKBufs] K tiles consumed
+    uint64_t *bar_hl = bar_kf + kKBufs;                              // [kHBufs] H tiles landed
+    uint64_t *bar_hf = bar_hl + kHBufs;                              // [kHBufs] H tiles consumed
+    uint64_t *bar_m1 = bar_hf + kHBufs;                              // first product done
+    uint64_t *bar_m2 = bar_m1 + 1;                                   // second product done
+    uint64_t *bar_m3 = bar_m2 + 1;                                   // H Z product done
+    uint64_t *bar_u = bar_m3 + 1;                                    // [2] U product done
+    uint64_t *bar_m1s = bar_u + 2;                                   // first product, off-chain warp
+    uint64_t *red_full = reinterpret_cast<uint64_t *>(sm + L::kRedBar);  // [2] row partials arrived
+    uint64_t *z_full = red_full + 2;                                     // gate logits landed
+    float *loc = reinterpret_cast<float *>(sm + L::kLoc);
+    float *red = reinterpret_cast<float *>(sm + L::kRed);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + L::kTmem);
+    volatile int *err = reinterpret_cast<volatile int *>(sm + L::kErr);
     // Bounded waits. A phase that has completed returns at once; otherwise the
     // CTA's error flag is read first (a volatile shared read costs about as
     // much as a barrier test, so it stays off the path of waits that succeed
@@ -1018,35 +1063,36 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         }
     };
 
-    // Compute-thread coordinates: TMEM lane / state row r, slab columns js .. js + 7.
-    const int r = 32 * (warp & 3) + lane, js = 8 * ((warp >> 2) & 3);
+    // Compute-thread coordinates: TMEM lane / state row r, slab columns js .. js + NJ - 1.
+    const int r = 32 * (warp & 3) + lane, js = NJ * ((warp >> 2) & 3);
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    float S[8];
+    float S[NJ];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) S[j] = ident && r == j0 + js + j ? 1.f : 0.f;
-    auto put_state = [&]() {  // B1 rows js + j (hi) and 32 + js + j (lo), K-row r
-        uint4 hi, lo;
-        split8(S, hi, lo);
-        *reinterpret_cast<uint4 *>(B1 + mnmaj(js, r, kB1Lbo, kB1Sbo)) = hi;
-        *reinterpret_cast<uint4 *>(B1 + mnmaj(kTN + js, r, kB1Lbo, kB1Sbo)) = lo;
+    for (int j = 0; j < NJ; ++j) S[j] = ident && r == j0 + js + j ? 1.f : 0.f;
+    auto put_state = [&]() {  // B1 rows js + j (hi) and TN + js + j (lo), K-row r
+#pragma unroll
+        for (int q = 0; q < NJ / 8; ++q) {
+            uint4 hi, lo;
+            split8(S + 8 * q, hi, lo);
+            *reinterpret_cast<uint4 *>(B1 + mnmaj(js + 8 * q, r, kB1Lbo, kB1Sbo)) = hi;
+            *reinterpret_cast<uint4 *>(B1 + mnmaj(TN + js + 8 * q, r, kB1Lbo, kB1Sbo)) = lo;
+        }
     };
     if (warp < kP2MmaWarp) {
         if (st_src) {
             const float *src = st_src + (size_t)r * D + j0 + js;
-            const float4 t0 = *reinterpret_cast<const float4 *>(src);
-            const float4 t1 = *reinterpret_cast<const float4 *>(src + 4);
-            S[0] = t0.x; S[1] = t0.y; S[2] = t0.z; S[3] = t0.w;
-            S[4] = t1.x; S[5] = t1.y; S[6] = t1.z; S[7] = t1.w;
+#pragma unroll
+            for (int q = 0; q < NJ / 4; ++q) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(src + 4 * q);
+                S[4 * q] = t4.x; S[4 * q + 1] = t4.y; S[4 * q + 2] = t4.z; S[4 * q + 3] = t4.w;
+            }
         }
         put_state();
     }
-    if (warp == 0) tmem_alloc<256>(tslot);
+    if (warp == 0) tmem_alloc<L::kCols>(tslot);
     if (tid == 0) {
-        // Y landed: the bulk copy's arrival and one per copy-warp lane.
-        for (int i = 0; i < kP2NBar; ++i)
-            mbar_init(bar_xl + i, i >= 2 * kXBufs && i < 2 * kXBufs + kYBufs ? 33 : 1);
-        mbar_init(bar_m1s, 2);
-        // every output thread of the four CTAs arrives once per chunk
+        // One arrival each, but two for the off-chain view of the first product.
+        for (int i = 0; i < kP2NBar; ++i) mbar_init(bar_xl + i, bar_xl + i == bar_m1s ? 2 : 1);
         if (gated) {
             // Each chunk's phase: one local arrival (with the expected bytes,
             // 4 CTAs x 64 rows x 4 B) and the peers' asynchronous stores.
@@ -1067,155 +1113,94 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
     if (gated) cluster_sync();
     const uint32_t tmem = *tslot;
 
-    // Chunk ch lives in X slot ch % kXBufs and Y slot ch % kYBufs, the
-    // (ch / kXBufs)-th and (ch / kYBufs)-th use of each: its loads complete the
-    // phase of that parity of the slot's "landed" barrier, and its release
-    // the phase of the same parity of the "free" one.
-    if (warp == kP2ProdWarp) {
-        // Chunk c's copies go out as their slots free, in the order the slots
-        // free: Y (its chunk c - 3 finished) before X (the first product of
-        // chunk c - 2 finished). Lane 0 waits and issues the bulk copies; in a
-        // Y slot, lane l copies the value rows' 16-byte pieces l, l + 32, ...
-        // straight into the MN-major operand layout (tokens past the sequence
-        // read as zeros), and every lane arrives once its copies have landed.
-        int nx = 0, ny = 0;  // copies issued
-        for (int ch = 0; ch < nchunks; ++ch) {
-            bool go = true;
-            if (lane == 0) go = ch < kYBufs || wait(bar_yf + ch % kYBufs, (uint32_t)(ch / kYBufs - 1) & 1);
-            go = __shfl_sync(0xffffffffu, go, 0) != 0;
-            if (!go) break;
-            const unsigned char *rg = ws + ((size_t)(slot0 + ch) * H + h) * TcRegion::bytes;
-            {
-                unsigned char *dst = sm + kP2Y + (ch % kYBufs) * kYBytes;
-                uint64_t *bar = bar_yl + ch % kYBufs;
-                if (lane == 0) {
-                    mbar_expect_tx(bar, kYCopy);
-                    bulk_g2s(dst, rg + TcRegion::A2, kYCopy, bar);
-                }
-                if (!ident) {
-                    const int tok0 = (c0 + ch) * C;
-#pragma unroll
-                    for (int m = 0; m < 8; ++m) {
-                        const int idx = lane + 32 * m, kk = idx >> 2, gi = idx & 3;
-                        const bool in = tok0 + kk < len;
-                        const __nv_bfloat16 *src =
-                            in ? vin + ((size_t)(bos + tok0 + kk) * H + h) * D + j0 + 8 * gi : vin;
-                        cp_async16(dst + kYV + gi * kBvSbo + (kk >> 3) * kBvLbo + (kk & 7) * 16, src,
-                                   in ? 16u : 0u);
-                    }
-                }
-                cp_async_mbar_arrive(bar);
-                ny = ch + 1;
-            }
-            if (lane == 0) go = ch < kXBufs || wait(bar_xf + ch % kXBufs, (uint32_t)(ch / kXBufs - 1) & 1);
-            go = __shfl_sync(0xffffffffu, go, 0) != 0;
-            if (!go) break;
-            if (lane == 0) {
-                uint64_t *bar = bar_xl + ch % kXBufs;
-                mbar_expect_tx(bar, (uint32_t)kXBytes);
-                bulk_g2s(sm + (ch % kXBufs) * kXBytes, rg, (uint32_t)kXBytes, bar);
-            }
-            nx = ch + 1;
-        }
-        // Every copy lands before the CTA exits (bounded; a slot's last use
-        // is the newest phase of its barrier).
-        cp_async_wait_all();
+    // Chunk ch lives in slot ch % kXBufs of X (and likewise K, H) and is that
+    // slot's (ch / kXBufs)-th use: its copies complete the phase of parity
+    // (ch / kXBufs) & 1 of the slot's "landed" barrier, and its release the
+    // phase of the same parity of the "free" one.
+    if (warp == kP2CopyWarp) {
         if (lane == 0) {
+            // Chunk c's copies go out as their slots free, in the order the
+            // slots free: H (chunk c - 3's last product), X (chunk c - 2's
+            // first), K (chunk c - 2's second). In the fused prefill the
+            // chunk's region is waited for first.
+            int nx = 0, nk = 0, nhh = 0;  // copies issued per ring
+            for (int ch = 0; ch < nchunks; ++ch) {
+                const size_t slot = (size_t)(slot0 + ch);
+                if (ready) {
+                    const int *f = ready + slot * H + h;
+                    bool got = false;
+                    for (uint32_t it = 0; it < (1u << 22); ++it) {
+                        if (ld_acquire_gpu(f) != 0) {
+                            got = true;
+                            break;
+                        }
+                        if ((it & 63) == 63 && (*err || *reinterpret_cast<volatile int *>(status) != 0))
+                            break;
+                        __nanosleep(256);
+                    }
+                    if (!got) {
+                        *err = 1;
+                        atomicCAS(status, 0, (int)KDA_ERR_TIMEOUT);
+                        break;
+                    }
+                    fence_async_global();
+                }
+                const unsigned char *rg = ws + (slot * H + h) * TcRegion::bytes;
+                if (has_h) {
+                    if (ch >= kHBufs && !wait(bar_hf + ch % kHBufs, (uint32_t)(ch / kHBufs - 1) & 1)) break;
+                    unsigned char *dst = sm + L::kH + (ch % kHBufs) * L::kHBytes;
+                    uint64_t *bar = bar_hl + ch % kHBufs;
+                    mbar_expect_tx(bar, kHTBytes + (ident ? 0u : L::kVBytes));
+                    bulk_g2s(dst, rg + TcRegion::HT, kHTBytes, bar);
+                    if (!ident) tma_load_3d(dst + kHTBytes, tm_v, 0, bos + (c0 + ch) * C, (h * D + j0) / 8, bar);
+                    nhh = ch + 1;
+                }
+                if (ch >= kXBufs && !wait(bar_xf + ch % kXBufs, (uint32_t)(ch / kXBufs - 1) & 1)) break;
+                mbar_expect_tx(bar_xl + ch % kXBufs, (uint32_t)kXBytes);
+                bulk_g2s(sm + (ch % kXBufs) * kXBytes, rg, (uint32_t)kXBytes, bar_xl + ch % kXBufs);
+                nx = ch + 1;
+                if (ch >= kKBufs && !wait(bar_kf + ch % kKBufs, (uint32_t)(ch / kKBufs - 1) & 1)) break;
+                mbar_expect_tx(bar_kl + ch % kKBufs, kKCopy);
+                bulk_g2s(sm + L::kK + (ch % kKBufs) * kKBytes, rg + TcRegion::A2, kKCopy, bar_kl + ch % kKBufs);
+                nk = ch + 1;
+            }
+            // Every copy lands before the CTA exits (bounded; a slot's last
+            // use is the newest phase of its barrier).
             for (int cc = nx > kXBufs ? nx - kXBufs : 0; cc < nx; ++cc)
                 mbar_wait(bar_xl + cc % kXBufs, (uint32_t)(cc / kXBufs) & 1);
-            for (int cc = ny > kYBufs ? ny - kYBufs : 0; cc < ny; ++cc)
-                mbar_wait(bar_yl + cc % kYBufs, (uint32_t)(cc / kYBufs) & 1);
-        }
-        __syncwarp();
-    } else if (warp == kP2MmaWarp) {
-        // One lane issues; the whole warp keeps the named-barrier protocol, so
-        // the compute warps never wait on a barrier that cannot complete.
-        // Descriptors of slot 0's tiles and of the state-side operands are
-        // built once; a chunk adds its slot's offset and a K step a constant
-        // (the address field is the byte address / 16).
-        const uint64_t d_a1 = desc(smem_u32(sm), kA1Lbo, kA1Sbo);
-        const uint64_t d_a2 = desc(smem_u32(sm + kP2Y + kYA2), kA2Lbo, kA2Sbo);
-        const uint64_t d_b1 = desc(smem_u32(B1), kB1Lbo, kB1Sbo);
-        const uint64_t d_b2 = desc(smem_u32(B2), kB2Lbo, kB2Sbo);
-        const uint32_t id1 = idesc_bf16(128, 2 * kTN, 1, 1), id2 = idesc_bf16(128, 2 * kTN, 0, 1);
-        bool ok = true;  // lane 0: every wait so far succeeded
-        for (int ch = 0; ch < nchunks; ++ch) {
-            const uint64_t xo = (uint64_t)(ch % kXBufs) * (kXBytes >> 4);
-            const uint64_t yo = (uint64_t)(ch % kYBufs) * (kYBytes >> 4);
-            const uint32_t d1 = tmem + 64 * (ch & 1);
-            if (lane == 0) {
-                // Chunk 0's tiles; a later chunk's were waited for before the
-                // state barrier (off the chain of dependent steps).
-                if (ch == 0) ok = ok && wait(bar_xl, 0);
-                if (ok) {
-                    // [s Qbar S; W S] with S = S_hi + S_lo: N = 64 (hi columns 0-31, lo 32-63).
-                    fence_after();
-#pragma unroll
-                    for (int s = 0; s < D / 16; ++s)
-                        mma_bf16(d1, d_a1 + xo + s * (2 * kA1Lbo >> 4), d_b1 + s * (2 * kB1Lbo >> 4),
-                                 id1, s > 0);
-                    commit(bar_m1);
-                    commit(bar_m1s);
-                }
-                // The X slot is free once everything issued so far has completed.
-                commit(bar_xf + ch % kXBufs);
-                // The second product reads the Y tiles (landed long ago: U of
-                // this chunk was formed from them).
-                ok = ok && wait(bar_yl + ch % kYBufs, (uint32_t)(ch / kYBufs) & 1);
-            }
-            __syncwarp();
-            bar_sync(kBarZ, kP2Sync);  // Z of this chunk is in B2
-            fence_after();
-            if (lane == 0) {
-                if (ok) {
-                    // D2 = Kbar^T [Z_hi | Z_lo] (N = 64).
-#pragma unroll
-                    for (int s = 0; s < C / 16; ++s)
-                        mma_bf16(tmem + kD2Col, d_a2 + yo + s * (2 * kA2Lbo >> 4),
-                                 d_b2 + s * (2 * kB2Lbo >> 4), id2, s > 0);
-                    commit(bar_m2);
-                }
-                // Without outputs this is the Y slot's last reader; with them
-                // the other issuing warp releases it after H Z.
-                if (!outputs) commit(bar_yf + ch % kYBufs);
-                if (ch + 1 < nchunks)
-                    ok = ok && wait(bar_xl + (ch + 1) % kXBufs, (uint32_t)((ch + 1) / kXBufs) & 1);
-            }
-            __syncwarp();
-            bar_sync(kBarS, kP2Sync);  // the new state is in B1
-            fence_after();
+            for (int cc = nk > kKBufs ? nk - kKBufs : 0; cc < nk; ++cc)
+                mbar_wait(bar_kl + cc % kKBufs, (uint32_t)(cc / kKBufs) & 1);
+            for (int cc = nhh > kHBufs ? nhh - kHBufs : 0; cc < nhh; ++cc)
+                mbar_wait(bar_hl + cc % kHBufs, (uint32_t)(cc / kHBufs) & 1);
         }
         __syncwarp();
     } else if (warp == kP2SideWarp) {
-        // U of chunk ch + 1 = [H; T B] times its value rows (rows 64-127 of the
-        // product; the H rows give nothing used), into TMEM columns by chunk
-        // parity, once chunk ch's first product has completed (the pipe runs it
-        // while the compute warps form Z); chunk 0's first. Then, with
-        // outputs, D1 += [H; T B] [Z_hi | Z_lo] once the second product has
-        // completed, which adds H Z to the s Qbar S rows 0-63 (rows 64-127
-        // take (T B) Z; W S there is consumed). The value rows were written by
-        // cp.async (generic proxy): a proxy fence after the landed barrier's
-        // wait hands them to the tensor core.
-        // Phases stay in step: the first product's barrier here completes a
-        // phase only with this warp's arrival; chunk ch + 1's second product
-        // needs the outputs of chunk ch read, hence H Z of chunk ch issued
-        // after this warp saw chunk ch's second product.
-        if (lane == 0 && (outputs || !ident)) {
-            const uint64_t d_ht = desc(smem_u32(sm + kP2Y + kYHT), kA2Lbo, kA2Sbo);
-            const uint64_t d_v = desc(smem_u32(sm + kP2Y + kYV), kBvLbo, kBvSbo);
+        if (lane == 0 && has_h) {
+            // U of chunk ch + 1 = [H; T B] times its value rows (rows 64-127 of
+            // the product; the H rows give nothing used), into TMEM columns by
+            // chunk parity, once chunk ch's first product has completed (the
+            // pipe runs it while the compute warps form Z); chunk 0's first.
+            // Then, with outputs, D1 += [H; T B] [Z_hi | Z_lo] once the second
+            // product has completed, which adds H Z to the s Qbar S rows 0-63
+            // (rows 64-127 take (T B) Z; W S there is consumed).
+            // Phases stay in step: the first product's barrier here completes
+            // a phase only with this warp's arrival; chunk ch + 1's second
+            // product needs the outputs of chunk ch read, hence H Z of chunk ch
+            // issued after this warp saw chunk ch's second product.
+            const uint64_t d_ht = desc(smem_u32(sm + L::kH), kA2Lbo, kA2Sbo);
+            const uint64_t d_v = desc(smem_u32(sm + L::kH + kHTBytes), kBvLbo, kBvSbo);
             const uint64_t d_b2 = desc(smem_u32(B2), kB2Lbo, kB2Sbo);
-            const uint32_t id2 = idesc_bf16(128, 2 * kTN, 0, 1), idu = idesc_bf16(128, kTN, 0, 1);
+            const uint32_t id2 = idesc_bf16(128, 2 * TN, 0, 1), idu = idesc_bf16(128, TN, 0, 1);
             bool ok = true;
             auto issue_u = [&](int ch) {
-                ok = ok && wait(bar_yl + ch % kYBufs, (uint32_t)(ch / kYBufs) & 1);
+                ok = ok && wait(bar_hl + ch % kHBufs, (uint32_t)(ch / kHBufs) & 1);
                 if (!ok) return;
-                const uint64_t yo = (uint64_t)(ch % kYBufs) * (kYBytes >> 4);
-                fence_async_smem();
+                const uint64_t ho = (uint64_t)(ch % kHBufs) * (L::kHBytes >> 4);
                 fence_after();
 #pragma unroll
                 for (int s = 0; s < C / 16; ++s)
-                    mma_bf16(tmem + kUCol + kTN * (ch & 1), d_ht + yo + s * (2 * kA2Lbo >> 4),
-                             d_v + yo + s * (2 * kBvLbo >> 4), idu, s > 0);
+                    mma_bf16(tmem + L::kUCol + TN * (ch & 1), d_ht + ho + s * (2 * kA2Lbo >> 4),
+                             d_v + ho + s * (2 * kBvLbo >> 4), idu, s > 0);
                 commit(bar_u + (ch & 1));
             };
             if (!ident && nchunks > 0) issue_u(0);
@@ -1230,15 +1215,73 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                     spin(bar_m2, (uint32_t)ch & 1);
                     if (*err) break;
                     fence_after();
-                    const uint64_t yo = (uint64_t)(ch % kYBufs) * (kYBytes >> 4);
+                    const uint64_t ho = (uint64_t)(ch % kHBufs) * (L::kHBytes >> 4);
 #pragma unroll
                     for (int s = 0; s < C / 16; ++s)
-                        mma_bf16(tmem + 64 * (ch & 1), d_ht + yo + s * (2 * kA2Lbo >> 4),
+                        mma_bf16(tmem + 2 * TN * (ch & 1), d_ht + ho + s * (2 * kA2Lbo >> 4),
                                  d_b2 + s * (2 * kB2Lbo >> 4), id2, 1);
                     commit(bar_m3);
-                    commit(bar_yf + ch % kYBufs);
                 }
+                // Everything this warp issued on chunk ch's H slot (its U, and
+                // H Z) precedes this commit.
+                commit(bar_hf + ch % kHBufs);
             }
+        }
+        __syncwarp();
+    } else if (warp == kP2MmaWarp) {
+        // One lane issues; the whole warp keeps the named-barrier protocol, so
+        // the compute warps never wait on a barrier that cannot complete.
+        // Descriptors of slot 0's tiles and of the state-side operands are
+        // built once; a chunk adds its slot's offset and a K step a constant
+        // (the address field is the byte address / 16).
+        const uint64_t d_a1 = desc(smem_u32(sm), kA1Lbo, kA1Sbo);
+        const uint64_t d_a2 = desc(smem_u32(sm + L::kK), kA2Lbo, kA2Sbo);
+        const uint64_t d_b1 = desc(smem_u32(B1), kB1Lbo, kB1Sbo);
+        const uint64_t d_b2 = desc(smem_u32(B2), kB2Lbo, kB2Sbo);
+        const uint32_t id1 = idesc_bf16(128, 2 * TN, 1, 1), id2 = idesc_bf16(128, 2 * TN, 0, 1);
+        bool ok = true;  // lane 0: every wait so far succeeded
+        for (int ch = 0; ch < nchunks; ++ch) {
+            const uint64_t xo = (uint64_t)(ch % kXBufs) * (kXBytes >> 4);
+            const uint64_t ko = (uint64_t)(ch % kKBufs) * (kKBytes >> 4);
+            const uint32_t d1 = tmem + 2 * TN * (ch & 1);
+            if (lane == 0) {
+                // Chunk 0's tiles; a later chunk's were waited for before the
+                // state barrier (off the chain of dependent steps).
+                if (ch == 0) ok = ok && wait(bar_xl, 0);
+                if (ok) {
+                    // [s Qbar S; W S] with S = S_hi + S_lo: N = 2 TN (hi columns first).
+                    fence_after();
+#pragma unroll
+                    for (int s = 0; s < D / 16; ++s)
+                        mma_bf16(d1, d_a1 + xo + s * (2 * kA1Lbo >> 4), d_b1 + s * (2 * kB1Lbo >> 4),
+                                 id1, s > 0);
+                    commit(bar_m1);
+                    commit(bar_m1s);
+                }
+                // The X slot is free once everything issued so far has completed.
+                commit(bar_xf + ch % kXBufs);
+                // The second product reads the K tiles.
+                ok = ok && wait(bar_kl + ch % kKBufs, (uint32_t)(ch / kKBufs) & 1);
+            }
+            __syncwarp();
+            bar_sync(kBarZ, kP2Sync);  // Z of this chunk is in B2
+            fence_after();
+            if (lane == 0) {
+                if (ok) {
+                    // D2 = Kbar^T [Z_hi | Z_lo] (N = 2 TN).
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        mma_bf16(tmem + L::kD2Col, d_a2 + ko + s * (2 * kA2Lbo >> 4),
+                                 d_b2 + s * (2 * kB2Lbo >> 4), id2, s > 0);
+                    commit(bar_m2);
+                }
+                commit(bar_kf + ch % kKBufs);
+                if (ch + 1 < nchunks)
+                    ok = ok && wait(bar_xl + (ch + 1) % kXBufs, (uint32_t)((ch + 1) / kXBufs) & 1);
+            }
+            __syncwarp();
+            bar_sync(kBarS, kP2Sync);  // the new state is in B1
+            fence_after();
         }
         __syncwarp();
     } else {
@@ -1250,17 +1293,18 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         for (int j = 0; j < 8; ++j) wv[j] = gated && og.w ? og.w[j0 + js + j] : 1.f;
         const uint32_t crank = gated ? cluster_rank() : 0u;
         // Token outputs of chunk `ch` (rows 0-63 of its D1): s Qbar S + H Z,
-        // or with the fused gate w o / rms(o) sigmoid(z), the mean of squares
-        // over all D columns: this CTA's 32 are summed through shared memory,
-        // then every CTA of the cluster sends its row sums to all four.
-        // The gate logits of chunk ch: one tensor-map tile (32 columns x 64
+        // or with the fused gate (TN = 32: eight columns a thread) w o / rms(o)
+        // sigmoid(z), the mean of squares over all D columns: this CTA's 32
+        // are summed through shared memory, then every CTA of the cluster
+        // sends its row sums to all four.
+        // The gate logits of chunk ch: one tensor-map tile (TN columns x 64
         // tokens) into the slot, issued by thread 0 once every output thread
         // has read the previous chunk's.
-        const __nv_bfloat16 *zslot = reinterpret_cast<const __nv_bfloat16 *>(sm + kP2Z);
+        const __nv_bfloat16 *zslot = reinterpret_cast<const __nv_bfloat16 *>(sm + L::kZ);
         auto issue_z = [&](int ch) {
             if (tid != 0 || ch >= nchunks) return;
-            mbar_expect_tx(z_full, kZBytes);
-            tma_load_3d(sm + kP2Z, &tm_z, j0, h, bos + (c0 + ch) * C, z_full);
+            mbar_expect_tx(z_full, L::kZBytes);
+            tma_load_3d(sm + L::kZ, tm_z, j0, h, bos + (c0 + ch) * C, z_full);
         };
         uint32_t zph = 0;
         int z_issued = 0;  // tiles issued (tid 0)
@@ -1276,56 +1320,63 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         float o8[8];
         uint4 zr = make_uint4(0u, 0u, 0u, 0u);
         auto put_outputs_a = [&](int ch) {  // ch counts this segment's chunks
-            const uint32_t d1 = tmem + lane_base + 64 * (ch & 1);
-            if (gated) {
-                if (!mbar_test(z_full, zph) && !*err && !mbar_wait(z_full, zph)) {
-                    *err = 1;
-                    atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            const uint32_t d1 = tmem + lane_base + 2 * TN * (ch & 1);
+            if (!gated) {
+                const int clen = min(C, len - (c0 + ch) * C);
+#pragma unroll
+                for (int q = 0; q < NJ / 8; ++q) {
+                    float hi[8], lo[8], o[8];
+                    tmem_ld8(d1 + js + 8 * q, hi);
+                    tmem_ld8(d1 + TN + js + 8 * q, lo);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) o[j] = hi[j] + lo[j];
+                    if (r < clen)
+                        *reinterpret_cast<uint4 *>(out + ((size_t)(bos + (c0 + ch) * C + r) * H + h) * D +
+                                                   j0 + js + 8 * q) = pack8(o);
                 }
-                zph ^= 1;
-                zr = *reinterpret_cast<const uint4 *>(zslot + r * kTN + js);
+                return;
             }
+            if (!mbar_test(z_full, zph) && !*err && !mbar_wait(z_full, zph)) {
+                *err = 1;
+                atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            }
+            zph ^= 1;
+            zr = *reinterpret_cast<const uint4 *>(zslot + r * TN + js);
             float hi[8], lo[8];
             tmem_ld8(d1 + js, hi);
-            tmem_ld8(d1 + kTN + js, lo);
+            tmem_ld8(d1 + TN + js, lo);
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 8; ++j) o8[j] = hi[j] + lo[j];
-            if (!gated) {
-                const int clen = min(C, len - (c0 + ch) * C);
-                if (r < clen)
-                    *reinterpret_cast<uint4 *>(out + ((size_t)(bos + (c0 + ch) * C + r) * H + h) * D + j0 + js) =
-                        pack8(o8);
-            } else {
-                const int par = ch & 1;
-                float ss = 0.f;
+            const int par = ch & 1;
+            float ss = 0.f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) ss += o8[j] * o8[j];
-                loc[(js >> 3) * 64 + r] = ss;
-                // Every output thread has read its z (the slot is free) and has
-                // finished the previous chunk, whose row sums it read: that
-                // barrier's next phase (chunk ch + 1) may now expect its bytes,
-                // before this CTA sends anything a peer could answer with them.
-                bar_sync(kBarO, 256);
-                if (ch + 1 < nchunks) {
-                    issue_z(ch + 1);
-                    z_issued = ch + 2;
+            for (int j = 0; j < 8; ++j) ss += o8[j] * o8[j];
+            loc[(js >> 3) * 64 + r] = ss;
+            // Every output thread has read its z (the slot is free) and has
+            // finished the previous chunk, whose row sums it read: that
+            // barrier's next phase (chunk ch + 1) may now expect its bytes,
+            // before this CTA sends anything a peer could answer with them.
+            bar_sync(kBarO, 256);
+            if (ch + 1 < nchunks) {
+                issue_z(ch + 1);
+                z_issued = ch + 2;
+            }
+            if (tid == 0 && ch >= 1 && ch + 1 < nchunks) mbar_expect_tx(red_full + (par ^ 1), kRedBytes);
+            if (tid < 16) {
+                // Rows 4 tid .. 4 tid + 3: this CTA's sums, 16 bytes to each CTA.
+                float4 pr;
+                float *pp = reinterpret_cast<float *>(&pr);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = 4 * tid + i;
+                    pp[i] = loc[row] + loc[64 + row] + loc[128 + row] + loc[192 + row];
                 }
-                if (tid == 0 && ch >= 1 && ch + 1 < nchunks) mbar_expect_tx(red_full + (par ^ 1), kRedBytes);
-                if (tid < 16) {
-                    // Rows 4 tid .. 4 tid + 3: this CTA's sums, 16 bytes to each CTA.
-                    float4 pr;
-                    float *pp = reinterpret_cast<float *>(&pr);
+                float *slot = red + (par * kGateCluster + (int)crank) * 64 + 4 * tid;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int row = 4 * tid + i;
-                        pp[i] = loc[row] + loc[64 + row] + loc[128 + row] + loc[192 + row];
-                    }
-                    float *slot = red + (par * kGateCluster + (int)crank) * 64 + 4 * tid;
-#pragma unroll
-                    for (uint32_t dst = 0; dst < (uint32_t)kGateCluster; ++dst)
-                        st_async_cluster_v4(cluster_addr(slot, dst), pr, cluster_addr(red_full + par, dst));
-                }
+                for (uint32_t dst = 0; dst < (uint32_t)kGateCluster; ++dst)
+                    st_async_cluster_v4(cluster_addr(slot, dst), pr, cluster_addr(red_full + par, dst));
             }
         };
         auto put_outputs_b = [&](int ch) {
@@ -1358,18 +1409,33 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             if (r < clen) *reinterpret_cast<uint4 *>(out + orow) = pack8(o8);
         };
         for (int ch = 0; ch < nchunks; ++ch) {
-            const uint32_t d1 = tmem + 64 * (ch & 1);
-            // The Y tiles landed before this chunk's U was formed; this
-            // thread's own wait makes the copied decay visible to it.
-            wait(bar_yl + ch % kYBufs, (uint32_t)(ch / kYBufs) & 1);
-            const float gam =
-                reinterpret_cast<const float *>(sm + kP2Y + (ch % kYBufs) * kYBytes + kYGam)[r];
+            const uint32_t d1 = tmem + 2 * TN * (ch & 1);
+            // The K tiles landed before this chunk's second product was
+            // issued; this thread's own wait makes the copied decay visible.
+            wait(bar_kl + ch % kKBufs, (uint32_t)(ch / kKBufs) & 1);
+            const float gam = reinterpret_cast<const float *>(sm + L::kK + (ch % kKBufs) * kKBytes + kKGam)[r];
+            if (zrow && outputs && ch > 0) {
+                // The previous chunk's H Z product reads B2, which this chunk's
+                // Z overwrites (it is issued by another thread than the first
+                // product, whose completion therefore does not imply its own).
+                wait(bar_m3, p3);
+                p3 ^= 1;
+            }
             // This chunk's U row (formed while the previous state was updated).
-            float uv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float uv[NJ];
+#pragma unroll
+            for (int j = 0; j < NJ; ++j) uv[j] = 0.f;
             if (zrow && !ident) {
                 spin(bar_u + (ch & 1), (uint32_t)(ch >> 1) & 1);
                 fence_after();
-                tmem_ld8(tmem + lane_base + kUCol + kTN * (ch & 1) + js, uv);
+#pragma unroll
+                for (int q = 0; q < NJ / 8; ++q) {
+                    float u8[8];
+                    tmem_ld8(tmem + lane_base + L::kUCol + TN * (ch & 1) + js + 8 * q, u8);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) uv[8 * q + j] = u8[j];
+                }
             }
             if (!zrow && outputs && ch > 0) {
                 // The previous chunk's outputs, complete once its H Z product is:
@@ -1379,30 +1445,25 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                 fence_after();
                 put_outputs_a(ch - 1);
             }
-            if (zrow && outputs && ch > 0) {
-                // The previous chunk's H Z product reads B2, which this chunk's
-                // Z overwrites (it is issued by another thread than the first
-                // product, whose completion therefore does not imply its own).
-                wait(bar_m3, p3);
-                p3 ^= 1;
-            }
             spin(bar_m1, p1);
             p1 ^= 1;
             fence_after();
             if (zrow) {
-                // Z = U - W S for token row i, slab columns js .. js + 7.
+                // Z = U - W S for token row i, slab columns js .. js + NJ - 1.
                 const int i = r - 64;
-                float hi[8], lo[8];
-                tmem_ld8(d1 + lane_base + js, hi);
-                tmem_ld8(d1 + lane_base + kTN + js, lo);
-                tmem_wait_ld();
-                float z[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) z[j] = uv[j] - (hi[j] + lo[j]);
-                uint4 zh, zl;
-                split8(z, zh, zl);
-                *reinterpret_cast<uint4 *>(B2 + mnmaj(js, i, kB2Lbo, kB2Sbo)) = zh;
-                *reinterpret_cast<uint4 *>(B2 + mnmaj(kTN + js, i, kB2Lbo, kB2Sbo)) = zl;
+                for (int q = 0; q < NJ / 8; ++q) {
+                    float hi[8], lo[8], z[8];
+                    tmem_ld8(d1 + lane_base + js + 8 * q, hi);
+                    tmem_ld8(d1 + lane_base + TN + js + 8 * q, lo);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) z[j] = uv[8 * q + j] - (hi[j] + lo[j]);
+                    uint4 zh, zl;
+                    split8(z, zh, zl);
+                    *reinterpret_cast<uint4 *>(B2 + mnmaj(js + 8 * q, i, kB2Lbo, kB2Sbo)) = zh;
+                    *reinterpret_cast<uint4 *>(B2 + mnmaj(TN + js + 8 * q, i, kB2Lbo, kB2Sbo)) = zl;
+                }
             }
             fence_async_smem();
             fence_before();
@@ -1411,15 +1472,16 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
             spin(bar_m2, p2);
             p2 ^= 1;
             fence_after();
-            {
+#pragma unroll
+            for (int q = 0; q < NJ / 8; ++q) {
                 float hi[8], lo[8];
-                tmem_ld8(tmem + lane_base + kD2Col + js, hi);
-                tmem_ld8(tmem + lane_base + kD2Col + kTN + js, lo);
+                tmem_ld8(tmem + lane_base + L::kD2Col + js + 8 * q, hi);
+                tmem_ld8(tmem + lane_base + L::kD2Col + TN + js + 8 * q, lo);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) S[j] = gam * S[j] + (hi[j] + lo[j]);
-                put_state();
+                for (int j = 0; j < 8; ++j) S[8 * q + j] = gam * S[8 * q + j] + (hi[j] + lo[j]);
             }
+            put_state();
             fence_async_smem();
             fence_before();
             // A full barrier here (an arrive would do on the normal path, where
@@ -1439,15 +1501,55 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
         if (gated && tid == 0 && z_issued > 0) mbar_wait(z_full, (uint32_t)(z_issued - 1) & 1u);
         if (st_dst && !refused && !*err) {
             float *dst = st_dst + (size_t)r * dst_row + j0 + js;
-            *reinterpret_cast<float4 *>(dst) = make_float4(S[0], S[1], S[2], S[3]);
-            *reinterpret_cast<float4 *>(dst + 4) = make_float4(S[4], S[5], S[6], S[7]);
+#pragma unroll
+            for (int q = 0; q < NJ / 4; ++q)
+                *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
         }
     }
     fence_before();
     __syncthreads();
     // No CTA leaves while a peer may still write into its shared memory.
     if (gated) cluster_sync();
-    if (warp == 0) tmem_dealloc<256>(tmem);
+    if (warp == 0) tmem_dealloc<L::kCols>(tmem);
+}
+
+__global__ void __launch_bounds__(kP2Threads, 1)
+tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
+              const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens,
+              int T_fixed, const float *init_state, __nv_bfloat16 *__restrict__ out,
+              float *final_state, int H, int *__restrict__ status, const SegPass sp,
+              const OutGate og, const __grid_constant__ CUtensorMap tm_z,
+              const __grid_constant__ CUtensorMap tm_v) {
+    state_pass_body<kTN>(ws, seq_first_slot, seq_order, cu_seqlens, T_fixed, init_state, out,
+                         final_state, H, status, sp, og, &tm_z, &tm_v, (int)blockIdx.x, nullptr);
+}
+
+// The fused prefill: one cooperative launch whose first n_state CTAs run the
+// state pass with 64-column slabs while the rest run phase 1, chunk-major,
+// handing each (slot, head) region over through its ready flag. Phase 1
+// never waits for the state pass, and the launch is cooperative (all CTAs
+// resident at once), so every flag a state-pass CTA waits for gets set.
+template <int kVar>
+__global__ void __launch_bounds__(kP2Threads, 1)
+tc_prefill_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
+                 const float *__restrict__ g_head, Prologue pro, const float *__restrict__ beta,
+                 float scale, const ChunkEntry *__restrict__ table, const int *__restrict__ used_slots,
+                 long long nslots, int H, unsigned char *__restrict__ ws, int *__restrict__ status,
+                 const int *__restrict__ seq_first_slot, const int *__restrict__ seq_order,
+                 const int32_t *__restrict__ cu_seqlens, int T_fixed, const float *init_state,
+                 __nv_bfloat16 *__restrict__ out, float *final_state, int n_state, int *ready, int ilv,
+                 int nch) {
+    if ((int)blockIdx.x < n_state) {
+        const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
+        state_pass_body<64>(ws, seq_first_slot, seq_order, cu_seqlens, T_fixed, init_state, out,
+                            final_state, H, status, sp, OutGate{nullptr, nullptr, 0.f}, &tm_v, &tm_v,
+                            (int)blockIdx.x, ready);
+    } else if (threadIdx.x < kP1Threads) {
+        intra_chunk_body<kVar>(&tm_q, &tm_k, &tm_g, g_head, pro, beta, scale, table, used_slots, nslots,
+                               H, ws, status,
+                               P1Walk{(int)blockIdx.x - n_state, (int)gridDim.x - n_state, ready, ilv, nch});
+    }
 }
 
 // Composition of the segment maps, in order: enter[p + 1] = M_p enter[p] + E_p
@@ -1509,7 +1611,9 @@ seg_combine(const float *__restrict__ xfer, float *__restrict__ enter, int P) {
 
 }  // namespace
 
-size_t tc_region_bytes() { return TcRegion::bytes; }
+// Workspace bytes per (slot, head): its region and, after all regions, its
+// ready flag (the fused prefill's hand-over from phase 1 to the state pass).
+size_t tc_region_bytes() { return TcRegion::bytes + sizeof(int); }
 
 namespace {
 
@@ -1565,6 +1669,40 @@ cudaError_t gate_rows_map(CUtensorMap *m, const void *base, int H, long long tok
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The value rows [tokens][H][128] bf16 seen as 3-D (8 channels, token, group
+// of 8 channels across the heads) with boxes of 8 channels x 64 tokens x
+// tn / 8 groups: a box lands as [group][token][8 channels], the MN-major
+// operand layout (K = token, N = channel) with 128-byte K steps and 1 KiB
+// channel-group strides. Tokens past the tensor read as zeros.
+cudaError_t value_rows_map(CUtensorMap *m, const void *base, int H, long long tokens, int tn) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {8u, (cuuint64_t)tokens, (cuuint64_t)H * D / 8};
+    const cuuint64_t strides[2] = {(cuuint64_t)H * D * 2, 16u};
+    const cuuint32_t box[3] = {8u, (cuuint32_t)C, (cuuint32_t)(tn / 8)};
+    const cuuint32_t unit[3] = {1u, 1u, 1u};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                           strides, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Whether the fused single launch is expected to beat the two launches, from
+// a cost model of the measured rates on this part: phase 1 about 12.2k
+// cycles per (chunk, head) item and SM; the state pass about 3.1k cycles per
+// chunk with 32-column slabs and 3.7k with 64-column ones. Two launches take
+// phase 1 on every SM, then the chain; the fused one runs phase 1 on the SMs
+// the 64-column state pass leaves and the chain beside it.
+bool fuse_pays(long long items, int chain_chunks, long long n_state, int sm_count) {
+    if (n_state < 1 || n_state > sm_count - 8) return false;
+    const double p1_all = 12.2 * (double)items / (double)(items < sm_count ? items : sm_count);
+    const double p1_rest = 12.2 * (double)items / (double)(sm_count - n_state);
+    const double two = p1_all + 3.1 * chain_chunks;
+    const double fused = (p1_rest > 3.7 * chain_chunks ? p1_rest : 3.7 * chain_chunks) + 12.2;
+    return fused < 0.95 * two;
+}
+
 // Segments of the state pass for the `segments` option (0: automatic, 1: the
 // serial chain, k: k segments), at most seg_max (the workspace's bound) and
 // one per chunk. Automatic: as many as keep the transfer launch within one
@@ -1592,64 +1730,130 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const ChunkEntry *table, const int *seq_first_slot,
                               unsigned char *region, int *status, const Prologue &pro,
                               int segments, int seg_max, float *seg_ws, const GateParams &gate,
-                              cudaStream_t stream, cudaEvent_t *events) {
-    // Per device, once: the SM count (phase 1 runs one persistent CTA per SM)
-    // and the dynamic shared-memory opt-ins. Repeating this is idempotent.
+                              int fused, cudaStream_t stream, cudaEvent_t *events) {
+    // Per device, once: the SM count (phase 1 runs one persistent CTA per SM),
+    // the dynamic shared-memory opt-ins and cooperative-launch support.
+    // Repeating this is idempotent.
     static int sm_counts[64];
+    static bool coop_ok[64];
+    constexpr int kFusedSmem = P1::bytes > P2L<64>::kSmem ? P1::bytes : P2L<64>::kSmem;
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (sm_counts[dev] == 0) {
-        int n = 0;
-        if ((err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        int n = 0, coop = 0;
+        if ((err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (err = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
             return err;
-        if ((err = cudaFuncSetAttribute(tc_intra_chunk<kVarChannel>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
-                cudaSuccess ||
-            (err = cudaFuncSetAttribute(tc_intra_chunk<kVarRuntime>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
-                cudaSuccess ||
-            (err = cudaFuncSetAttribute(tc_intra_chunk<kVarScalar>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
-                cudaSuccess ||
-            (err = cudaFuncSetAttribute(tc_intra_chunk<kVarNone>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
-                cudaSuccess ||
-            (err = cudaFuncSetAttribute(tc_intra_chunk<kVarGated>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P1::bytes)) !=
-                cudaSuccess)
-            return err;
-        if ((err = cudaFuncSetAttribute(tc_state_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kP2Smem)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(seg_combine, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kCombSmem)) != cudaSuccess)
-            return err;
+#define KDA_SMEM(F, B)                                                                             \
+    if ((err = cudaFuncSetAttribute(F, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(B))) != \
+        cudaSuccess)                                                                               \
+        return err;
+        KDA_SMEM(tc_intra_chunk<kVarChannel>, P1::bytes)
+        KDA_SMEM(tc_intra_chunk<kVarRuntime>, P1::bytes)
+        KDA_SMEM(tc_intra_chunk<kVarScalar>, P1::bytes)
+        KDA_SMEM(tc_intra_chunk<kVarNone>, P1::bytes)
+        KDA_SMEM(tc_intra_chunk<kVarGated>, P1::bytes)
+        KDA_SMEM(tc_prefill_fused<kVarChannel>, kFusedSmem)
+        KDA_SMEM(tc_prefill_fused<kVarRuntime>, kFusedSmem)
+        KDA_SMEM(tc_prefill_fused<kVarScalar>, kFusedSmem)
+        KDA_SMEM(tc_prefill_fused<kVarNone>, kFusedSmem)
+        KDA_SMEM(tc_prefill_fused<kVarGated>, kFusedSmem)
+        KDA_SMEM(tc_state_pass, P2L<kTN>::kSmem)
+        KDA_SMEM(seg_combine, kCombSmem)
+#undef KDA_SMEM
+        coop_ok[dev] = coop != 0;
         sm_counts[dev] = n;
     }
     const int sm_count = sm_counts[dev];
+    const int *used = seq_first_slot + num_seqs;
+    const int *order = seq_first_slot + num_seqs + 1;
+    const int nch = (T_fixed + C - 1) / C;
+    const long long items = slots * H;
+    // The fused output gate runs on the serial chain (its clusters are the
+    // four column tiles of one sequence and head).
+    const OutGate og{static_cast<const __nv_bfloat16 *>(gate.z), gate.w, gate.eps};
+    const int P = og.z ? 1 : state_segments(segments, seg_max, nch, (long long)num_seqs * H, sm_count);
+    // The fused launch: on the serial chain, with chunk c of every sequence at
+    // the same place in phase 1's order (fixed-length batches, or one packed
+    // sequence), and when the cost model favours it. With the output gate it
+    // writes plain outputs and the gate pass follows (one read of o and z, one
+    // write: cheaper than the two launches with the gate in the state pass,
+    // whose output warps then lengthen every chunk).
+    const long long n_state = (long long)num_seqs * H * (D / 64);
+    const int chain_chunks = cu_seqlens ? (int)(slots / (num_seqs > 0 ? num_seqs : 1)) : nch;
+    const bool use_fused = fused >= 0 && coop_ok[dev] && P <= 1 && slots > 0 && tokens > 0 &&
+                           (!cu_seqlens || num_seqs == 1) && n_state <= sm_count - 8 &&
+                           (fused == 1 || fuse_pays(items, chain_chunks, n_state, sm_count));
+    int var = kVarRuntime;
+    if (!pro.l2norm) {
+        if (pro.decay == KDA_DECAY_NONE)  // the gate is never applied
+            var = kVarNone;
+        else if (pro.gate == KDA_GATE_LOG)
+            var = pro.decay == KDA_DECAY_CHANNEL ? kVarChannel : kVarScalar;
+    } else if (pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOGSIGMOID) {
+        var = kVarGated;
+    }
     if ((err = mark(events, 1, stream)) != cudaSuccess) return err;
+    CUtensorMap tq, tk, tg;
+    memset(&tg, 0, sizeof(tg));  // read only with a per-channel g
     if (slots > 0 && tokens > 0) {
-        CUtensorMap tq, tk, tg;
-        memset(&tg, 0, sizeof(tg));  // read only with a per-channel g
         if ((err = token_rows_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess ||
             (err = token_rows_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, H, tokens)) != cudaSuccess)
             return err;
         if (pro.decay == KDA_DECAY_CHANNEL &&
             (err = token_rows_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, H, tokens)) != cudaSuccess)
             return err;
-        const long long items = slots * H;
-        const unsigned grid = (unsigned)(items < sm_count ? items : sm_count);
-        int var = kVarRuntime;
-        if (!pro.l2norm) {
-            if (pro.decay == KDA_DECAY_NONE)  // the gate is never applied
-                var = kVarNone;
-            else if (pro.gate == KDA_GATE_LOG)
-                var = pro.decay == KDA_DECAY_CHANNEL ? kVarChannel : kVarScalar;
-        } else if (pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOGSIGMOID) {
-            var = kVarGated;
+    }
+    if (use_fused) {
+        // Ready flags after the regions: one int per (slot, head), cleared here.
+        int *ready = reinterpret_cast<int *>(region + (size_t)slots * H * TcRegion::bytes);
+        CUtensorMap tv;
+        if ((err = value_rows_map(&tv, v, H, tokens, 64)) != cudaSuccess) return err;
+        if ((err = cudaMemsetAsync(ready, 0, (size_t)slots * H * sizeof(int), stream)) != cudaSuccess)
+            return err;
+        const int ilv = cu_seqlens ? 1 : num_seqs;
+        const int nstate = (int)n_state;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)sm_count);
+        cfg.blockDim = dim3(kP2Threads);
+        cfg.dynamicSmemBytes = kFusedSmem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out);
+        unsigned char *ws = region;
+#define KDA_FUSED(V)                                                                               \
+    err = cudaLaunchKernelEx(&cfg, tc_prefill_fused<V>, tq, tk, tg, tv, g, pro, beta, scale, table, \
+                             used, slots, H, ws, status, seq_first_slot, order, cu_seqlens, T_fixed, \
+                             init_state, o, final_state, nstate, ready, ilv, nch)
+        switch (var) {
+            case kVarChannel: KDA_FUSED(kVarChannel); break;
+            case kVarScalar: KDA_FUSED(kVarScalar); break;
+            case kVarNone: KDA_FUSED(kVarNone); break;
+            case kVarGated: KDA_FUSED(kVarGated); break;
+            default: KDA_FUSED(kVarRuntime); break;
         }
-        const int *used = seq_first_slot + num_seqs;
+#undef KDA_FUSED
+        if (err == cudaSuccess) {
+            // Phase 1 and the state pass are one launch: both phase marks follow it.
+            if ((err = mark(events, 2, stream)) != cudaSuccess) return err;
+            if (og.z && (err = launch_output_gate_rmsnorm(out, og.z, og.w, og.eps, out, tokens * H, D,
+                                                          KDA_DTYPE_BF16, stream)) != cudaSuccess)
+                return err;
+            return mark(events, 3, stream);
+        }
+        // Not resident all at once on this device (or not supported): the
+        // two launches below do the same work.
+        if (err != cudaErrorCooperativeLaunchTooLarge && err != cudaErrorNotSupported) return err;
+        (void)cudaGetLastError();
+    }
+    if (slots > 0 && tokens > 0) {
+        const unsigned grid = (unsigned)(items < sm_count ? items : sm_count);
 #define KDA_P1_LAUNCH(V)                                                                        \
     tc_intra_chunk<V><<<grid, kP1Threads, P1::bytes, stream>>>(tq, tk, tg, g, pro, beta, scale,     \
                                                                table, used, slots, H, region, status)
@@ -1667,23 +1871,19 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     if (num_seqs > 0) {
         static_assert(2 * (D / kTN) <= kMaxStateTiles, "grid bound checked with kMaxStateTiles");
         constexpr int kTiles = D / kTN;
-        const int *order = seq_first_slot + num_seqs + 1;
-        const int nch = (T_fixed + C - 1) / C;
-        // The fused output gate runs on the serial chain (its clusters are the
-        // four column tiles of one sequence and head).
-        const OutGate og{static_cast<const __nv_bfloat16 *>(gate.z), gate.w, gate.eps};
-        const __nv_bfloat16 *vin = static_cast<const __nv_bfloat16 *>(v);
-        CUtensorMap tz;
+        constexpr int kSmem = P2L<kTN>::kSmem;
+        CUtensorMap tz, tv;
         memset(&tz, 0, sizeof(tz));  // read only by the fused gate
+        memset(&tv, 0, sizeof(tv));  // read only when there are tokens
         if (og.z && (err = gate_rows_map(&tz, og.z, H, tokens)) != cudaSuccess) return err;
-        const int P = og.z ? 1 : state_segments(segments, seg_max, nch, (long long)num_seqs * H, sm_count);
+        if (tokens > 0 && (err = value_rows_map(&tv, v, H, tokens, kTN)) != cudaSuccess) return err;
         if (P <= 1 && og.z) {
             static_assert(kGateCluster == kTiles, "a cluster holds the column tiles of one head");
             const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)num_seqs * H * kTiles);
             cfg.blockDim = dim3(kP2Threads);
-            cfg.dynamicSmemBytes = kP2Smem;
+            cfg.dynamicSmemBytes = kSmem;
             cfg.stream = stream;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1695,13 +1895,13 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             if ((err = cudaLaunchKernelEx(&cfg, tc_state_pass, (const unsigned char *)region,
                                           seq_first_slot, order, cu_seqlens, T_fixed, init_state,
                                           static_cast<__nv_bfloat16 *>(out), final_state, H, status,
-                                          sp, og, tz, vin)) != cudaSuccess)
+                                          sp, og, tz, tv)) != cudaSuccess)
                 return err;
         } else if (P <= 1) {
             const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
-            tc_state_pass<<<(unsigned)num_seqs * H * kTiles, kP2Threads, kP2Smem, stream>>>(
+            tc_state_pass<<<(unsigned)num_seqs * H * kTiles, kP2Threads, kSmem, stream>>>(
                 region, seq_first_slot, order, cu_seqlens, T_fixed, init_state,
-                static_cast<__nv_bfloat16 *>(out), final_state, H, status, sp, og, tz, vin);
+                static_cast<__nv_bfloat16 *>(out), final_state, H, status, sp, og, tz, tv);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         } else {
             const int L = (nch + P - 1) / P;
@@ -1709,10 +1909,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             float *xfer = seg_ws;
             float *enter = seg_ws + (size_t)num_seqs * H * Pn * D * 2 * D;
             const SegPass sa{L, Pn, 0, Pn - 1, 1, xfer, enter};
-            tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * 2 * kTiles, kP2Threads, kP2Smem,
+            tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * 2 * kTiles, kP2Threads, kSmem,
                             stream>>>(region, seq_first_slot, order, cu_seqlens, T_fixed,
                                       init_state, static_cast<__nv_bfloat16 *>(out), final_state,
-                                      H, status, sa, og, tz, vin);
+                                      H, status, sa, og, tz, tv);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
             if (Pn > 2) {
                 seg_combine<<<(unsigned)num_seqs * H * (D / kCombCols), kCombThreads, kCombSmem,
@@ -1720,10 +1920,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                 if ((err = cudaGetLastError()) != cudaSuccess) return err;
             }
             const SegPass sc{L, Pn, 1, Pn - 1, 0, xfer, enter};
-            tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * kTiles, kP2Threads, kP2Smem,
+            tc_state_pass<<<(unsigned)num_seqs * H * (Pn - 1) * kTiles, kP2Threads, kSmem,
                             stream>>>(region, seq_first_slot, order, cu_seqlens, T_fixed,
                                       init_state, static_cast<__nv_bfloat16 *>(out), final_state,
-                                      H, status, sc, og, tz, vin);
+                                      H, status, sc, og, tz, tv);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
         }
     }

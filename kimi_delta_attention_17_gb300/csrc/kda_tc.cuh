@@ -135,6 +135,46 @@ __device__ __forceinline__ void bar_arrive(int id, int nthreads) {
 __device__ __forceinline__ void bar_sync(int id, int nthreads) {
     asm volatile("barrier.cta.sync.aligned %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Barrier `id` over `nthreads` threads (whole warps) that also returns whether
+// `pred` holds in every one of them (bar_and) or in any (bar_or).
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{.reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.cta.red.and.aligned.pred q, %2, %3, p; "
+        "selp.u32 %0, 1, 0, q;}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool bar_or(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{.reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.cta.red.or.aligned.pred q, %2, %3, p; "
+        "selp.u32 %0, 1, 0, q;}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+// A flag in global memory handed from one CTA to another: the writer's
+// release orders every earlier write it has seen (a barrier before it makes
+// its CTA's writes seen) before the flag; the reader's acquire orders its
+// later reads after it.
+__device__ __forceinline__ void st_release_gpu(int *p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Orders this thread's earlier generic-proxy accesses of global memory (such
+// as an acquire of data another CTA wrote) before its later async-proxy ones
+// (bulk and tensor copies).
+__device__ __forceinline__ void fence_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 // Barrier `id` over `nthreads` threads of the CTA (whole warps),
 // returning whether `pred` held in every one of them.
 __device__ __forceinline__ bool bar_and(bool pred, int id, int nthreads) {

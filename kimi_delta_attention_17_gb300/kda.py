@@ -48,9 +48,9 @@ def workspace_size(B, T, H, dk, dv, num_seqs, dtype):
                                                        _DTYPES[dtype]))
 
 
-def _options(decay, gate, gate_lower, l2norm_qk, segments=0):
+def _options(decay, gate, gate_lower, l2norm_qk, segments=0, fused=None):
     """kda_options for the given names, or None for the plain entry points."""
-    if decay == "channel" and gate == "log" and not l2norm_qk and segments == 0:
+    if decay == "channel" and gate == "log" and not l2norm_qk and segments == 0 and fused is None:
         return None
     if decay not in _lib.DECAY or gate not in _lib.GATE:
         raise ValueError("decay must be one of %s and gate one of %s"
@@ -58,7 +58,7 @@ def _options(decay, gate, gate_lower, l2norm_qk, segments=0):
     if int(segments) < 0:
         raise ValueError("segments must be >= 0")
     return _lib.Options(_lib.DECAY[decay], _lib.GATE[gate], float(gate_lower), int(bool(l2norm_qk)),
-                        int(segments))
+                        int(segments), 0 if fused is None else (1 if fused else -1))
 
 
 def _check_g(g, decay, nd):
@@ -73,7 +73,7 @@ def _check_g(g, decay, nd):
 def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=None,
               final_state=None, workspace=None, output_final_state=True, stream=None,
               phase_events=None, decay="channel", gate="log", gate_lower=-5.0, l2norm_qk=False,
-              segments=0, out_gate=None, norm_weight=None, norm_eps=1e-6):
+              segments=0, out_gate=None, norm_weight=None, norm_eps=1e-6, fused=None):
     """Chunkwise prefill. q, k [B, T, H, dk]; v [B, T, H, dv] (bf16 or fp32);
     g [B, T, H, dk] fp32; beta [B, T, H] fp32; init_state [N, H, dk, dv] fp32
     or None; cu_seqlens int32 [N+1] (device) or None (then N = B).
@@ -87,11 +87,14 @@ def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=
     gate_lower * sigmoid(g)); ``l2norm_qk`` normalises q and k in the kernel;
     ``segments`` how the state crosses the chunks on the tensor-core path (0
     automatic, 1 one serial chain, k up to k segments composed as affine maps;
-    kda_options.segments).
+    kda_options.segments). ``fused`` (kda_options.fused): None lets the
+    library run phase 1 and the state pass as one cooperative launch where
+    that is expected to be faster, True wherever it is supported, False never.
     ``out_gate`` (gate logits z, q's dtype and v's shape) makes ``out`` the
     gated, RMS-normalised output w * o / sqrt(mean(o^2) + norm_eps) *
     sigmoid(z), with ``norm_weight`` [dv] fp32 or None (kda_chunk_fwd_gated;
-    fused into the state pass on the tensor-core path)."""
+    on the tensor-core path applied in the state pass, or as a pass over the
+    outputs of the fused launch)."""
     _need(q, "q", ndim=4)
     dtype = q.dtype
     if dtype not in _DTYPES:
@@ -122,7 +125,7 @@ def chunk_fwd(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     else:
         _need(workspace, "workspace", torch.uint8, 1)
-    opts = _options(decay, gate, gate_lower, l2norm_qk, segments)
+    opts = _options(decay, gate, gate_lower, l2norm_qk, segments, fused)
     head = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(init_state),
             _ptr(cu_seqlens), _ptr(out), _ptr(final_state), B, T, H, dk, dv, N, _DTYPES[dtype])
     tail = (_ptr(workspace), workspace.numel(), _stream_ptr(stream))
@@ -230,7 +233,7 @@ def host_workspace_size(H, dk, dv, dtype, window_tokens=16384, decay="channel"):
 def chunk_fwd_host(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *, out=None,
                    final_state=None, window_tokens=16384, workspace=None, scratch=None,
                    device=None, stream=None, decay="channel", gate="log", gate_lower=-5.0,
-                   l2norm_qk=False):
+                   l2norm_qk=False, fused=None):
     """The prefill with every tensor in host memory (kda_chunk_fwd_host): q, k,
     v [B, T, H, d], g, beta as in chunk_fwd, init_state [N, H, dk, dv] or None,
     cu_seqlens an int32 HOST tensor [N + 1] or None, all pinned for the copies
@@ -266,7 +269,7 @@ def chunk_fwd_host(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, *,
         out = torch.empty((B, T, H, dv), dtype=dtype).pin_memory()
     if final_state is None:
         final_state = torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory()
-    opts = _options(decay, gate, gate_lower, l2norm_qk, 1)
+    opts = _options(decay, gate, gate_lower, l2norm_qk, 1, fused)
     need = int(_lib.lib().kda_chunk_fwd_host_workspace_size(H, dk, dv, _DTYPES[dtype],
                                                             ctypes.byref(opts), window_tokens))
     if workspace is None:
