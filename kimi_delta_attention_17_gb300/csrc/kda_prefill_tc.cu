@@ -198,6 +198,12 @@ struct P1Walk {
     int ilv, nch;
 };
 
+// The item order's slot index -> the table slot.
+__device__ __forceinline__ int p1_phys(const P1Walk &wk, int s) {
+    return wk.ilv > 1 ? (s % wk.ilv) * wk.nch + s / wk.ilv : s;
+}
+
+
 // Phase 1 for the threads 0 .. kP1Threads - 1 of a CTA (its barriers count
 // exactly those threads, so a larger CTA may run it with the rest idle).
 template <int kVar>
@@ -221,8 +227,13 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
     // ...: stepping by the grid in (slot, head) form keeps 64-bit divisions off
     // the item path.
     const int step_s = (int)(wk.count / H), step_h = (int)(wk.count % H);
-    // The table slot of the item order's slot index.
-    auto phys = [&](int s) { return wk.ilv > 1 ? (s % wk.ilv) * wk.nch + s / wk.ilv : s; };
+    auto phys = [&](int s) { return p1_phys(wk, s); };
+    // Fused prefill: the ready flag of the item before, released by thread 0
+    // in the middle of this item's triangular solve. A release waits for the
+    // stores in flight to reach L2; the solve writes only shared memory, and
+    // by then the region writes have drained, so the wait is short (right
+    // after an item's stores it takes an L2 round trip per item).
+    long long flag_prev = -1;  // its index in wk.ready, or -1
     auto advance = [&](int &sl, int &hh) {
         sl += step_s;
         hh += step_h;
@@ -647,6 +658,10 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
                 }
             }
             bar_sync(0, kP1Threads);
+            if (wk.ready && tid == 0 && flag_prev >= 0) {
+                st_release_gpu(wk.ready + flag_prev, 1);
+                flag_prev = -1;
+            }
             // Off-diagonal blocks: with M_IK = T_II A_IK (K < I), block row I of
             // (I - A) T = I gives T_IJ = sum_{K = J}^{I - 1} M_IK T_KJ. The
             // substitution above formed the six M blocks; stage 2 forms the first
@@ -780,9 +795,9 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
         fence_before();
         bar_sync(0, kP1Threads);
         fence_after();
-        // Every thread's region writes precede the barrier: the release makes
-        // them visible before the flag that hands the item to the state pass.
-        if (wk.ready && tid == 0) st_release_gpu(wk.ready + (size_t)phys(sl) * H + hc, 1);
+        // Every thread's region writes precede this barrier, so a later
+        // release by thread 0 makes them visible before the item's flag.
+        flag_prev = (long long)phys(sl) * H + hc;
         sl = sn;
         hc = hn;
         ce = en;
@@ -797,6 +812,8 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
         mbar_wait(bar_ld, ld_phase);
         mbar_wait(bar_mma, mma_phase);
     }
+    // The last item's flag (after an error the state pass gives up on its own).
+    if (wk.ready && tid == 0 && flag_prev >= 0 && ok) st_release_gpu(wk.ready + flag_prev, 1);
     fence_before();
     bar_sync(0, kP1Threads);
     if (warp == 0) tmem_dealloc<256>(tmem);
@@ -827,20 +844,23 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 //                  S <- Diag(exp G_n) S + D2,  O = D1[0:64] = s Qbar S + H Z
 // ("Understanding Kimi Delta Attention", "The token outputs" and "One state
 // crosses the chunk boundary"). S and Z enter the MMAs as bf16 hi + lo pairs.
-// Warp roles: warps 0-15 compute. Warp 16's lane 0 issues the two products on
-// the chain of dependent steps, and the warp keeps the named barriers with
-// the compute warps. Warp 17's lane 0 issues the copies of the chunk tiles and
-// warp 18's lane 0 the products off the chain (U a chunk ahead, H Z), both
-// paced by mbarriers alone: an MMA's issue holds its thread while the tensor
-// pipe is busy (about 60 cycles per M = 128, K = 16 step), and a bulk copy's
-// issue can too, which must not delay a named barrier. (Two roles in one warp
-// would stall each other: a suspended wait holds the whole warp.)
-constexpr int kP2Compute = 512;
-constexpr int kP2MmaWarp = kP2Compute / 32;
-constexpr int kP2CopyWarp = kP2MmaWarp + 1;
-constexpr int kP2SideWarp = kP2MmaWarp + 2;
-constexpr int kP2Threads = kP2Compute + 96;
-constexpr int kP2Sync = kP2Compute + 32;  // compute warps + MMA warp
+// Warp roles, 32-column slabs: warps 0-15 compute. Warp 16's lane 0 issues
+// the two products on the chain of dependent steps, and the warp keeps the
+// named barriers with the compute warps. Warp 17's lane 0 issues the copies
+// of the chunk tiles and warp 18's lane 0 the products off the chain (U a
+// chunk ahead, H Z), both paced by mbarriers alone: an MMA's issue holds its
+// thread while the tensor pipe is busy (about 60 cycles per M = 128, K = 16
+// step), and a bulk copy's issue can too, which must not delay a named
+// barrier. (Two roles in one warp would stall each other: a suspended wait
+// holds the whole warp.)
+// 64-column slabs (the fused prefill): 12 compute warps (three column groups
+// of 24, 24 and 16 columns), warp 12 the chain and warp 13 the copies; the
+// chain warp issues U and H Z as well (the Z and state-update windows, longer
+// with up to 24 columns a thread, cover their issue). The fused kernel then
+// fits in 16 warps: with more, one SM sub-partition holds five warps and the
+// register file caps every thread at 96 registers, which slows phase 1.
+constexpr int kP2Threads = 16 * 32 + 96;   // the 32-column state pass
+constexpr int kFusedThreads = kP1Threads;  // the fused kernel (16 warps)
 constexpr int kBarZ = 1, kBarS = 2;       // named barriers: Z written, state written
 constexpr int kBarO = 3;                  // named barrier of the output warps (fused gate)
 // A chunk's tiles sit in three rings, by lifetime:
@@ -959,7 +979,15 @@ __device__ __forceinline__ void state_pass_body(
     int *__restrict__ status, const SegPass sp, const OutGate og_in, const CUtensorMap *tm_z,
     const CUtensorMap *tm_v, int vblock, const int *ready) {
     using L = P2L<TN>;
-    constexpr int NJ = TN / 4;  // slab columns per compute thread
+    // Compute warps: the four lane quadrants times CG column groups; a group
+    // takes NP 8-column pieces of the slab (the last one may take fewer).
+    constexpr int CW = TN == kTN ? 16 : 12;
+    constexpr int CG = CW / 4;
+    constexpr int NP = (TN / 8 + CG - 1) / CG;
+    constexpr int NJ = 8 * NP;                        // slab columns a compute thread holds, at most
+    constexpr int kMma = CW, kCopy = CW + 1, kSideW = CW + 2;  // warp roles
+    constexpr int kSync = CW * 32 + 32;               // compute warps + MMA warp
+    constexpr bool kSide = TN == kTN;     // U and H Z from their own warp
     extern __shared__ __align__(1024) unsigned char sm[];
     const OutGate og = TN == kTN ? og_in : OutGate{nullptr, nullptr, 0.f};
     const bool gated = og.z != nullptr;
@@ -1064,25 +1092,26 @@ __device__ __forceinline__ void state_pass_body(
     };
 
     // Compute-thread coordinates: TMEM lane / state row r, slab columns js .. js + NJ - 1.
-    const int r = 32 * (warp & 3) + lane, js = NJ * ((warp >> 2) & 3);
+    const int r = 32 * (warp & 3) + lane, cgi = warp >> 2, js = 8 * NP * cgi;
+    const int np = warp < CW ? min(NP, TN / 8 - NP * cgi) : 0;  // this thread's pieces
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     float S[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) S[j] = ident && r == j0 + js + j ? 1.f : 0.f;
     auto put_state = [&]() {  // B1 rows js + j (hi) and TN + js + j (lo), K-row r
 #pragma unroll
-        for (int q = 0; q < NJ / 8; ++q) {
+        for (int q = 0; q < NP; ++q) if (q < np) {
             uint4 hi, lo;
             split8(S + 8 * q, hi, lo);
             *reinterpret_cast<uint4 *>(B1 + mnmaj(js + 8 * q, r, kB1Lbo, kB1Sbo)) = hi;
             *reinterpret_cast<uint4 *>(B1 + mnmaj(TN + js + 8 * q, r, kB1Lbo, kB1Sbo)) = lo;
         }
     };
-    if (warp < kP2MmaWarp) {
+    if (warp < CW) {
         if (st_src) {
             const float *src = st_src + (size_t)r * D + j0 + js;
 #pragma unroll
-            for (int q = 0; q < NJ / 4; ++q) {
+            for (int q = 0; q < 2 * NP; ++q) if (q < 2 * np) {
                 const float4 t4 = *reinterpret_cast<const float4 *>(src + 4 * q);
                 S[4 * q] = t4.x; S[4 * q + 1] = t4.y; S[4 * q + 2] = t4.z; S[4 * q + 3] = t4.w;
             }
@@ -1117,7 +1146,7 @@ __device__ __forceinline__ void state_pass_body(
     // slot's (ch / kXBufs)-th use: its copies complete the phase of parity
     // (ch / kXBufs) & 1 of the slot's "landed" barrier, and its release the
     // phase of the same parity of the "free" one.
-    if (warp == kP2CopyWarp) {
+    if (warp == kCopy) {
         if (lane == 0) {
             // Chunk c's copies go out as their slots free, in the order the
             // slots free: H (chunk c - 3's last product), X (chunk c - 2's
@@ -1174,7 +1203,7 @@ __device__ __forceinline__ void state_pass_body(
                 mbar_wait(bar_hl + cc % kHBufs, (uint32_t)(cc / kHBufs) & 1);
         }
         __syncwarp();
-    } else if (warp == kP2SideWarp) {
+    } else if (kSide && warp == kSideW) {
         if (lane == 0 && has_h) {
             // U of chunk ch + 1 = [H; T B] times its value rows (rows 64-127 of
             // the product; the H rows give nothing used), into TMEM columns by
@@ -1228,7 +1257,7 @@ __device__ __forceinline__ void state_pass_body(
             }
         }
         __syncwarp();
-    } else if (warp == kP2MmaWarp) {
+    } else if (warp == kMma) {
         // One lane issues; the whole warp keeps the named-barrier protocol, so
         // the compute warps never wait on a barrier that cannot complete.
         // Descriptors of slot 0's tiles and of the state-side operands are
@@ -1240,6 +1269,24 @@ __device__ __forceinline__ void state_pass_body(
         const uint64_t d_b2 = desc(smem_u32(B2), kB2Lbo, kB2Sbo);
         const uint32_t id1 = idesc_bf16(128, 2 * TN, 1, 1), id2 = idesc_bf16(128, 2 * TN, 0, 1);
         bool ok = true;  // lane 0: every wait so far succeeded
+        // Without the side warp: U of chunk ch + 1 right after chunk ch's first
+        // product (the pipe runs it while the compute warps form Z), and H Z
+        // right after the second product.
+        const uint64_t d_ht = desc(smem_u32(sm + L::kH), kA2Lbo, kA2Sbo);
+        const uint64_t d_v = desc(smem_u32(sm + L::kH + kHTBytes), kBvLbo, kBvSbo);
+        const uint32_t idu = idesc_bf16(128, TN, 0, 1);
+        auto issue_u = [&](int ch) {
+            ok = ok && wait(bar_hl + ch % kHBufs, (uint32_t)(ch / kHBufs) & 1);
+            if (!ok) return;
+            const uint64_t ho = (uint64_t)(ch % kHBufs) * (L::kHBytes >> 4);
+            fence_after();
+#pragma unroll
+            for (int s = 0; s < C / 16; ++s)
+                mma_bf16(tmem + L::kUCol + TN * (ch & 1), d_ht + ho + s * (2 * kA2Lbo >> 4),
+                         d_v + ho + s * (2 * kBvLbo >> 4), idu, s > 0);
+            commit(bar_u + (ch & 1));
+        };
+        if (!kSide && lane == 0 && !ident && nchunks > 0) issue_u(0);
         for (int ch = 0; ch < nchunks; ++ch) {
             const uint64_t xo = (uint64_t)(ch % kXBufs) * (kXBytes >> 4);
             const uint64_t ko = (uint64_t)(ch % kKBufs) * (kKBytes >> 4);
@@ -1256,15 +1303,16 @@ __device__ __forceinline__ void state_pass_body(
                         mma_bf16(d1, d_a1 + xo + s * (2 * kA1Lbo >> 4), d_b1 + s * (2 * kB1Lbo >> 4),
                                  id1, s > 0);
                     commit(bar_m1);
-                    commit(bar_m1s);
+                    if (kSide) commit(bar_m1s);
                 }
                 // The X slot is free once everything issued so far has completed.
                 commit(bar_xf + ch % kXBufs);
+                if (!kSide && !ident && ch + 1 < nchunks) issue_u(ch + 1);
                 // The second product reads the K tiles.
                 ok = ok && wait(bar_kl + ch % kKBufs, (uint32_t)(ch / kKBufs) & 1);
             }
             __syncwarp();
-            bar_sync(kBarZ, kP2Sync);  // Z of this chunk is in B2
+            bar_sync(kBarZ, kSync);  // Z of this chunk is in B2
             fence_after();
             if (lane == 0) {
                 if (ok) {
@@ -1274,17 +1322,28 @@ __device__ __forceinline__ void state_pass_body(
                         mma_bf16(tmem + L::kD2Col, d_a2 + ko + s * (2 * kA2Lbo >> 4),
                                  d_b2 + s * (2 * kB2Lbo >> 4), id2, s > 0);
                     commit(bar_m2);
+                    if (!kSide && outputs) {
+                        // D1 += [H; T B] [Z_hi | Z_lo]: H Z into the s Qbar S rows.
+                        const uint64_t ho = (uint64_t)(ch % kHBufs) * (L::kHBytes >> 4);
+#pragma unroll
+                        for (int s = 0; s < C / 16; ++s)
+                            mma_bf16(d1, d_ht + ho + s * (2 * kA2Lbo >> 4), d_b2 + s * (2 * kB2Lbo >> 4),
+                                     id2, 1);
+                        commit(bar_m3);
+                    }
                 }
                 commit(bar_kf + ch % kKBufs);
+                // Chunk ch's U (issued a chunk ago) and H Z were the H slot's readers.
+                if (!kSide && has_h) commit(bar_hf + ch % kHBufs);
                 if (ch + 1 < nchunks)
                     ok = ok && wait(bar_xl + (ch + 1) % kXBufs, (uint32_t)((ch + 1) / kXBufs) & 1);
             }
             __syncwarp();
-            bar_sync(kBarS, kP2Sync);  // the new state is in B1
+            bar_sync(kBarS, kSync);  // the new state is in B1
             fence_after();
         }
         __syncwarp();
-    } else {
+    } else if (warp < CW) {
         uint32_t p1 = 0, p2 = 0, p3 = 0;  // phases of the three product barriers
         uint32_t rph = 0;                 // phases of the two row-partial barriers (bit per parity)
         const bool zrow = r >= 64;
@@ -1324,7 +1383,7 @@ __device__ __forceinline__ void state_pass_body(
             if (!gated) {
                 const int clen = min(C, len - (c0 + ch) * C);
 #pragma unroll
-                for (int q = 0; q < NJ / 8; ++q) {
+                for (int q = 0; q < NP; ++q) if (q < np) {
                     float hi[8], lo[8], o[8];
                     tmem_ld8(d1 + js + 8 * q, hi);
                     tmem_ld8(d1 + TN + js + 8 * q, lo);
@@ -1429,7 +1488,7 @@ __device__ __forceinline__ void state_pass_body(
                 spin(bar_u + (ch & 1), (uint32_t)(ch >> 1) & 1);
                 fence_after();
 #pragma unroll
-                for (int q = 0; q < NJ / 8; ++q) {
+                for (int q = 0; q < NP; ++q) if (q < np) {
                     float u8[8];
                     tmem_ld8(tmem + lane_base + L::kUCol + TN * (ch & 1) + js + 8 * q, u8);
                     tmem_wait_ld();
@@ -1452,7 +1511,7 @@ __device__ __forceinline__ void state_pass_body(
                 // Z = U - W S for token row i, slab columns js .. js + NJ - 1.
                 const int i = r - 64;
 #pragma unroll
-                for (int q = 0; q < NJ / 8; ++q) {
+                for (int q = 0; q < NP; ++q) if (q < np) {
                     float hi[8], lo[8], z[8];
                     tmem_ld8(d1 + lane_base + js + 8 * q, hi);
                     tmem_ld8(d1 + lane_base + TN + js + 8 * q, lo);
@@ -1467,13 +1526,13 @@ __device__ __forceinline__ void state_pass_body(
             }
             fence_async_smem();
             fence_before();
-            bar_arrive(kBarZ, kP2Sync);
+            bar_arrive(kBarZ, kSync);
             if (!zrow && outputs && ch > 0) put_outputs_b(ch - 1);  // while the second product runs
             spin(bar_m2, p2);
             p2 ^= 1;
             fence_after();
 #pragma unroll
-            for (int q = 0; q < NJ / 8; ++q) {
+            for (int q = 0; q < NP; ++q) if (q < np) {
                 float hi[8], lo[8];
                 tmem_ld8(tmem + lane_base + L::kD2Col + js + 8 * q, hi);
                 tmem_ld8(tmem + lane_base + L::kD2Col + TN + js + 8 * q, lo);
@@ -1488,7 +1547,7 @@ __device__ __forceinline__ void state_pass_body(
             // the product barriers pace the compute warps) keeps every warp
             // within one phase of the named barriers even when a timeout has
             // made the product waits fall through.
-            bar_sync(kBarS, kP2Sync);
+            bar_sync(kBarS, kSync);
         }
         if (nchunks > 0 && !zrow && outputs) {
             wait(bar_m3, p3);
@@ -1502,8 +1561,8 @@ __device__ __forceinline__ void state_pass_body(
         if (st_dst && !refused && !*err) {
             float *dst = st_dst + (size_t)r * dst_row + j0 + js;
 #pragma unroll
-            for (int q = 0; q < NJ / 4; ++q)
-                *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+            for (int q = 0; q < 2 * NP; ++q)
+                if (q < 2 * np) *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
         }
     }
     fence_before();
@@ -1530,7 +1589,7 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
 // never waits for the state pass, and the launch is cooperative (all CTAs
 // resident at once), so every flag a state-pass CTA waits for gets set.
 template <int kVar>
-__global__ void __launch_bounds__(kP2Threads, 1)
+__global__ void __launch_bounds__(kFusedThreads, 1)
 tc_prefill_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_v,
                  const float *__restrict__ g_head, Prologue pro, const float *__restrict__ beta,
@@ -1545,7 +1604,7 @@ tc_prefill_fused(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         state_pass_body<64>(ws, seq_first_slot, seq_order, cu_seqlens, T_fixed, init_state, out,
                             final_state, H, status, sp, OutGate{nullptr, nullptr, 0.f}, &tm_v, &tm_v,
                             (int)blockIdx.x, ready);
-    } else if (threadIdx.x < kP1Threads) {
+    } else {
         intra_chunk_body<kVar>(&tm_q, &tm_k, &tm_g, g_head, pro, beta, scale, table, used_slots, nslots,
                                H, ws, status,
                                P1Walk{(int)blockIdx.x - n_state, (int)gridDim.x - n_state, ready, ilv, nch});
@@ -1817,7 +1876,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         const int nstate = (int)n_state;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)sm_count);
-        cfg.blockDim = dim3(kP2Threads);
+        cfg.blockDim = dim3(kFusedThreads);
         cfg.dynamicSmemBytes = kFusedSmem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
