@@ -1402,6 +1402,7 @@ __device__ __forceinline__ void state_pass_body(
             }
             zph ^= 1;
             zr = *reinterpret_cast<const uint4 *>(zslot + r * TN + js);
+            __syncwarp();
             float hi[8], lo[8];
             tmem_ld8(d1 + js, hi);
             tmem_ld8(d1 + TN + js, lo);
@@ -1413,6 +1414,9 @@ __device__ __forceinline__ void state_pass_body(
 #pragma unroll
             for (int j = 0; j < 8; ++j) ss += o8[j] * o8[j];
             loc[(js >> 3) * 64 + r] = ss;
+            // The z reads (generic proxy) are ordered before the tensor-map
+            // copy that refills the slot (async proxy) after the barrier.
+            fence_async_smem();
             // Every output thread has read its z (the slot is free) and has
             // finished the previous chunk, whose row sums it read: that
             // barrier's next phase (chunk ch + 1) may now expect its bytes,
@@ -1487,6 +1491,7 @@ __device__ __forceinline__ void state_pass_body(
             if (zrow && !ident) {
                 spin(bar_u + (ch & 1), (uint32_t)(ch >> 1) & 1);
                 fence_after();
+                __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane wait
 #pragma unroll
                 for (int q = 0; q < NP; ++q) if (q < np) {
                     float u8[8];
@@ -1502,11 +1507,13 @@ __device__ __forceinline__ void state_pass_body(
                 wait(bar_m3, p3);
                 p3 ^= 1;
                 fence_after();
+                __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane wait
                 put_outputs_a(ch - 1);
             }
             spin(bar_m1, p1);
             p1 ^= 1;
             fence_after();
+            __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane wait
             if (zrow) {
                 // Z = U - W S for token row i, slab columns js .. js + NJ - 1.
                 const int i = r - 64;
@@ -1531,6 +1538,7 @@ __device__ __forceinline__ void state_pass_body(
             spin(bar_m2, p2);
             p2 ^= 1;
             fence_after();
+            __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane wait
 #pragma unroll
             for (int q = 0; q < NP; ++q) if (q < np) {
                 float hi[8], lo[8];
@@ -1552,6 +1560,7 @@ __device__ __forceinline__ void state_pass_body(
         if (nchunks > 0 && !zrow && outputs) {
             wait(bar_m3, p3);
             fence_after();
+            __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane wait
             put_outputs_a(nchunks - 1);
             put_outputs_b(nchunks - 1);
         }

@@ -6,7 +6,7 @@ several chunks with ragged tails, fixed-length batches (phase 1 then walks
 the items chunk-major across the sequences), one packed sequence, initial
 states, the decay / gate / normalisation variants, edge-case decays, the
 gated output (the fused launch, then the gate pass), one workspace reused by
-consecutive calls (the flags are cleared by every call), the fall-back when
+consecutive calls (the flags are cleared by every call), repeatability, the fall-back when
 too many chains leave no SMs to phase 1, agreement with the two launches, and
 the automatic choice on the long workload's shape at a shorter length."""
 import numpy as np
@@ -136,10 +136,12 @@ def test_fused_edge_decays():
     check(out, fin, ref_out, ref_fin, "edge heads")
 
 
-def test_fused_then_gate_pass():
+@pytest.mark.parametrize("T", [300, 64, 20], ids=["T300", "T64", "T20"])
+def test_fused_then_gate_pass(T):
     """The gated prefill where the fused launch applies: plain outputs, then
-    the gate and RMS normalisation as a pass over them."""
-    spec = PrefillSpec("fused gated", H=4, d=128, B=2, T=300, init="normal0.1", seed=70)
+    the gate and RMS normalisation as a pass over them (several chunks,
+    exactly one chunk, a single ragged chunk)."""
+    spec = PrefillSpec("fused gated", H=4, d=128, B=2, T=T, init="normal0.1", seed=70)
     inp = make_prefill(spec)
     gen = torch.Generator().manual_seed(71)
     z = torch.randn(inp["v"].shape, generator=gen).to(inp["v"].dtype)
@@ -152,6 +154,28 @@ def test_fused_then_gate_pass():
     print("\nfused + gate pass: max|err| %.3g (bound %.3g), rel %.3g" % (m, BF16_MAX_ABS * gain, r))
     assert m <= BF16_MAX_ABS * gain and r <= BF16_REL_FRO
     assert_parity(f64(fin), ref_fin, "bf16", "final state (gated)")
+
+
+@pytest.mark.parametrize("fused,gated", [(True, False), (True, True), (False, True)],
+                         ids=["fused-plain", "fused-gated", "two-launch-gated"])
+def test_repeatable(fused, gated):
+    """Twelve identical calls give bit-identical outputs: nothing in the
+    launches depends on the order in which their CTAs, warps or copies finish
+    (a race on a shared-memory slot, a TMEM tile, a ready flag or the gate
+    logits' slot, refilled by a tensor-map copy, would show as a difference
+    between calls). The two-launch gated case runs the in-pass gate of the
+    32-column state pass."""
+    spec = PrefillSpec("fused repeat", H=4, d=128, B=2, T=300, init="normal0.1", seed=74)
+    inp = make_prefill(spec)
+    gen = torch.Generator().manual_seed(75)
+    extra = {}
+    if gated:
+        extra = dict(out_gate=torch.randn(inp["v"].shape, generator=gen).to(inp["v"].dtype).cuda(),
+                     norm_weight=(1.0 + 0.5 * torch.randn(inp["v"].shape[-1], generator=gen)).cuda())
+    first, ffin = gpu(inp, fused=fused, **extra)
+    for _ in range(11):
+        out, fin = gpu(inp, fused=fused, **extra)
+        assert torch.equal(out, first) and torch.equal(fin, ffin)
 
 
 def test_too_many_chains_fall_back():
