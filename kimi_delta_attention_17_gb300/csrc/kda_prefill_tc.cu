@@ -75,34 +75,45 @@ constexpr uint32_t kA2Lbo = 2048, kA2Sbo = 128;  // K-major: channel groups adja
 
 // ---------------------------------------------------------------- phase 1
 // Persistent: one CTA of 16 warps per SM walks the (chunk slot, head) items,
-// heads fastest. The raw rows of the next item (q, k bf16 and g fp32: three
-// tensor-map tiles) stream into the staging area while the current item runs
-// its MMAs, solve and stores. Thread (c, blk) owns key/value channel c and the
-// 16-token block blk in the elementwise pass; for TMEM read-back thread t owns
-// lane t mod 128, the four warps of a lane quadrant splitting the columns.
+// heads fastest, as a two-stage pipeline over two items. Warps 0-7 (the
+// elementwise side) take the raw rows of item n + 1 (q, k bf16 and g fp32:
+// three tensor-map tiles in staging) to the MMA operands and the workspace
+// rows that need no solve, then issue its A/H product; meanwhile warps 8-15
+// (the solve side) read back item n's A and H, run the triangular solve and
+// the W product and write the rest of its region. The elementwise pass is
+// bound by instruction issue and the solve by its dependent stages (MMA round
+// trips, barriers, a shuffle chain), so each fills the other's idle issue
+// slots. Elementwise thread (c, hb) owns key/value channel c and the 16-token
+// blocks 2 hb, 2 hb + 1; solve-side warp w reads TMEM lanes 32 (w mod 4) ...
+// What the two sides hand over is double-buffered by item parity: the TMEM
+// accumulators (two 256-column halves), L^T, beta and the steep flag.
 constexpr int kP1Threads = 512;
+constexpr int kP1E = 256, kP1S = 256;   // elementwise side: threads 0-255; solve side: 256-511
+constexpr int kBarE = 1, kBarSv = 2;    // their named barriers
 struct P1 {  // shared-memory offsets, bytes
-    static constexpr int q = 0, k = 16384, g = 49152;  // staging rows of one chunk
-    static constexpr int am = 81920;    // [Ktilde; s Qtilde] bf16, MN-major 128 x 128
-    static constexpr int bm = 114688;   // column versions bf16, MN-major 160 x 128
-    static constexpr int lt = 155648;   // L^T bf16, K-major [channel][token]
-    static constexpr int beta = 188416; // 64 floats
-    static constexpr int bar = 188672;  // mbarriers: staging loaded, MMA done
-    static constexpr int tmem = 188688;
-    static constexpr int exch = 188704; // fp32 [2][4][128]: block totals and local references of G
-    static constexpr int gsc = 192800;  // fp32 [64]: per-head log-decay of the item's tokens
-    static constexpr int fac = 193056;  // fp32 [2 (k, q)][64]: reciprocal norms (q's times the scale)
-    static constexpr int dg = 193568;   // fp32 [2 (A, H)][64][16]: diagonal blocks of steep items
-    static constexpr int bytes = 201760;
-    // Reused once the first MMA has consumed am / bm:
-    static constexpr int As = am;                // fp32 [64][68]: A
-    static constexpr int Ts = am + 17408;        // fp32 [64][68]: T
-    static constexpr int TBs = am + 34816;       // bf16 K-major [i][j]: T Diag(beta)
-    static constexpr int Ms = TBs + 8192;        // fp32 [6][16][kMS]: M_IK = T_II A_IK
-    static constexpr int Rs = Ms + 6 * 16 * 20 * 4;  // fp32 [3][16][kMS]: partial sums of T_IJ
+    static constexpr int q = 0, k = 16384, g = 32768;  // staging rows of one chunk
+    static constexpr int am = 65536;    // [Ktilde; s Qtilde] bf16, MN-major 128 x 128
+    static constexpr int bm = 98304;    // column versions bf16, MN-major 160 x 128
+    static constexpr int lt = 139264;   // [2] L^T bf16, K-major [channel][token], 16 KiB each
+    static constexpr int As = 172032;   // fp32 [64][68]: A; the solve overwrites it with T
+    static constexpr int TBs = 189440;  // bf16 K-major [i][j]: T Diag(beta)
+    static constexpr int Ms = 197632;   // fp32 [6][16][kMS]: M_IK = T_II A_IK
+    static constexpr int Rs = 205312;   // fp32 [3][16][kMS]: partial sums of T_IJ
+    static constexpr int beta = 209152; // fp32 [2][64] by item parity
+    static constexpr int bar = 209664;  // 9 mbarriers (see intra_chunk_body)
+    static constexpr int tmem = 209744;
+    static constexpr int flags = 209760;  // int [2] steep, by item parity; int error flag
+    static constexpr int exch = 209776; // fp32 [2][4][128]: block totals and local references of G
+    static constexpr int gsc = 213872;  // fp32 [64]: per-head log-decay of the item's tokens
+    static constexpr int fac = 214128;  // fp32 [2 (k, q)][64]: reciprocal norms (q's times the scale)
+    static constexpr int dg = 214640;   // fp32 [2 (A, H)][64][16]: diagonal blocks of steep items
+    static constexpr int bytes = 222832;
+    static constexpr int Ts = As;       // T (fp32 [64][68]) takes A's place
 };
 constexpr int kMS = 20;  // row stride (floats) of the M / R blocks: 8 rows hit 8 bank groups
-static_assert(P1::Rs + 3 * 16 * kMS * 4 <= P1::lt, "solve scratch overlaps L^T");
+static_assert(P1::As + 64 * 68 * 4 == P1::TBs && P1::Rs + 3 * 16 * kMS * 4 == P1::beta &&
+              P1::lt + 2 * 16384 == P1::As && P1::dg + 2 * 64 * 16 * 4 == P1::bytes,
+              "phase-1 shared-memory regions are disjoint");
 static_assert(P1::bytes <= 232448, "phase-1 shared memory exceeds 227 KiB");
 constexpr int kAS = 68;  // row stride (floats) of A and T: 16-byte rows, 8 rows hit 8 bank groups
 // Largest total decay, in nats, of one channel over a 16-token block for which
@@ -119,13 +130,22 @@ __device__ __forceinline__ void st16(unsigned char *p, const float *x) {
     *reinterpret_cast<uint4 *>(p) = pack8(x);
 }
 
+// Phase 1 keeps its cumulative log-decays in base-2 units (nats times
+// log2 e), so that every decay factor is one hardware 2^x.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Steep item (kSteepNats): the diagonal 16 x 16 blocks of A and H in fp32,
-// sum_c x_ic k_jc exp(G_ic - G_jc) with the pair decay formed directly (its
+// sum_c x_ic k_jc 2^(G_ic - G_jc) (G in base-2 units) with the pair decay formed directly (its
 // exponent is <= 0 wherever j <= i), into P1::dg as raw sums (the readback
 // applies -beta and the causal masks). Reads the staged q, k rows, the
 // reciprocal norms and the in-block log-decay prefixes that replaced g in
-// staging. Thread (row i, group of 16 channels); the eight groups of a row
-// combine by shuffles. Kept out of line: it runs only for steep items and the
+// staging. Elementwise-side thread t (t < 256): row i = t / 4 and the 32
+// channels of group t mod 4; the four groups of a row combine by shuffles. Kept out of line: it runs only for steep items and the
 // kernel's common path must stay within the instruction cache.
 __device__ __noinline__ void steep_diagonal_blocks(unsigned char *sm, int tid, int len, int l2norm,
                                                    float scale) {
@@ -134,7 +154,7 @@ __device__ __noinline__ void steep_diagonal_blocks(unsigned char *sm, int tid, i
     const float *gG = reinterpret_cast<const float *>(sm + P1::g);
     const float *fac_s = reinterpret_cast<const float *>(sm + P1::fac);
     float *dgA = reinterpret_cast<float *>(sm + P1::dg), *dgH = dgA + 64 * 16;
-    const int i = tid >> 3, cg = tid & 7, i0 = i & ~15;
+    const int i = tid >> 2, cg = tid & 3, i0 = i & ~15;
     const float fki = l2norm ? fac_s[i] : 1.f, fqi = l2norm ? fac_s[C + i] : scale;
 #pragma unroll 1
     for (int jj = 0; jj < 16; ++jj) {
@@ -142,8 +162,8 @@ __device__ __noinline__ void steep_diagonal_blocks(unsigned char *sm, int tid, i
         const float fkj = j < len ? (l2norm ? fac_s[j] : 1.f) : 0.f;
         float a = 0.f, hq = 0.f;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            const int c0 = 16 * cg + 8 * hf;
+        for (int hf = 0; hf < 4; ++hf) {
+            const int c0 = 32 * cg + 8 * hf;
             const uint4 kiw = *reinterpret_cast<const uint4 *>(ks + i * D + c0);
             const uint4 qiw = *reinterpret_cast<const uint4 *>(qs + i * D + c0);
             const uint4 kjw = *reinterpret_cast<const uint4 *>(ks + j * D + c0);
@@ -162,13 +182,13 @@ __device__ __noinline__ void steep_diagonal_blocks(unsigned char *sm, int tid, i
                 const float kie = __uint_as_float((ki[e >> 1] << sh) & 0xFFFF0000u);
                 const float qie = __uint_as_float((qi[e >> 1] << sh) & 0xFFFF0000u);
                 const float kje = __uint_as_float((kj[e >> 1] << sh) & 0xFFFF0000u);
-                const float w = kje * __expf(gi[e] - gj[e]);
+                const float w = kje * ex2(gi[e] - gj[e]);
                 a += kie * w;
                 hq += qie * w;
             }
         }
 #pragma unroll
-        for (int m = 1; m < 8; m <<= 1) {
+        for (int m = 1; m < 4; m <<= 1) {
             a += __shfl_xor_sync(0xffffffffu, a, m);
             hq += __shfl_xor_sync(0xffffffffu, hq, m);
         }
@@ -206,6 +226,20 @@ __device__ __forceinline__ int p1_phys(const P1Walk &wk, int s) {
 
 // Phase 1 for the threads 0 .. kP1Threads - 1 of a CTA (its barriers count
 // exactly those threads, so a larger CTA may run it with the rest idle).
+//
+// Hand-over between the two sides (mbarriers; phase k of a barrier pair
+// [item parity] belongs to item 2 k + parity):
+//   bar_ld       q, k of item n landed in staging (tensor-map copies)
+//   bar_ldg      g of item n landed in staging (issued as soon as the item
+//                before has summed its own, unless that item was steep)
+//   bar_ah[2]    item n's A/H product done: the solve side may read it, the
+//                elementwise side may overwrite the operands (am, bm)
+//   bar_e[2]     the elementwise side is done with item n (beta, the steep
+//                flag, L^T and its workspace rows written)
+//   bar_w        the W product of the solve side's item done
+//   bar_rb       item n's A/H read back (the steep blocks' scratch is free)
+//   bar_sf[2]    the solve side is done with item n: its TMEM half, L^T and
+//                beta slots may take item n + 2
 template <int kVar>
 __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                                                  const CUtensorMap *tm_g, const float *__restrict__ g_head,
@@ -215,25 +249,25 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
                                                  int H, unsigned char *__restrict__ ws,
                                                  int *__restrict__ status, const P1Walk wk) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int c = tid & 127, blk = tid >> 7;  // channel; 16-token block / column group
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint64_t *bar_ld = reinterpret_cast<uint64_t *>(sm + P1::bar);
-    uint64_t *bar_mma = bar_ld + 1;
+    uint64_t *bar_ah = bar_ld + 1;
+    uint64_t *bar_e = bar_ah + 2;
+    uint64_t *bar_w = bar_e + 2;
+    uint64_t *bar_rb = bar_w + 1;
+    uint64_t *bar_sf = bar_rb + 1;
+    uint64_t *bar_ldg = bar_sf + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P1::tmem);
-    float *beta_s = reinterpret_cast<float *>(sm + P1::beta);
+    int *steep_s = reinterpret_cast<int *>(sm + P1::flags);
+    volatile int *err = reinterpret_cast<volatile int *>(sm + P1::flags + 8);
+    float *betas = reinterpret_cast<float *>(sm + P1::beta);
     // Slots [0, used) of the table hold every chunk, in order; the rest are empty.
     const int used = (int)min((long long)*used_slots, nslots);
     // Items are (slot, head) pairs, heads fastest; CTA b takes items b, b + grid,
     // ...: stepping by the grid in (slot, head) form keeps 64-bit divisions off
-    // the item path.
+    // the item path. Both sides walk the same items.
     const int step_s = (int)(wk.count / H), step_h = (int)(wk.count % H);
     auto phys = [&](int s) { return p1_phys(wk, s); };
-    // Fused prefill: the ready flag of the item before, released by thread 0
-    // in the middle of this item's triangular solve. A release waits for the
-    // stores in flight to reach L2; the solve writes only shared memory, and
-    // by then the region writes have drained, so the wait is short (right
-    // after an item's stores it takes an L2 round trip per item).
-    long long flag_prev = -1;  // its index in wk.ready, or -1
     auto advance = [&](int &sl, int &hh) {
         sl += step_s;
         hh += step_h;
@@ -242,141 +276,194 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
             ++sl;
         }
     };
+    // Bounded waits: a completed phase returns at once; otherwise the CTA's
+    // error flag is read first and the wait is skipped once either side has
+    // given up. A timeout raises the flag and the call's status.
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        if (mbar_test(bar, parity)) return true;
+        if (*err) return false;
+        if (!mbar_wait(bar, parity)) {
+            *err = 1;
+            atomicExch(status, (int)KDA_ERR_TIMEOUT);
+            return false;
+        }
+        return true;
+    };
 
-    if (warp == 0) tmem_alloc<256>(tslot);
+    if (warp == 0) tmem_alloc<512>(tslot);
     if (tid == 0) {
         mbar_init(bar_ld, 1);
-        mbar_init(bar_mma, 1);
+        mbar_init(bar_ldg, 1);
+        mbar_init(bar_w, 1);
+        mbar_init(bar_rb, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_ah + b, 1);
+            mbar_init(bar_e + b, 1);
+            mbar_init(bar_sf + b, 1);
+        }
+        *err = 0;
         mbar_fence_init();
     }
     fence_before();
     bar_sync(0, kP1Threads);
     fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    // Operand descriptors, built once: a K step adds a constant to the
-    // address field (byte address / 16), which keeps descriptor arithmetic
-    // off the MMA issue path.
-    const uint64_t d_am = desc(smem_u32(sm + P1::am), kA1Lbo, kA1Sbo);
-    const uint64_t d_bm = desc(smem_u32(sm + P1::bm), kA1Lbo, kA1Sbo);
-    const uint64_t d_lt = desc(smem_u32(sm + P1::lt), kA2Lbo, kA2Sbo);
-    const uint64_t d_tb = desc(smem_u32(sm + P1::TBs), 1024, 128);
 
-    // One thread fetches an item: four 3-D TMA tiles (128 channels x 1 head x
-    // 64 tokens) land as dense [token][channel] rows. Tokens past the end of
-    // the tensor read as zeros; tokens of the next sequence are masked by len.
     if (kVar == kVarChannel) pro = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOG, 0.f, 0};
     if (kVar == kVarScalar) pro = Prologue{KDA_DECAY_SCALAR, KDA_GATE_LOG, 0.f, 0};
     if (kVar == kVarNone) pro = Prologue{KDA_DECAY_NONE, KDA_GATE_LOG, 0.f, 0};
     if (kVar == kVarGated) pro = Prologue{KDA_DECAY_CHANNEL, KDA_GATE_LOGSIGMOID, 0.f, 1};
-    const bool g_tile = pro.decay == KDA_DECAY_CHANNEL;  // g arrives as a tile only per channel
-    auto issue = [&](int hh, const ChunkEntry e) {
-        if (tid != 0) return;
-        mbar_expect_tx(bar_ld, 64u * (2u * 256u + (g_tile ? 512u : 0u)));
-        tma_load_3d(sm + P1::q, tm_q, 0, hh, e.bos, bar_ld);
-        tma_load_3d(sm + P1::k, tm_k, 0, hh, e.bos, bar_ld);
-        if (g_tile) tma_load_3d(sm + P1::g, tm_g, 0, hh, e.bos, bar_ld);
-    };
 
-    // Each item's table entry and beta values are read one item ahead, so
-    // that no global load latency sits on the item's path.
-    auto beta_of = [&](int hh, const ChunkEntry &e) {
-        return tid < C && tid < e.len ? beta[(size_t)(e.bos + tid) * H + hh] : 0.f;
-    };
-    // The per-head decay value of token tid (Gated DeltaNet form), read the
-    // same way; it becomes log a (log_decay) when it is stored for its item.
-    auto ghead_of = [&](int hh, const ChunkEntry &e) {
-        return pro.decay == KDA_DECAY_SCALAR && tid < C && tid < e.len
-                   ? g_head[(size_t)(e.bos + tid) * H + hh]
-                   : 0.f;
-    };
-    int sl = (int)(wk.rank / H), hc = (int)(wk.rank % H);  // this item
-    ChunkEntry ce{};
-    float bcur = 0.f;
-    if (sl < used) {
-        ce = table[phys(sl)];
-        issue(hc, ce);
-        bcur = beta_of(hc, ce);
-        if (pro.decay == KDA_DECAY_SCALAR && tid < C)
-            reinterpret_cast<float *>(sm + P1::gsc)[tid] =
-                tid < ce.len ? log_decay(ghead_of(hc, ce), pro) : 0.f;
-    }
-    int sn = sl, hn = hc;  // the next item
-    advance(sn, hn);
-    ChunkEntry en = sn < used ? table[phys(sn)] : ce;
-    uint32_t ld_phase = 0, mma_phase = 0;
-    bool ok = true;
-    bool steep = false;  // this item takes the steep-decay form
-    while (sl < used) {
-        const int len = ce.len;
-        int snn = sn, hnn = hn;  // the item after next
-        ChunkEntry enn;
-        float bn, gn;
-        unsigned char *reg = ws + ((size_t)phys(sl) * H + hc) * TcRegion::bytes;
-        ok = bar_and(0, kP1Threads, mbar_wait(bar_ld, ld_phase));
-        ld_phase ^= 1;
-        if (!ok) break;
+    if (tid < kP1E) {
+        // ============================================ elementwise side
+        // Channel c and blocks hb, 3 - hb: the earlier a block, the more
+        // column versions it writes, so each thread takes one early and one late.
+        const int c = tid & 127, hb = tid >> 7;
+        // Operand descriptors, built once: a K step adds a constant to the
+        // address field (byte address / 16).
+        const uint64_t d_am = desc(smem_u32(sm + P1::am), kA1Lbo, kA1Sbo);
+        const uint64_t d_bm = desc(smem_u32(sm + P1::bm), kA1Lbo, kA1Sbo);
+        // One thread fetches an item: 3-D TMA tiles (128 channels x 1 head x
+        // 64 tokens) land as dense [token][channel] rows, q and k on one
+        // barrier and g on another. Tokens past the end of the tensor read as
+        // zeros; tokens of the next sequence are masked by len.
+        const bool g_tile = pro.decay == KDA_DECAY_CHANNEL;  // g arrives as a tile only per channel
+        auto issue_qk = [&](int hh, const ChunkEntry e) {
+            mbar_expect_tx(bar_ld, 64u * 2u * 256u);
+            tma_load_3d(sm + P1::q, tm_q, 0, hh, e.bos, bar_ld);
+            tma_load_3d(sm + P1::k, tm_k, 0, hh, e.bos, bar_ld);
+        };
+        auto issue_g = [&](int hh, const ChunkEntry e) {
+            mbar_expect_tx(bar_ldg, 64u * 512u);
+            tma_load_3d(sm + P1::g, tm_g, 0, hh, e.bos, bar_ldg);
+        };
+        // Each item's table entry and beta values are read one item ahead, so
+        // that no global load latency sits on the item's path.
+        auto beta_of = [&](int hh, const ChunkEntry &e) {
+            return tid < C && tid < e.len ? beta[(size_t)(e.bos + tid) * H + hh] : 0.f;
+        };
+        // The per-head decay value of token tid (Gated DeltaNet form), read the
+        // same way; it becomes log a (log_decay) when it is stored for its item.
+        auto ghead_of = [&](int hh, const ChunkEntry &e) {
+            return pro.decay == KDA_DECAY_SCALAR && tid < C && tid < e.len
+                       ? g_head[(size_t)(e.bos + tid) * H + hh]
+                       : 0.f;
+        };
+        float *gs = reinterpret_cast<float *>(sm + P1::g);
+        const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::q);
+        const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::k);
+        float *gsc_s = reinterpret_cast<float *>(sm + P1::gsc);  // written one item ahead
+        float *tot_s = reinterpret_cast<float *>(sm + P1::exch);
+        float *ref_s = tot_s + 4 * D;
+        float *fac_s = reinterpret_cast<float *>(sm + P1::fac);
 
-        // ================= elementwise pass (thread = channel c, block blk of 16 tokens)
-        {
-            const float *gs = reinterpret_cast<const float *>(sm + P1::g);
-            const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::q);
-            const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(sm + P1::k);
-            // Cumulative log-decay of channel c: each thread sums its own block,
-            // keeping the 16 in-block prefixes; block totals and in-block
-            // references (token 7 of each block) are exchanged so that every
-            // thread has the absolute references R_I = G_{16 I + 7} and the chunk
-            // total. In-block factors need only the local prefixes (the block's
-            // offset cancels in G_i - G_r).
-            float *gsc_s = reinterpret_cast<float *>(sm + P1::gsc);  // written one item ahead
-            float G[16];
-            float acc = 0.f;
-            if (pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOG) {
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int tok = 16 * blk + t;
-                    acc += tok < len ? gs[tok * D + c] : 0.f;
-                    G[t] = acc;
+        int sl = (int)(wk.rank / H), hc = (int)(wk.rank % H);  // this item
+        ChunkEntry ce{};
+        float bcur = 0.f;
+        int ld_issued = 0, g_issued = 0, ah_issued = 0;  // copies / products issued (thread 0)
+        bool g_next = false;  // thread 0: the next item's g is on its way
+        if (sl < used) {
+            ce = table[phys(sl)];
+            if (tid == 0) {
+                issue_qk(hc, ce);
+                ld_issued = 1;
+                if (g_tile) {
+                    issue_g(hc, ce);
+                    g_issued = 1;
                 }
-            } else if (pro.decay == KDA_DECAY_CHANNEL) {
-                // Gate logits become log a in registers as they are summed (the
-                // staged g is read nowhere else); the 16 transforms are
-                // independent, so they issue back to back.
-                float gv[16];
+            }
+            bcur = beta_of(hc, ce);
+            if (pro.decay == KDA_DECAY_SCALAR && tid < C)
+                gsc_s[tid] = tid < ce.len ? log_decay(ghead_of(hc, ce), pro) : 0.f;
+        }
+        int sn = sl, hn = hc;  // the next item
+        advance(sn, hn);
+        ChunkEntry en = sn < used ? table[phys(sn)] : ce;
+        bar_sync(kBarE, kP1E);  // the first item's per-head decays
+        int n = 0;              // items done by this side
+        while (sl < used) {
+            const int len = ce.len;
+            const int par = n & 1;
+            int snn = sn, hnn = hn;  // the item after next
+            ChunkEntry enn;
+            float bn, gn;
+            unsigned char *reg = ws + ((size_t)phys(sl) * H + hc) * TcRegion::bytes;
+            if (g_tile) wait(bar_ldg, (uint32_t)par);  // a failure shows in the error flag after the barrier
+            if (pro.l2norm) wait(bar_ld, (uint32_t)par);
+            if (tid == 0) {
+                // Item n - 2's TMEM half, L^T and beta slots, and the operands
+                // item n - 1's product read, are free before anything is written.
+                if (n >= 2) wait(bar_sf + par, (uint32_t)((n - 2) >> 1) & 1);
+                if (n >= 1) wait(bar_ah + (par ^ 1), (uint32_t)((n - 1) >> 1) & 1);
+            }
+
+            // Cumulative log-decay of channel c over each of the thread's two
+            // blocks, kept in registers (G0, G1: in-block prefixes) for the
+            // factor loop, so that staging may take the next item's g as soon
+            // as every thread has summed this one's. Block totals and in-block
+            // references (token 7 of each block) go to the exchange, so that
+            // every thread has the absolute references R_I = G_{16 I + 7} and
+            // the chunk total. In-block factors need only the local prefixes
+            // (the block's offset cancels in G_i - G_r).
+            float G0[16], G1[16], accb[2];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) gv[t] = gs[(16 * blk + t) * D + c];
-                if (pro.gate == KDA_GATE_LOGSIGMOID) {
+            for (int bb = 0; bb < 2; ++bb) {
+                const int b = bb == 0 ? hb : 3 - hb;
+                float *G = bb == 0 ? G0 : G1;
+                float acc = 0.f;
+                if (pro.decay == KDA_DECAY_CHANNEL && pro.gate == KDA_GATE_LOG) {
 #pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        gv[t] = fminf(gv[t], 0.f) - __logf(1.f + __expf(-fabsf(gv[t])));
+                    for (int t = 0; t < 16; ++t) {
+                        const int tok = 16 * b + t;
+                        acc = fmaf(tok < len ? gs[tok * D + c] : 0.f, kLog2e, acc);
+                        G[t] = acc;
+                    }
+                } else if (pro.decay == KDA_DECAY_CHANNEL) {
+                    // Gate logits become log a in registers as they are summed;
+                    // the 16 transforms are independent, so they issue back to back.
+                    float gv[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) gv[t] = gs[(16 * b + t) * D + c];
+                    if (pro.gate == KDA_GATE_LOGSIGMOID) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t)
+                            gv[t] = fminf(gv[t], 0.f) - __logf(1.f + __expf(-fabsf(gv[t])));
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) gv[t] = pro.lower * __fdividef(1.f, 1.f + __expf(-gv[t]));
+                    }
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        acc = fmaf(16 * b + t < len ? gv[t] : 0.f, kLog2e, acc);
+                        G[t] = acc;
+                    }
+                } else if (pro.decay == KDA_DECAY_SCALAR) {
+                    // One decay per head: every channel's prefix is the same.
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        acc = fmaf(gsc_s[16 * b + t], kLog2e, acc);
+                        G[t] = acc;
+                    }
                 } else {
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) gv[t] = pro.lower * __fdividef(1.f, 1.f + __expf(-gv[t]));
+                    for (int t = 0; t < 16; ++t) G[t] = 0.f;
                 }
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    acc += 16 * blk + t < len ? gv[t] : 0.f;
-                    G[t] = acc;
-                }
-            } else {
-#pragma unroll
-                for (int t = 0; t < 16; ++t) G[t] = 0.f;
+                tot_s[b * D + c] = acc;
+                ref_s[b * D + c] = G[7];
+                accb[bb] = acc;
             }
-            float *tot_s = reinterpret_cast<float *>(sm + P1::exch);
-            float *ref_s = tot_s + 4 * D;
-            float *fac_s = reinterpret_cast<float *>(sm + P1::fac);
             if (pro.l2norm) {
                 // Reciprocal norms of k and q per token (the query scale folded
-                // in): four threads per (tensor, token) each sum 32 channels of
+                // in): two threads per (tensor, token) each sum 64 channels of
                 // the staged row, in 16-byte pieces rotated by the token so that
-                // a warp's reads spread over all banks; two shuffles combine them.
-                const int pair = tid >> 2, part = tid & 3;
+                // a warp's reads spread over the banks; one shuffle combines them.
+                const int pair = tid >> 1, part = tid & 1;
                 const int tsr = pair >> 6, tok = pair & 63;  // tensor 0: k, 1: q
                 const __nv_bfloat16 *row = (tsr ? qs : ks) + tok * D;
                 float ss = 0.f;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int piece = 4 * part + ((j + tok) & 3);  // 8 channels
+                for (int j = 0; j < 8; ++j) {
+                    const int piece = 8 * part + ((j + tok) & 7);  // 8 channels
                     const uint4 w = *reinterpret_cast<const uint4 *>(row + 8 * piece);
                     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -386,32 +473,32 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
                     }
                 }
                 ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
                 if (part == 0) fac_s[pair] = rsqrtf(ss + kL2Eps) * (tsr ? scale : 1.f);
             }
-            if (tid < C) beta_s[tid] = bcur;
-            if (pro.decay == KDA_DECAY_SCALAR) {
-                // One decay per head: every channel's prefix is the same.
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    acc += gsc_s[16 * blk + t];
-                    G[t] = acc;
-                }
+            // A block's total decay bounds every factor of its references (the
+            // log-decay is non-increasing within the block); over kSteepNats
+            // anywhere, the whole item takes the steep-decay form (the decision
+            // is uniform over the side). The reads of staged g are ordered
+            // before the copy that may refill it right after this barrier.
+            fence_async_smem();
+            const bool steep =
+                bar_or(kBarE, kP1E, fminf(accb[0], accb[1]) < -kSteepNats * kLog2e) != 0;
+            if (*err) break;
+            // The next item's g, unless a steep item still needs staging's g
+            // rows for its in-block prefixes.
+            if (tid == 0 && g_tile && !steep && sn < used) {
+                issue_g(hn, en);
+                ++g_issued;
+                g_next = true;
             }
-            tot_s[blk * D + c] = acc;
-            ref_s[blk * D + c] = G[7];
-            // The block's total decay bounds every factor of its references
-            // (the log-decay is non-increasing within the block); over
-            // kSteepNats anywhere, the whole item takes the steep-decay form
-            // (the decision is CTA-uniform).
-            steep = bar_or(0, kP1Threads, acc < -kSteepNats) != 0;
             // The table entry of the item after next and the next item's beta,
-            // read here: a CTA barrier waits for its threads' loads, and the next
-            // one is the whole elementwise pass away.
+            // read here: the next barrier is the whole factor pass away.
             advance(snn, hnn);
             enn = snn < used ? table[phys(snn)] : en;
             bn = sn < used ? beta_of(hn, en) : 0.f;
             gn = sn < used ? ghead_of(hn, en) : 0.f;
+            if (tid < C) betas[par * C + tid] = bcur;
+            if (tid == 0) steep_s[par] = steep ? 1 : 0;
             // References of every block for this channel, as cumulative
             // log-decays from the chunk start: rows (K-tilde, Q-tilde, L, Qbar)
             // are scaled relative to Rr, columns (the versions, Kbar) relative
@@ -429,394 +516,489 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
                 off += tt;
             }
             const float Gend = off;
-            // Per-channel block constants (see the header comment): the own
-            // block's references, exp of the row one from the chunk start and
-            // of the column one to the chunk end, and the factors
-            // exp(Rr_I - Rc_blk) of the later blocks' versions (the own block's
-            // version: 1, or 0 in a steep item).
-            const float Rrs = blk == 0 ? Rr[0] : blk == 1 ? Rr[1] : blk == 2 ? Rr[2] : Rr[3];
-            const float Rcs = blk == 0 ? Rc[0] : blk == 1 ? Rc[1] : blk == 2 ? Rc[2] : Rc[3];
-            // The same references relative to the block start.
-            const float Rlr = steep ? 0.f : G[7], Rlc = steep ? G[15] : G[7];
-            const float Ps = __expf(Rrs), Ys = __expf(Gend - Rcs);
-            float Xv[4];
-#pragma unroll
-            for (int I = 0; I < 4; ++I) Xv[I] = I > blk ? __expf(Rr[I] - Rcs) : (steep ? 0.f : 1.f);
-            // A runtime loop over the two 8-token groups (one copy of the body
-            // keeps the kernel within the instruction cache).
+            unsigned char *ltp = sm + P1::lt + par * 16384;
+            if (!pro.l2norm) wait(bar_ld, (uint32_t)par);  // q, k (a failure skips the rest below)
+            if (len < C) {
+                // A ragged chunk: the staged q, k rows past len (the next
+                // sequence's, or zeros past the tensor) are cleared, each thread
+                // its own entries, which are all it reads below.
+                __nv_bfloat16 *qw = reinterpret_cast<__nv_bfloat16 *>(sm + P1::q);
+                __nv_bfloat16 *kw = reinterpret_cast<__nv_bfloat16 *>(sm + P1::k);
 #pragma unroll 1
-            for (int ig = 0; ig < 2; ++ig) {
-                const int i0 = 16 * blk + 8 * ig;  // first token of the group
-                float kv[8], qv[8], E[8], kF[8], t8[8], Gi[8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) Gi[r] = ig ? G[8 + r] : G[r];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int i = i0 + r;
-                    const bool in = i < len;
-                    float fk = 1.f, fq = scale;
-                    if (pro.l2norm) {
-                        fk = fac_s[i];
-                        fq = fac_s[C + i];
-                    }
-                    kv[r] = in ? fk * __bfloat162float(ks[i * D + c]) : 0.f;
-                    qv[r] = in ? fq * __bfloat162float(qs[i * D + c]) : 0.f;
-                    E[r] = __expf(Gi[r] - Rlr);
-                    kF[r] = kv[r] * __expf(Rlc - Gi[r]);
-                }
-#pragma unroll
-                for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r];
-                st16(sm + P1::am + mnmaj(i0, c, kA1Lbo, kA1Sbo), t8);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) t8[r] = qv[r] * E[r];
-                st16(sm + P1::am + mnmaj(64 + i0, c, kA1Lbo, kA1Sbo), t8);
-#pragma unroll
-                for (int I = 0; I < 4; ++I) {
-                    if (I < blk) continue;
-                    const int n0 = 16 * (I * (I + 1) / 2 + blk) + 8 * ig;
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) t8[r] = kF[r] * Xv[I];
-                    st16(sm + P1::bm + mnmaj(n0, c, kA1Lbo, kA1Sbo), t8);
-                }
-#pragma unroll
-                for (int r = 0; r < 8; ++r) t8[r] = kF[r] * Ys;
-                st16(reg + TcRegion::A2 + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r] * Ps;
-                st16(sm + P1::lt + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
-                // s Qbar, rows 0-63 of the state-pass operand [s Qbar; W].
-#pragma unroll
-                for (int r = 0; r < 8; ++r) t8[r] = qv[r] * E[r] * Ps;
-                st16(reg + TcRegion::A1 + mnmaj(i0, c, kA1Lbo, kA1Sbo), t8);
-            }
-            if (blk == 3) reinterpret_cast<float *>(reg + TcRegion::Gam)[c] = __expf(Gend);
-            if (steep) {
-                // Steep item: the in-block log-decay prefixes replace g in
-                // staging (each thread its own entries), then the diagonal
-                // blocks are formed directly.
-                float *gG = reinterpret_cast<float *>(sm + P1::g);
-#pragma unroll
-                for (int t = 0; t < 16; ++t) gG[(16 * blk + t) * D + c] = G[t];
-                bar_sync(0, kP1Threads);
-                steep_diagonal_blocks(sm, tid, len, pro.l2norm, scale);
-            }
-        }
-        fence_async_smem();
-        fence_before();
-        bar_sync(0, kP1Threads);
-        fence_after();
-
-        // ================= A / H = gated K K^T and Q K^T (M=128, N=160, K=128)
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16(128, 160, 1, 1);
-#pragma unroll
-            for (int s = 0; s < D / 16; ++s)
-                mma_bf16(tmem, d_am + s * (2 * kA1Lbo >> 4), d_bm + s * (2 * kA1Lbo >> 4), id, s > 0);
-            commit(bar_mma);
-        }
-        // The staging rows are consumed: fetch the next item's while this one runs.
-        if (sn < used) issue(hn, en);
-        ok = bar_and(0, kP1Threads, mbar_wait(bar_mma, mma_phase));
-        mma_phase ^= 1;
-        fence_after();
-        if (!ok) break;
-        {
-            float *As = reinterpret_cast<float *>(sm + P1::As);
-            unsigned char *Hs = reg + TcRegion::HT;  // H goes straight to the workspace (rows 0-63)
-            const int lr = tid & 127, i = lr & 63, Iblk = i >> 4;
-            const bool isH = lr >= 64;
-            const int grp = warp >> 2;           // which of the quadrant's four warps
-            const bool upper = (warp & 1) != 0;  // rows 32-63: blocks 2, 3
-            const float bi = beta_s[i];
-            // Versions of this warp's rows (blocks 0-1: versions 0-2; blocks 2-3:
-            // versions 3-9), split among the quadrant's four warps; a runtime
-            // loop keeps the code small enough for the instruction cache.
-            const int v0 = upper ? 3 + 2 * grp : grp;
-            const int nv = upper ? (grp < 3 ? 2 : 1) : (grp < 3 ? 1 : 0);
-#pragma unroll 1
-            for (int k = 0; k < nv; ++k) {
-                const int vv = v0 + k;  // warp-uniform
-                float x[16];
-                tmem_ld16(tmem + lane_base + vv * 16, x);
-                tmem_wait_ld();
-                if (ver_I(vv) != Iblk) continue;
-                const int J = ver_J(vv);
-                if (steep && J == Iblk) {  // formed directly in the elementwise pass
-                    const float *src = reinterpret_cast<const float *>(sm + P1::dg) + (isH ? 64 * 16 : 0) + i * 16;
-#pragma unroll
-                    for (int f = 0; f < 4; ++f) {
-                        const float4 d4 = *reinterpret_cast<const float4 *>(src + 4 * f);
-                        x[4 * f] = d4.x; x[4 * f + 1] = d4.y; x[4 * f + 2] = d4.z; x[4 * f + 3] = d4.w;
-                    }
-                }
-                if (!isH) {
-#pragma unroll
-                    for (int f = 0; f < 4; ++f) {
-                        float a4[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int j = 16 * J + 4 * f + e;
-                            a4[e] = j < i ? -bi * x[4 * f + e] : 0.f;
+                for (int bb = 0; bb < 2; ++bb) {
+                    const int b = bb == 0 ? hb : 3 - hb;
+                    for (int t = 16 * b; t < 16 * b + 16; ++t)
+                        if (t >= len) {
+                            qw[t * D + c] = __float2bfloat16(0.f);
+                            kw[t * D + c] = __float2bfloat16(0.f);
                         }
-                        *reinterpret_cast<float4 *>(As + i * kAS + 16 * J + 4 * f) =
-                            make_float4(a4[0], a4[1], a4[2], a4[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        float t8[8];
-#pragma unroll
-                        for (int r = 0; r < 8; ++r) t8[r] = (16 * J + 8 * hf + r <= i) ? x[8 * hf + r] : 0.f;
-                        st16(Hs + kmaj(i, 16 * J + 8 * hf, kA2Lbo, kA2Sbo), t8);
-                    }
                 }
             }
-            if (grp == 3) {
+            // Runtime loops over the thread's two blocks and their two 8-token
+            // groups (one copy of the body keeps the kernel within the
+            // instruction cache).
+#pragma unroll 1
+            for (int bb = 0; bb < 2; ++bb) {
+                const int b = bb == 0 ? hb : 3 - hb;
+                // Per-block constants: the block's references, exp of the row
+                // one from the chunk start and of the column one to the chunk
+                // end, and the factors exp(Rr_I - Rc_b) of the later blocks'
+                // versions (the own block's version: 1, or 0 in a steep item).
+                const float Rrs = b == 0 ? Rr[0] : b == 1 ? Rr[1] : b == 2 ? Rr[2] : Rr[3];
+                const float Rcs = b == 0 ? Rc[0] : b == 1 ? Rc[1] : b == 2 ? Rc[2] : Rc[3];
+                // The same references relative to the block start.
+                const float refb = bb ? G1[7] : G0[7], totb = bb ? G1[15] : G0[15];
+                const float Rlr = steep ? 0.f : refb, Rlc = steep ? totb : refb;
+                // (The query scale s rides on the s Qbar rows' factor; the
+                // solve side applies it to H.)
+                const float Ps = ex2(Rrs), Ys = ex2(Gend - Rcs), PsQ = Ps * (pro.l2norm ? 1.f : scale);
+                float Xv[4];
 #pragma unroll
-                for (int J = 0; J < 4; ++J) {
-                    if (J <= Iblk) continue;
+                for (int I = 0; I < 4; ++I) Xv[I] = I > b ? ex2(Rr[I] - Rcs) : (steep ? 0.f : 1.f);
+#pragma unroll 1
+                for (int ig = 0; ig < 2; ++ig) {
+                    const int i0 = 16 * b + 8 * ig;  // first token of the group
+                    float kv[8], qv[8], E[8], kF[8], t8[8], Gi[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        Gi[r] = bb ? (ig ? G1[8 + r] : G1[r]) : (ig ? G0[8 + r] : G0[r]);
+                    if (steep) {
+                        // The in-block log-decay prefixes replace g in staging
+                        // (each thread its own entries) for the diagonal blocks.
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) gs[(i0 + r) * D + c] = Gi[r];
+                    }
+                    // Staged rows past len are zero (see above), so no masks here.
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int i = i0 + r;
+                        kv[r] = __bfloat162float(ks[i * D + c]);
+                        qv[r] = __bfloat162float(qs[i * D + c]);
+                        if (pro.l2norm) {
+                            kv[r] *= fac_s[i];
+                            qv[r] *= fac_s[C + i];
+                        }
+                        E[r] = ex2(Gi[r] - Rlr);
+                        kF[r] = kv[r] * ex2(Rlc - Gi[r]);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r];
+                    st16(sm + P1::am + mnmaj(i0, c, kA1Lbo, kA1Sbo), t8);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) t8[r] = qv[r] * E[r];
+                    st16(sm + P1::am + mnmaj(64 + i0, c, kA1Lbo, kA1Sbo), t8);
+#pragma unroll
+                    for (int I = 0; I < 4; ++I) {
+                        if (I < b) continue;
+                        const int n0 = 16 * (I * (I + 1) / 2 + b) + 8 * ig;
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) t8[r] = kF[r] * Xv[I];
+                        st16(sm + P1::bm + mnmaj(n0, c, kA1Lbo, kA1Sbo), t8);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) t8[r] = kF[r] * Ys;
+                    st16(reg + TcRegion::A2 + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) t8[r] = kv[r] * E[r] * Ps;
+                    st16(ltp + kmaj(c, i0, kA2Lbo, kA2Sbo), t8);
+                    // s Qbar, rows 0-63 of the state-pass operand [s Qbar; W].
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) t8[r] = qv[r] * E[r] * PsQ;
+                    st16(reg + TcRegion::A1 + mnmaj(i0, c, kA1Lbo, kA1Sbo), t8);
+                }
+            }
+            if (hb == 0) reinterpret_cast<float *>(reg + TcRegion::Gam)[c] = ex2(Gend);
+            if (steep) {
+                // Steep item: the diagonal blocks formed directly, once the
+                // solve side has read back the previous item's.
+                if (tid == 0 && n >= 1) wait(bar_rb, (uint32_t)(n - 1) & 1);
+                bar_sync(kBarE, kP1E);
+                steep_diagonal_blocks(sm, tid, len, pro.l2norm, pro.l2norm ? scale : 1.f);
+            }
+            // The next item's per-head log-decays (this item's were read above).
+            if (pro.decay == KDA_DECAY_SCALAR && tid < C)
+                gsc_s[tid] = sn < used && tid < en.len ? log_decay(gn, pro) : 0.f;
+            // The operands (and this side's reads of staging) are ordered before
+            // the product and the copies that refill staging.
+            fence_async_smem();
+            bar_sync(kBarE, kP1E);
+            if (tid == 0 && !*err) {
+                fence_after();
+                if (sn < used) {
+                    issue_qk(hn, en);
+                    ++ld_issued;
+                    if (g_tile && !g_next) {
+                        issue_g(hn, en);
+                        ++g_issued;
+                    }
+                }
+                g_next = false;
+                // A / H = gated K K^T and Q K^T (M=128, N=160, K=128) into this
+                // item's TMEM half.
+                const uint32_t id = idesc_bf16(128, 160, 1, 1);
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s)
+                    mma_bf16(tmem + (uint32_t)(par * 256), d_am + s * (2 * kA1Lbo >> 4),
+                             d_bm + s * (2 * kA1Lbo >> 4), id, s > 0);
+                commit(bar_ah + par);
+                ++ah_issued;
+                mbar_arrive(bar_e + par);
+            }
+            ++n;
+            sl = sn;
+            hc = hn;
+            ce = en;
+            sn = snn;
+            hn = hnn;
+            en = enn;
+            bcur = bn;
+        }
+        if (tid == 0) {
+            // Bounded waits for copies and products that may still be in flight
+            // after an error (at once otherwise).
+            if (ld_issued > 0) mbar_wait(bar_ld, (uint32_t)(ld_issued - 1) & 1);
+            if (g_issued > 0) mbar_wait(bar_ldg, (uint32_t)(g_issued - 1) & 1);
+            if (ah_issued >= 1) mbar_wait(bar_ah + ((ah_issued - 1) & 1), (uint32_t)((ah_issued - 1) >> 1) & 1);
+        }
+    } else {
+        // ============================================ solve side
+        const int st = tid - kP1E, sw = st >> 5;  // thread and warp within the side
+        const int quad = warp & 3;                // TMEM lane quadrant of this warp
+        const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+        const uint64_t d_lt = desc(smem_u32(sm + P1::lt), kA2Lbo, kA2Sbo);
+        const uint64_t d_tb = desc(smem_u32(sm + P1::TBs), 1024, 128);
+        float *As = reinterpret_cast<float *>(sm + P1::As);
+        float *Ts = reinterpret_cast<float *>(sm + P1::Ts);
+        float *Ms = reinterpret_cast<float *>(sm + P1::Ms);
+        float *Rs = reinterpret_cast<float *>(sm + P1::Rs);
+        int sl = (int)(wk.rank / H), hc = (int)(wk.rank % H);
+        int n = 0, w_issued = 0;
+        // Fused prefill: the ready flag of the item before, released by the
+        // side's first thread in the middle of this item's solve. A release
+        // waits for the stores in flight to reach L2; the solve writes only
+        // shared memory, and by then the region writes have drained, so the
+        // wait is short (right after an item's stores it takes an L2 round
+        // trip per item).
+        long long flag_prev = -1;  // its index in wk.ready, or -1
+        while (sl < used) {
+            const int par = n & 1;
+            unsigned char *reg = ws + ((size_t)phys(sl) * H + hc) * TcRegion::bytes;
+            const uint32_t tb = tmem + (uint32_t)(par * 256);
+            wait(bar_e + par, (uint32_t)(n >> 1) & 1);
+            wait(bar_ah + par, (uint32_t)(n >> 1) & 1);
+            fence_after();
+            __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane waits
+            const bool steep = steep_s[par] != 0;
+            const float *beta_n = betas + par * C;
+
+            // ================= read back A (rows 0-63) and H (rows 64-127)
+            {
+                unsigned char *Hs = reg + TcRegion::HT;  // H goes straight to the workspace (rows 0-63)
+                const int lr = 32 * quad + lane, i = lr & 63, Iblk = i >> 4;
+                const bool isH = lr >= 64;
+                const int g2 = sw >> 2;               // which of the quadrant's two warps
+                const bool upper = (quad & 1) != 0;   // rows 32-63: blocks 2, 3
+                const float bi = beta_n[i];
+                // The query scale s (not applied to the staged Q-tilde rows unless
+                // the normalisation folded it into q's norm factor).
+                const float hsc = pro.l2norm ? 1.f : scale;
+                // Versions of this warp's rows (blocks 0-1: versions 0-2; blocks
+                // 2-3: versions 3-9), split between the quadrant's two warps; a
+                // runtime loop keeps the code small enough for the instruction cache.
+                const int v0 = upper ? (g2 ? 7 : 3) : (g2 ? 2 : 0);
+                const int nv = upper ? (g2 ? 3 : 4) : (g2 ? 1 : 2);
+#pragma unroll 1
+                for (int k = 0; k < nv; ++k) {
+                    const int vv = v0 + k;  // warp-uniform
+                    float x[16];
+                    tmem_ld16(tb + lane_base + vv * 16, x);
+                    tmem_wait_ld();
+                    if (ver_I(vv) != Iblk) continue;
+                    const int J = ver_J(vv);
+                    if (steep && J == Iblk) {  // formed directly in the elementwise pass
+                        const float *src = reinterpret_cast<const float *>(sm + P1::dg) + (isH ? 64 * 16 : 0) + i * 16;
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) {
+                            const float4 d4 = *reinterpret_cast<const float4 *>(src + 4 * f);
+                            x[4 * f] = d4.x; x[4 * f + 1] = d4.y; x[4 * f + 2] = d4.z; x[4 * f + 3] = d4.w;
+                        }
+                    }
                     if (!isH) {
 #pragma unroll
-                        for (int f = 0; f < 4; ++f)
+                        for (int f = 0; f < 4; ++f) {
+                            float a4[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int j = 16 * J + 4 * f + e;
+                                a4[e] = j < i ? -bi * x[4 * f + e] : 0.f;
+                            }
                             *reinterpret_cast<float4 *>(As + i * kAS + 16 * J + 4 * f) =
-                                make_float4(0.f, 0.f, 0.f, 0.f);
+                                make_float4(a4[0], a4[1], a4[2], a4[3]);
+                        }
                     } else {
-                        const uint4 z = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J, kA2Lbo, kA2Sbo)) = z;
-                        *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J + 8, kA2Lbo, kA2Sbo)) = z;
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            float t8[8];
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) t8[r] = (16 * J + 8 * hf + r <= i) ? hsc * x[8 * hf + r] : 0.f;
+                            st16(Hs + kmaj(i, 16 * J + 8 * hf, kA2Lbo, kA2Sbo), t8);
+                        }
+                    }
+                }
+                if (g2 == 1) {
+#pragma unroll
+                    for (int J = 0; J < 4; ++J) {
+                        if (J <= Iblk) continue;
+                        if (!isH) {
+#pragma unroll
+                            for (int f = 0; f < 4; ++f)
+                                *reinterpret_cast<float4 *>(As + i * kAS + 16 * J + 4 * f) =
+                                    make_float4(0.f, 0.f, 0.f, 0.f);
+                        } else {
+                            const uint4 z = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J, kA2Lbo, kA2Sbo)) = z;
+                            *reinterpret_cast<uint4 *>(Hs + kmaj(i, 16 * J + 8, kA2Lbo, kA2Sbo)) = z;
+                        }
                     }
                 }
             }
-        }
-        fence_before();
-        bar_sync(0, kP1Threads);
+            fence_before();
+            bar_sync(kBarSv, kP1S);
+            if (*err) break;
+            if (st == 0) mbar_arrive(bar_rb);
 
-        // ================= T = (I - A)^{-1}, then T Diag(beta) as a bf16 operand.
-        {
-            const float *As = reinterpret_cast<const float *>(sm + P1::As);
-            float *Ts = reinterpret_cast<float *>(sm + P1::Ts);
-            float *Ms = reinterpret_cast<float *>(sm + P1::Ms);
-            float *Rs = reinterpret_cast<float *>(sm + P1::Rs);
-            // Block row I of the substitution (I - A_II) X = [A_I0 .. A_I,I-1 | I]
-            // gives M_IK = T_II A_IK (K < I) and T_II = (I - A_II)^{-1} together:
-            // 16 (I + 1) right-hand columns, 160 in all, two per group of four
-            // threads; each thread owns rows sub, sub + 4, sub + 8, sub + 12 of its
-            // two columns. Once x_r is final its owner broadcasts it (one shuffle
-            // per column) and every thread pushes it into its later rows, so the
-            // dependent chain is one shuffle and one FMA per row.
-            if (tid < 320) {
-                const int pr2 = tid >> 2, sub = tid & 3;  // column pair; warps never span two block rows
-                const int I = pr2 < 8 ? 0 : pr2 < 24 ? 1 : pr2 < 48 ? 2 : 3;
-                const int cc = 2 * (pr2 - 4 * I * (I + 1));  // first column, in [0, 16 (I + 1))
-                const float *Ab = As + 16 * I * kAS + 16 * I;
-                // This thread's rows of A_II, loaded before the dependent chain
-                // (a[q][r] = A_II[4 q + sub][r], r < 4 q + sub; the rest unused).
-                float a[4][16];
+            // ================= T = (I - A)^{-1}, then T Diag(beta) as a bf16 operand.
+            {
+                // Block row I of the substitution (I - A_II) X = [A_I0 .. A_I,I-1 | I]
+                // gives M_IK = T_II A_IK (K < I) and T_II = (I - A_II)^{-1} together:
+                // 16 (I + 1) right-hand columns, 160 in all, four per group of four
+                // threads (threads 0-159 of the side); each thread owns rows sub,
+                // sub + 4, sub + 8, sub + 12 of its four columns. Once x_r is final
+                // its owner broadcasts it (one shuffle per column) and every thread
+                // pushes it into its later rows, so the dependent chain is one
+                // shuffle and one FMA per row. T_II is written over A_II, so
+                // every read of A precedes a barrier before the first write.
+                const bool act = st < 160;  // whole warps
+                const int g4 = st >> 2, sub = st & 3;
+                const int I = g4 < 4 ? 0 : g4 < 12 ? 1 : g4 < 24 ? 2 : 3;
+                const int cc = 4 * (g4 - (I == 0 ? 0 : I == 1 ? 4 : I == 2 ? 12 : 24));  // in [0, 16 (I + 1))
+                const bool rhs_a = cc < 16 * I;  // columns of A_IK (K < I), or of the identity
+                float a[4][16], xs[4][4];
+                if (act) {
+                    const float *Ab = As + 16 * I * kAS + 16 * I;
+                    // This thread's rows of A_II (a[q][r] = A_II[4 q + sub][r],
+                    // r < 4 q + sub; the rest unused).
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+                    for (int q = 0; q < 4; ++q)
 #pragma unroll
-                    for (int r4 = 0; r4 < 16; r4 += 4) {
-                        if (r4 < 4 * q + 3) {
-                            const float4 t = *reinterpret_cast<const float4 *>(Ab + (4 * q + sub) * kAS + r4);
-                            a[q][r4] = t.x; a[q][r4 + 1] = t.y; a[q][r4 + 2] = t.z; a[q][r4 + 3] = t.w;
+                        for (int r4 = 0; r4 < 16; r4 += 4) {
+                            if (r4 < 4 * q + 3) {
+                                const float4 t = *reinterpret_cast<const float4 *>(Ab + (4 * q + sub) * kAS + r4);
+                                a[q][r4] = t.x; a[q][r4 + 1] = t.y; a[q][r4 + 2] = t.z; a[q][r4 + 3] = t.w;
+                            }
                         }
-                    }
-                // Right-hand sides: columns of A_IK (K < I), or of the identity.
-                const bool rhs_a = cc < 16 * I;
-                float x0[4], x1[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int row = 4 * q + sub;
-                    if (rhs_a) {
-                        const float2 t = *reinterpret_cast<const float2 *>(As + (16 * I + row) * kAS + cc);
-                        x0[q] = t.x;
-                        x1[q] = t.y;
-                    } else {
-                        x0[q] = row == cc - 16 * I ? 1.f : 0.f;
-                        x1[q] = row == cc + 1 - 16 * I ? 1.f : 0.f;
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < 15; ++r) {
-                    const int src = (tid & 31 & ~3) | (r & 3);
-                    const float xr0 = __shfl_sync(0xffffffffu, x0[r >> 2], src);
-                    const float xr1 = __shfl_sync(0xffffffffu, x1[r >> 2], src);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        if (4 * q + 3 > r && 4 * q + sub > r) {
-                            x0[q] += a[q][r] * xr0;
-                            x1[q] += a[q][r] * xr1;
+                        const int row = 4 * q + sub;
+                        if (rhs_a) {
+                            const float4 t = *reinterpret_cast<const float4 *>(As + (16 * I + row) * kAS + cc);
+                            xs[0][q] = t.x; xs[1][q] = t.y; xs[2][q] = t.z; xs[3][q] = t.w;
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) xs[k][q] = row == cc + k - 16 * I ? 1.f : 0.f;
                         }
                     }
                 }
+                bar_sync(kBarSv, kP1S);
+                if (act) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int row = 4 * q + sub;
-                    float *dst = rhs_a ? Ms + (I * (I - 1) / 2 + (cc >> 4)) * 16 * kMS + row * kMS + (cc & 15)
-                                       : Ts + (16 * I + row) * kAS + cc;
-                    *reinterpret_cast<float2 *>(dst) = make_float2(x0[q], x1[q]);
+                    for (int r = 0; r < 15; ++r) {
+                        const int src = (lane & ~3) | (r & 3);
+                        float xr[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) xr[k] = __shfl_sync(0xffffffffu, xs[k][r >> 2], src);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (4 * q + 3 > r && 4 * q + sub > r) {
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) xs[k][q] += a[q][r] * xr[k];
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int row = 4 * q + sub;
+                        float *dst = rhs_a ? Ms + (I * (I - 1) / 2 + (cc >> 4)) * 16 * kMS + row * kMS + (cc & 15)
+                                           : Ts + (16 * I + row) * kAS + cc;
+                        *reinterpret_cast<float4 *>(dst) = make_float4(xs[0][q], xs[1][q], xs[2][q], xs[3][q]);
+                    }
                 }
             }
-            bar_sync(0, kP1Threads);
-            if (wk.ready && tid == 0 && flag_prev >= 0) {
+            bar_sync(kBarSv, kP1S);
+            if (wk.ready && st == 0 && flag_prev >= 0) {
                 st_release_gpu(wk.ready + flag_prev, 1);
                 flag_prev = -1;
             }
-            // Off-diagonal blocks: with M_IK = T_II A_IK (K < I), block row I of
-            // (I - A) T = I gives T_IJ = sum_{K = J}^{I - 1} M_IK T_KJ. The
-            // substitution above formed the six M blocks; stage 2 forms the first
-            // subdiagonal and the terms of the lower blocks that need only T_JJ;
-            // stages 3 and 4 finish the second and third subdiagonals. Each thread
-            // computes a 1 x 4 strip (row r, columns 4 cg .. 4 cg + 3) of one
-            // 16 x 16 product.
-            auto mi = [](int I, int K) { return I * (I - 1) / 2 + K; };  // M block index, K < I
-            // acc += P (16 x 16, row stride ps) row r  x  Q (16 x 16, row stride qs) columns 4 cg ..
-            auto prod = [](float4 acc, const float *P, int ps, const float *Q, int qs, int r, int cg) {
+            {
+                // Off-diagonal blocks: with M_IK = T_II A_IK (K < I), block row I of
+                // (I - A) T = I gives T_IJ = sum_{K = J}^{I - 1} M_IK T_KJ. The
+                // substitution above formed the six M blocks. Written out,
+                //   T_10 = M_10 T_00,  T_21 = M_21 T_11,  T_32 = M_32 T_22,
+                //   T_20 = M_20 T_00 + M_21 T_10,
+                //   T_31 = (M_31 + M_32 M_21) T_11,
+                //   T_30 = (M_30 + M_32 M_20) T_00 + (M_31 + M_32 M_21) T_10,
+                // so two dependent levels suffice: level 1 forms T_10, T_21, T_32,
+                // R = M_20 T_00, U = M_30 + M_32 M_20 and V = M_31 + M_32 M_21
+                // (six warps, one 16 x 16 product each, a 1 x 8 strip per thread:
+                // row r, columns 8 hf .. 8 hf + 7); level 2 forms T_20 = R + M_21
+                // T_10, T_31 = V T_11 and T_30 = U T_00 + V T_10 (four warps; T_30's
+                // two products split by columns over two warps, 1 x 4 strips).
+                auto mi = [](int I, int K) { return I * (I - 1) / 2 + K; };  // M block index, K < I
+                auto Tb = [&](int I, int J) { return Ts + 16 * I * kAS + 16 * J; };
+                auto Mb = [&](int I, int K) { return Ms + mi(I, K) * 16 * kMS; };
+                float *Rb = Rs, *Ub = Rs + 16 * kMS, *Vb = Rs + 2 * 16 * kMS;
+                // acc[0 .. 4 nq) += P (16 x 16, row stride kMS) row r x Q (row
+                // stride qs) columns c0 .. c0 + 4 nq - 1; every load before the FMAs.
+                auto prod = [](float *acc, const float *P, const float *Q, int qs, int r, int c0, int nq) {
 #pragma unroll
-                for (int h8 = 0; h8 < 16; h8 += 8) {
-                    // Eight rows of Q and the matching eight entries of P's row,
-                    // all loaded before the FMAs that consume them.
-                    float pm[8];
-                    float4 qv[8];
+                    for (int h8 = 0; h8 < 16; h8 += 8) {
+                        float pm[8];
+                        float4 qv[8][2];
 #pragma unroll
-                    for (int m0 = 0; m0 < 8; m0 += 4) {
-                        const float4 pv = *reinterpret_cast<const float4 *>(P + r * ps + h8 + m0);
-                        pm[m0] = pv.x; pm[m0 + 1] = pv.y; pm[m0 + 2] = pv.z; pm[m0 + 3] = pv.w;
+                        for (int m0 = 0; m0 < 8; m0 += 4) {
+                            const float4 pv = *reinterpret_cast<const float4 *>(P + r * kMS + h8 + m0);
+                            pm[m0] = pv.x; pm[m0 + 1] = pv.y; pm[m0 + 2] = pv.z; pm[m0 + 3] = pv.w;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+#pragma unroll
+                            for (int u = 0; u < 2; ++u)
+                                if (u < nq) qv[e][u] = *reinterpret_cast<const float4 *>(Q + (h8 + e) * qs + c0 + 4 * u);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+#pragma unroll
+                            for (int u = 0; u < 2; ++u)
+                                if (u < nq) {
+                                    acc[4 * u] += pm[e] * qv[e][u].x; acc[4 * u + 1] += pm[e] * qv[e][u].y;
+                                    acc[4 * u + 2] += pm[e] * qv[e][u].z; acc[4 * u + 3] += pm[e] * qv[e][u].w;
+                                }
                     }
+                };
+                const int r = lane >> 1, hf = lane & 1;
+                {   // level 1: warps 0-5
+                    const float *P = nullptr, *Q = nullptr, *init = nullptr;
+                    float *dst = nullptr;
+                    int qs = kAS, ds = kAS;
+                    switch (sw) {
+                        case 0: P = Mb(1, 0); Q = Tb(0, 0); dst = Tb(1, 0); break;
+                        case 1: P = Mb(2, 1); Q = Tb(1, 1); dst = Tb(2, 1); break;
+                        case 2: P = Mb(3, 2); Q = Tb(2, 2); dst = Tb(3, 2); break;
+                        case 3: P = Mb(2, 0); Q = Tb(0, 0); dst = Rb; ds = kMS; break;
+                        case 4: P = Mb(3, 2); Q = Mb(2, 0); qs = kMS; init = Mb(3, 0); dst = Ub; ds = kMS; break;
+                        case 5: P = Mb(3, 2); Q = Mb(2, 1); qs = kMS; init = Mb(3, 1); dst = Vb; ds = kMS; break;
+                        default: break;
+                    }
+                    if (sw < 6) {
+                        float acc[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        qv[e] = *reinterpret_cast<const float4 *>(Q + (h8 + e) * qs + 4 * cg);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc.x += pm[e] * qv[e].x; acc.y += pm[e] * qv[e].y;
-                        acc.z += pm[e] * qv[e].z; acc.w += pm[e] * qv[e].w;
+                        for (int j = 0; j < 8; ++j) acc[j] = init ? init[r * kMS + 8 * hf + j] : 0.f;
+                        prod(acc, P, Q, qs, r, 8 * hf, 2);
+                        *reinterpret_cast<float4 *>(dst + r * ds + 8 * hf) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                        *reinterpret_cast<float4 *>(dst + r * ds + 8 * hf + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
                     }
                 }
-                return acc;
-            };
-            const int pr = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;  // product index, strip
-            const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            auto Tb = [&](int I, int J) { return Ts + 16 * I * kAS + 16 * J; };
-            auto Mb = [&](int I, int K) { return Ms + mi(I, K) * 16 * kMS; };
-            auto put = [](float *B, int stride, int r, int cg, float4 v) {
-                *reinterpret_cast<float4 *>(B + r * stride + 4 * cg) = v;
-            };
-            // Stage 2: T_10, T_21, T_32 = M_{J+1,J} T_JJ; R_20 = M_20 T_00,
-            //          R_31 = M_31 T_11, R_30 = M_30 T_00.
-            // Stage 3: T_20 = R_20 + M_21 T_10, T_31 = R_31 + M_32 T_21; R_30 += M_31 T_10.
-            // Stage 4: T_30 = R_30 + M_32 T_20.
-            // One runtime loop picks each stage's operands and expands a single
-            // product (the kernel must stay within the instruction cache).
-#pragma unroll 1
-            for (int stg = 1; stg < 4; ++stg) {
-                const int nprod = stg == 1 ? 6 : stg == 2 ? 3 : 1;
-                if (pr < nprod) {
-                    const float *P, *Q;
-                    float *dst;
-                    int ps, qs = kAS, ds;
-                    const float *init = nullptr;  // partial sum to start from (R block)
-                    if (stg == 1) {
-                        const int J = pr < 3 ? pr : pr < 5 ? pr - 3 : 0;
-                        const int I = pr < 3 ? J + 1 : pr < 5 ? J + 2 : 3;
-                        P = Mb(I, J); ps = kMS;
-                        Q = Tb(J, J);
-                        dst = pr < 3 ? Tb(I, J) : Rs + (pr - 3) * 16 * kMS;
-                        ds = pr < 3 ? kAS : kMS;
-                    } else if (stg == 2) {
-                        const int J = pr < 2 ? pr : 0;
-                        const int I = pr < 2 ? J + 2 : 3, K = pr < 2 ? J + 1 : 1;
-                        P = Mb(I, K); ps = kMS;
-                        Q = Tb(K, J);
-                        init = Rs + pr * 16 * kMS;
-                        dst = pr < 2 ? Tb(I, J) : Rs + pr * 16 * kMS;
-                        ds = pr < 2 ? kAS : kMS;
-                    } else {
-                        P = Mb(3, 2); ps = kMS;
-                        Q = Tb(2, 0);
-                        init = Rs + 2 * 16 * kMS;
-                        dst = Tb(3, 0); ds = kAS;
-                    }
-                    const float4 a0 = init ? *reinterpret_cast<const float4 *>(init + r * kMS + 4 * cg) : z4;
-                    put(dst, ds, r, cg, prod(a0, P, ps, Q, qs, r, cg));
+                bar_sync(kBarSv, kP1S);
+                if (sw < 2) {  // level 2: T_20 (warp 0), T_31 (warp 1)
+                    float acc[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = sw == 0 ? Rb[r * kMS + 8 * hf + j] : 0.f;
+                    if (sw == 0) prod(acc, Mb(2, 1), Tb(1, 0), kAS, r, 8 * hf, 2);
+                    else prod(acc, Vb, Tb(1, 1), kAS, r, 8 * hf, 2);
+                    float *dst = sw == 0 ? Tb(2, 0) : Tb(3, 1);
+                    *reinterpret_cast<float4 *>(dst + r * kAS + 8 * hf) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    *reinterpret_cast<float4 *>(dst + r * kAS + 8 * hf + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                } else if (sw < 4) {  // level 2: T_30 columns 8 (sw - 2) .. + 7, a 1 x 4 strip per thread
+                    const int c0 = 8 * (sw - 2) + 4 * hf;
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                    prod(acc, Ub, Tb(0, 0), kAS, r, c0, 1);
+                    prod(acc, Vb, Tb(1, 0), kAS, r, c0, 1);
+                    *reinterpret_cast<float4 *>(Tb(3, 0) + r * kAS + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 }
-                bar_sync(0, kP1Threads);
+                bar_sync(kBarSv, kP1S);
             }
             {
-                // Row i, columns jb .. jb + 7 of T Diag(beta): one 16-byte run per thread.
-                const int i = tid & 63, jb = 8 * (tid >> 6);
-                float t8[8];
+                // Row i, columns jb .. jb + 15 of T Diag(beta): two 16-byte runs per thread,
+                const int i = st & 63, jb = 16 * (st >> 6);
 #pragma unroll
-                for (int f = 0; f < 2; ++f) {
-                    const float4 t = *reinterpret_cast<const float4 *>(Ts + i * kAS + jb + 4 * f);
-                    const float tv[4] = {t.x, t.y, t.z, t.w};
+                for (int h = 0; h < 2; ++h) {
+                    float t8[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = jb + 4 * f + e;
-                        t8[4 * f + e] = j <= i ? tv[e] * beta_s[j] : 0.f;
+                    for (int f = 0; f < 2; ++f) {
+                        const float4 t = *reinterpret_cast<const float4 *>(Ts + i * kAS + jb + 8 * h + 4 * f);
+                        const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = jb + 8 * h + 4 * f + e;
+                            t8[4 * f + e] = j <= i ? tv[e] * beta_n[j] : 0.f;
+                        }
                     }
+                    st16(sm + P1::TBs + kmaj(i, jb + 8 * h, 1024, 128), t8);
+                    // and rows 64-127 of the workspace's [H; T B], from which each
+                    // state-pass CTA forms its slab of U = (T B) V
+                    st16(reg + TcRegion::HT + kmaj(64 + i, jb + 8 * h, kA2Lbo, kA2Sbo), t8);
                 }
-                st16(sm + P1::TBs + kmaj(i, jb, 1024, 128), t8);
-                // and rows 64-127 of the workspace's [H; T B], from which each
-                // state-pass CTA forms its slab of U = (T B) V
-                st16(reg + TcRegion::HT + kmaj(64 + i, jb, kA2Lbo, kA2Sbo), t8);
             }
-        }
-        fence_async_smem();
-        fence_before();
-        bar_sync(0, kP1Threads);
-        fence_after();
-
-        // ================= W = (T B) L
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16(128, 64, 0, 0);
+            fence_async_smem();
+            fence_before();
+            bar_sync(kBarSv, kP1S);
+            // ================= W = (T B) L, into the first 64 columns of the item's TMEM half
+            if (st == 0 && !*err) {
+                fence_after();
+                const uint32_t id = idesc_bf16(128, 64, 0, 0);
+                const uint64_t lo = (uint64_t)par * (16384 >> 4);
 #pragma unroll
-            for (int s = 0; s < C / 16; ++s)
-                mma_bf16(tmem + 0, d_lt + s * (2 * kA2Lbo >> 4), d_tb + s * (2 * 1024 >> 4), id, s > 0);
-            commit(bar_mma);
+                for (int s = 0; s < C / 16; ++s)
+                    mma_bf16(tb, d_lt + lo + s * (2 * kA2Lbo >> 4), d_tb + s * (2 * 1024 >> 4), id, s > 0);
+                commit(bar_w);
+                ++w_issued;
+            }
+            if (!wait(bar_w, (uint32_t)n & 1)) break;
+            fence_after();
+            __syncwarp();
+            {
+                // W^T (lane = channel c, column = token) -> rows 64-127 of [s Qbar; W];
+                // warp (quadrant, h) reads tokens 32 h .. 32 h + 31 of its channels.
+                const int c = 32 * quad + lane, t0 = 32 * (sw >> 2);
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    float x[16];
+                    tmem_ld16(tb + lane_base + t0 + 16 * m, x);
+                    tmem_wait_ld();
+                    st16(reg + TcRegion::A1 + mnmaj(64 + t0 + 16 * m, c, kA1Lbo, kA1Sbo), x);
+                    st16(reg + TcRegion::A1 + mnmaj(64 + t0 + 16 * m + 8, c, kA1Lbo, kA1Sbo), x + 8);
+                }
+            }
+            fence_before();
+            bar_sync(kBarSv, kP1S);
+            // Every thread of the side has written its part of the region (and
+            // read its TMEM): the half, L^T and beta slots may take item n + 2,
+            // and a later release by the side's first thread makes the region
+            // visible before the item's flag (the elementwise side's writes
+            // precede bar_e, which that thread waited for).
+            if (st == 0) mbar_arrive(bar_sf + par);
+            flag_prev = (long long)phys(sl) * H + hc;
+            ++n;
+            advance(sl, hc);
         }
-        ok = bar_and(0, kP1Threads, mbar_wait(bar_mma, mma_phase));
-        mma_phase ^= 1;
-        fence_after();
-        if (!ok) break;
-        {
-            // W^T (lane = channel c, column = token) -> rows 64-127 of [s Qbar; W];
-            // thread (c, blk) writes tokens 16 blk .. 16 blk + 15 of its channel.
-            float x[16];
-            tmem_ld16(tmem + lane_base + 16 * blk, x);
-            tmem_wait_ld();
-            st16(reg + TcRegion::A1 + mnmaj(64 + 16 * blk, c, kA1Lbo, kA1Sbo), x);
-            st16(reg + TcRegion::A1 + mnmaj(64 + 16 * blk + 8, c, kA1Lbo, kA1Sbo), x + 8);
+        if (st == 0) {
+            if (w_issued > 0) mbar_wait(bar_w, (uint32_t)(w_issued - 1) & 1);
+            // The last item's flag (after an error the state pass gives up on its own).
+            if (wk.ready && flag_prev >= 0 && !*err) st_release_gpu(wk.ready + flag_prev, 1);
         }
-        // The next item's per-head log-decays (this item read its own before
-        // its exchange barrier; the next item's load barrier orders these).
-        if (pro.decay == KDA_DECAY_SCALAR && tid < C)
-            reinterpret_cast<float *>(sm + P1::gsc)[tid] =
-                sn < used && tid < en.len ? log_decay(gn, pro) : 0.f;
-        fence_before();
-        bar_sync(0, kP1Threads);
-        fence_after();
-        // Every thread's region writes precede this barrier, so a later
-        // release by thread 0 makes them visible before the item's flag.
-        flag_prev = (long long)phys(sl) * H + hc;
-        sl = sn;
-        hc = hn;
-        ce = en;
-        sn = snn;
-        hn = hnn;
-        en = enn;
-        bcur = bn;
     }
-    if (!ok) {
-        if (tid == 0) atomicExch(status, (int)KDA_ERR_TIMEOUT);
-        // Bounded waits for copies and MMAs that may still be in flight.
-        mbar_wait(bar_ld, ld_phase);
-        mbar_wait(bar_mma, mma_phase);
-    }
-    // The last item's flag (after an error the state pass gives up on its own).
-    if (wk.ready && tid == 0 && flag_prev >= 0 && ok) st_release_gpu(wk.ready + flag_prev, 1);
     fence_before();
     bar_sync(0, kP1Threads);
-    if (warp == 0) tmem_dealloc<256>(tmem);
+    if (warp == 0) tmem_dealloc<512>(tmem);
 }
 
 template <int kVar>
