@@ -361,6 +361,14 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
         ChunkEntry ce{};
         float bcur = 0.f;
         int ld_issued = 0, g_issued = 0, ah_issued = 0;  // copies / products issued (thread 0)
+        // Fused prefill (thread 0): the ready flags of the two items in the
+        // solve side's hands, by parity. Item n - 2's flag is released as soon
+        // as the solve side is done with it (bar_sf, which this thread waits
+        // for anyway); the region's writes by both sides precede that barrier
+        // (this side's through its own barriers), so the release makes them
+        // visible before the flag. A release waits for stores in flight to
+        // reach L2, which this side's idle wait absorbs.
+        long long flag0 = -1, flag1 = -1;  // even, odd items
         bool g_next = false;  // thread 0: the next item's g is on its way
         if (sl < used) {
             ce = table[phys(sl)];
@@ -393,8 +401,12 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
             if (tid == 0) {
                 // Item n - 2's TMEM half, L^T and beta slots, and the operands
                 // item n - 1's product read, are free before anything is written.
-                if (n >= 2) wait(bar_sf + par, (uint32_t)((n - 2) >> 1) & 1);
+                if (n >= 2 && wait(bar_sf + par, (uint32_t)((n - 2) >> 1) & 1) && wk.ready)
+                    st_release_gpu(wk.ready + (par ? flag1 : flag0), 1);
                 if (n >= 1) wait(bar_ah + (par ^ 1), (uint32_t)((n - 1) >> 1) & 1);
+                const long long f = (long long)phys(sl) * H + hc;
+                flag0 = par ? flag0 : f;
+                flag1 = par ? f : flag1;
             }
 
             // Cumulative log-decay of channel c over each of the thread's two
@@ -659,6 +671,11 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
             if (ld_issued > 0) mbar_wait(bar_ld, (uint32_t)(ld_issued - 1) & 1);
             if (g_issued > 0) mbar_wait(bar_ldg, (uint32_t)(g_issued - 1) & 1);
             if (ah_issued >= 1) mbar_wait(bar_ah + ((ah_issued - 1) & 1), (uint32_t)((ah_issued - 1) >> 1) & 1);
+            // The flags of the last two items, once the solve side is done with
+            // them (after an error the state pass gives up on its own).
+            for (int k = n - 2; k < n; ++k)
+                if (k >= 0 && wait(bar_sf + (k & 1), (uint32_t)(k >> 1) & 1) && wk.ready && !*err)
+                    st_release_gpu(wk.ready + ((k & 1) ? flag1 : flag0), 1);
         }
     } else {
         // ============================================ solve side
@@ -673,13 +690,6 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
         float *Rs = reinterpret_cast<float *>(sm + P1::Rs);
         int sl = (int)(wk.rank / H), hc = (int)(wk.rank % H);
         int n = 0, w_issued = 0;
-        // Fused prefill: the ready flag of the item before, released by the
-        // side's first thread in the middle of this item's solve. A release
-        // waits for the stores in flight to reach L2; the solve writes only
-        // shared memory, and by then the region writes have drained, so the
-        // wait is short (right after an item's stores it takes an L2 round
-        // trip per item).
-        long long flag_prev = -1;  // its index in wk.ready, or -1
         while (sl < used) {
             const int par = n & 1;
             unsigned char *reg = ws + ((size_t)phys(sl) * H + hc) * TcRegion::bytes;
@@ -765,7 +775,7 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
             fence_before();
             bar_sync(kBarSv, kP1S);
             if (*err) break;
-            if (st == 0) mbar_arrive(bar_rb);
+            if (st == 160) mbar_arrive(bar_rb);  // a warp that sits out the substitution
 
             // ================= T = (I - A)^{-1}, then T Diag(beta) as a bf16 operand.
             {
@@ -835,10 +845,6 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
                 }
             }
             bar_sync(kBarSv, kP1S);
-            if (wk.ready && st == 0 && flag_prev >= 0) {
-                st_release_gpu(wk.ready + flag_prev, 1);
-                flag_prev = -1;
-            }
             {
                 // Off-diagonal blocks: with M_IK = T_II A_IK (K < I), block row I of
                 // (I - A) T = I gives T_IJ = sum_{K = J}^{I - 1} M_IK T_KJ. The
@@ -981,20 +987,13 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
             fence_before();
             bar_sync(kBarSv, kP1S);
             // Every thread of the side has written its part of the region (and
-            // read its TMEM): the half, L^T and beta slots may take item n + 2,
-            // and a later release by the side's first thread makes the region
-            // visible before the item's flag (the elementwise side's writes
-            // precede bar_e, which that thread waited for).
+            // read its TMEM): the half, L^T and beta slots may take item n + 2.
             if (st == 0) mbar_arrive(bar_sf + par);
-            flag_prev = (long long)phys(sl) * H + hc;
             ++n;
             advance(sl, hc);
         }
-        if (st == 0) {
-            if (w_issued > 0) mbar_wait(bar_w, (uint32_t)(w_issued - 1) & 1);
-            // The last item's flag (after an error the state pass gives up on its own).
-            if (wk.ready && flag_prev >= 0 && !*err) st_release_gpu(wk.ready + flag_prev, 1);
-        }
+        if (st == 0 && w_issued > 0) mbar_wait(bar_w, (uint32_t)(w_issued - 1) & 1);
+
     }
     fence_before();
     bar_sync(0, kP1Threads);
@@ -1037,10 +1036,11 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // holds the whole warp.)
 // 64-column slabs (the fused prefill): 12 compute warps (three column groups
 // of 24, 24 and 16 columns), warp 12 the chain and warp 13 the copies; the
-// chain warp issues U and H Z as well (the Z and state-update windows, longer
-// with up to 24 columns a thread, cover their issue). The fused kernel then
-// fits in 16 warps: with more, one SM sub-partition holds five warps and the
-// register file caps every thread at 96 registers, which slows phase 1.
+// chain warp issues U and H Z as well (a warp of their own measured the same
+// chunk period: the Z and state-update windows cover their issue). The fused
+// kernel then fits in 16 warps: with more, one SM sub-partition holds five
+// warps and the register file caps every thread at 96 registers, which slows
+// phase 1.
 constexpr int kP2Threads = 16 * 32 + 96;   // the 32-column state pass
 constexpr int kFusedThreads = kP1Threads;  // the fused kernel (16 warps)
 constexpr int kBarZ = 1, kBarS = 2;       // named barriers: Z written, state written
