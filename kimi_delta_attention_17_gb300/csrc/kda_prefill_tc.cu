@@ -1162,13 +1162,18 @@ __device__ __forceinline__ void state_pass_body(
     const CUtensorMap *tm_v, int vblock, const int *ready) {
     using L = P2L<TN>;
     // Compute warps: the four lane quadrants times CG column groups; a group
-    // takes NP 8-column pieces of the slab (the last one may take fewer).
+    // takes NP 8-column pieces of the slab (the last one may take fewer). With
+    // 64-column slabs the Z rows (lanes 64-127, quadrants 2 and 3) take two more
+    // warps (CW + 2, CW + 3) and four groups of 16 columns, which shortens the
+    // Z step on the chain; rows 0-63 keep three groups (24, 24, 16).
     constexpr int CW = TN == kTN ? 16 : 12;
     constexpr int CG = CW / 4;
     constexpr int NP = (TN / 8 + CG - 1) / CG;
     constexpr int NJ = 8 * NP;                        // slab columns a compute thread holds, at most
     constexpr int kMma = CW, kCopy = CW + 1, kSideW = CW + 2;  // warp roles
-    constexpr int kSync = CW * 32 + 32;               // compute warps + MMA warp
+    constexpr int kNComp = TN == kTN ? CW : CW + 2;   // compute warps
+    constexpr int ZP = TN == kTN ? 1 : 2;             // pieces of a Z-row thread (lanes 64-127)
+    constexpr int kSync = kNComp * 32 + 32;           // compute warps + MMA warp
     constexpr bool kSide = TN == kTN;     // U and H Z from their own warp
     extern __shared__ __align__(1024) unsigned char sm[];
     const OutGate og = TN == kTN ? og_in : OutGate{nullptr, nullptr, 0.f};
@@ -1274,8 +1279,11 @@ __device__ __forceinline__ void state_pass_body(
     };
 
     // Compute-thread coordinates: TMEM lane / state row r, slab columns js .. js + NJ - 1.
-    const int r = 32 * (warp & 3) + lane, cgi = warp >> 2, js = 8 * NP * cgi;
-    const int np = warp < CW ? min(NP, TN / 8 - NP * cgi) : 0;  // this thread's pieces
+    const bool compute = warp < CW || (TN != kTN && warp >= CW + 2);
+    const bool zq = TN != kTN && (warp & 2) != 0;  // a Z-row warp of the 64-column pass
+    const int r = 32 * (warp & 3) + lane, cgi = warp >> 2;
+    const int js = TN == kTN ? 8 * NP * cgi : zq ? 16 * cgi : 24 * cgi;
+    const int np = !compute ? 0 : TN == kTN ? min(NP, TN / 8 - NP * cgi) : zq ? 2 : (cgi < 2 ? 3 : 2);
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     float S[NJ];
 #pragma unroll
@@ -1289,7 +1297,7 @@ __device__ __forceinline__ void state_pass_body(
             *reinterpret_cast<uint4 *>(B1 + mnmaj(TN + js + 8 * q, r, kB1Lbo, kB1Sbo)) = lo;
         }
     };
-    if (warp < CW) {
+    if (compute) {
         if (st_src) {
             const float *src = st_src + (size_t)r * D + j0 + js;
 #pragma unroll
@@ -1525,7 +1533,7 @@ __device__ __forceinline__ void state_pass_body(
             fence_after();
         }
         __syncwarp();
-    } else if (warp < CW) {
+    } else if (compute) {
         uint32_t p1 = 0, p2 = 0, p3 = 0;  // phases of the three product barriers
         uint32_t rph = 0;                 // phases of the two row-partial barriers (bit per parity)
         const bool zrow = r >= 64;
@@ -1674,14 +1682,16 @@ __device__ __forceinline__ void state_pass_body(
                 spin(bar_u + (ch & 1), (uint32_t)(ch >> 1) & 1);
                 fence_after();
                 __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane wait
+                // Z-row threads hold exactly ZP pieces; their loads are issued
+                // before one wait, so that the latencies overlap.
+                float u8[ZP][8];
 #pragma unroll
-                for (int q = 0; q < NP; ++q) if (q < np) {
-                    float u8[8];
-                    tmem_ld8(tmem + lane_base + L::kUCol + TN * (ch & 1) + js + 8 * q, u8);
-                    tmem_wait_ld();
+                for (int q = 0; q < ZP; ++q) tmem_ld8(tmem + lane_base + L::kUCol + TN * (ch & 1) + js + 8 * q, u8[q]);
+                tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) uv[8 * q + j] = u8[j];
-                }
+                for (int q = 0; q < ZP; ++q)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) uv[8 * q + j] = u8[q][j];
             }
             if (!zrow && outputs && ch > 0) {
                 // The previous chunk's outputs, complete once its H Z product is:
@@ -1699,14 +1709,18 @@ __device__ __forceinline__ void state_pass_body(
             if (zrow) {
                 // Z = U - W S for token row i, slab columns js .. js + NJ - 1.
                 const int i = r - 64;
+                float hi[ZP][8], lo[ZP][8];
 #pragma unroll
-                for (int q = 0; q < NP; ++q) if (q < np) {
-                    float hi[8], lo[8], z[8];
-                    tmem_ld8(d1 + lane_base + js + 8 * q, hi);
-                    tmem_ld8(d1 + lane_base + TN + js + 8 * q, lo);
-                    tmem_wait_ld();
+                for (int q = 0; q < ZP; ++q) {
+                    tmem_ld8(d1 + lane_base + js + 8 * q, hi[q]);
+                    tmem_ld8(d1 + lane_base + TN + js + 8 * q, lo[q]);
+                }
+                tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) z[j] = uv[8 * q + j] - (hi[j] + lo[j]);
+                for (int q = 0; q < ZP; ++q) {
+                    float z[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) z[j] = uv[8 * q + j] - (hi[q][j] + lo[q][j]);
                     uint4 zh, zl;
                     split8(z, zh, zl);
                     *reinterpret_cast<uint4 *>(B2 + mnmaj(js + 8 * q, i, kB2Lbo, kB2Sbo)) = zh;
@@ -1721,14 +1735,22 @@ __device__ __forceinline__ void state_pass_body(
             p2 ^= 1;
             fence_after();
             __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the per-lane wait
+            // Pieces in pairs: both loads of a pair before one wait.
 #pragma unroll
-            for (int q = 0; q < NP; ++q) if (q < np) {
-                float hi[8], lo[8];
-                tmem_ld8(tmem + lane_base + L::kD2Col + js + 8 * q, hi);
-                tmem_ld8(tmem + lane_base + L::kD2Col + TN + js + 8 * q, lo);
+            for (int q0 = 0; q0 < NP; q0 += 2) {
+                float hi[2][8], lo[2][8];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) if (q0 + u < NP && q0 + u < np) {
+                    tmem_ld8(tmem + lane_base + L::kD2Col + js + 8 * (q0 + u), hi[u]);
+                    tmem_ld8(tmem + lane_base + L::kD2Col + TN + js + 8 * (q0 + u), lo[u]);
+                }
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) S[8 * q + j] = gam * S[8 * q + j] + (hi[j] + lo[j]);
+                for (int u = 0; u < 2; ++u) if (q0 + u < NP && q0 + u < np) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        S[8 * (q0 + u) + j] = gam * S[8 * (q0 + u) + j] + (hi[u][j] + lo[u][j]);
+                }
             }
             put_state();
             fence_async_smem();
