@@ -101,23 +101,42 @@ chunk_table_kernel(const int32_t *__restrict__ cu_seqlens, int num_seqs, int T_f
         int bos, len;
         seq_bounds(n, bos, len);
         seq_first_slot[n] = slot;
-        for (int c = 0; c * kChunk < len; ++c, ++slot) {
-            ChunkEntry e;
-            e.seq = n;
-            e.bos = bos + c * kChunk;
-            e.len = min(kChunk, len - c * kChunk);
-            e.idx = c;
-            if (slot < slots) table[slot] = e;  // cu_seqlens is trusted; never write past the table
-        }
+        slot += (len + kChunk - 1) / kChunk;
     }
     const int used = part[kTableThreads - 1];
     if (tid == 0) seq_first_slot[num_seqs] = used;
-    for (long long s = used + tid; s < slots; s += kTableThreads) {
+    __syncthreads();  // every sequence's first slot is in place
+    // The entries, spread over all threads (one sequence of many chunks would
+    // otherwise be one thread's serial loop). Slot s belongs to the last
+    // sequence whose first slot is <= s (an empty sequence shares its first
+    // slot with the next one, which is later).
+    const int nch_fixed = (T_fixed + kChunk - 1) / kChunk;
+    for (long long s = tid; s < slots; s += kTableThreads) {
         ChunkEntry e;
         e.seq = -1;
         e.bos = 0;
         e.len = 0;
         e.idx = 0;
+        if (s < used) {
+            int n;
+            if (!cu_seqlens) {
+                n = (int)(s / nch_fixed);
+            } else {
+                int a = 0, b = num_seqs - 1;  // seq_first_slot[a] <= s holds throughout
+                while (a < b) {
+                    const int m = (a + b + 1) >> 1;
+                    if (seq_first_slot[m] <= s) a = m; else b = m - 1;
+                }
+                n = a;
+            }
+            int bos, len;
+            seq_bounds(n, bos, len);
+            const int c = (int)(s - seq_first_slot[n]);
+            e.seq = n;
+            e.bos = bos + c * kChunk;
+            e.len = min(kChunk, len - c * kChunk);
+            e.idx = c;
+        }
         table[s] = e;
     }
 }
