@@ -312,11 +312,16 @@ def prefill_workload_variant(spec, dev, K, world, peaks):
     v1 = torch.cuda.Event(enable_timing=True)
     v0.record(stream)
     for s in range(K):
-        run(phase[s])
+        run()
     v1.record(stream)
     torch.cuda.synchronize()
     barrier()
     vms = max_over_ranks(v0.elapsed_time(v1), dev) / K
+    # The phase marks (four event records per call, about 4 us each on a
+    # 0.16 ms call) are taken in a second, untimed loop.
+    for s in range(K):
+        run(phase[s])
+    torch.cuda.synchronize()
     tokens = B * T
     vbytes = prefill_bytes(spec, tokens, N, inp["init_state"] is not None)
     names = ["chunk_table", "intra_chunk", "state_pass"]
@@ -560,10 +565,14 @@ def bench_ours(args):
     v1 = torch.cuda.Event(enable_timing=True)
     v0.record(stream)
     for s in range(K):
-        two_launches(tl_phase[s])
+        two_launches()
     v1.record(stream)
     torch.cuda.synchronize()
     tl_ms = max_over_ranks(v0.elapsed_time(v1), dev) / K
+    # The phase marks (four event records per call) outside the timed loop.
+    for s in range(K):
+        two_launches(tl_phase[s])
+    torch.cuda.synchronize()
     tl_bytes = prefill_bytes(spec, tokens, N, inp["init_state"] is not None)
     variants["prefill_two_launches"] = {
         "metric": "KDA prefill tokens/s (%s, fused=False)" % spec.name,
