@@ -1796,6 +1796,22 @@ tc_state_pass(const unsigned char *__restrict__ ws, const int *__restrict__ seq_
                          final_state, H, status, sp, og, &tm_z, &tm_v, (int)blockIdx.x, nullptr);
 }
 
+// The serial state pass with 64-column slabs as a launch of its own (two CTAs
+// per sequence and head; the fused kernel's state-pass role without the ready
+// flags). Per column it costs less than the 32-column pass (about 3.7k cycles
+// per chunk for 64 columns against 2 x 2.9k), the 32-column pass has the shorter
+// chain: this one serves many chains, where the CTAs run in several waves.
+__global__ void __launch_bounds__(kFusedThreads, 1)
+tc_state_pass64(const unsigned char *__restrict__ ws, const int *__restrict__ seq_first_slot,
+                const int *__restrict__ seq_order, const int32_t *__restrict__ cu_seqlens, int T_fixed,
+                const float *init_state, __nv_bfloat16 *__restrict__ out, float *final_state, int H,
+                int *__restrict__ status, const __grid_constant__ CUtensorMap tm_v) {
+    const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
+    state_pass_body<64>(ws, seq_first_slot, seq_order, cu_seqlens, T_fixed, init_state, out, final_state,
+                        H, status, sp, OutGate{nullptr, nullptr, 0.f}, &tm_v, &tm_v, (int)blockIdx.x,
+                        nullptr);
+}
+
 // The fused prefill: one cooperative launch whose first n_state CTAs run the
 // state pass with 64-column slabs while the rest run phase 1, chunk-major,
 // handing each (slot, head) region over through its ready flag. Phase 1
@@ -2033,6 +2049,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         KDA_SMEM(tc_prefill_fused<kVarNone>, kFusedSmem)
         KDA_SMEM(tc_prefill_fused<kVarGated>, kFusedSmem)
         KDA_SMEM(tc_state_pass, P2L<kTN>::kSmem)
+        KDA_SMEM(tc_state_pass64, P2L<64>::kSmem)
         KDA_SMEM(seg_combine, kCombSmem)
 #undef KDA_SMEM
         coop_ok[dev] = coop != 0;
@@ -2169,6 +2186,16 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                                           static_cast<__nv_bfloat16 *>(out), final_state, H, status,
                                           sp, og, tz, tv)) != cudaSuccess)
                 return err;
+        } else if (P <= 1 && (long long)num_seqs * H * kTiles > 2LL * sm_count) {
+            // Many chains: the 32-column pass would run in more than two waves,
+            // so the 64-column pass, cheaper per column, finishes first.
+            CUtensorMap tv64;
+            memset(&tv64, 0, sizeof(tv64));
+            if (tokens > 0 && (err = value_rows_map(&tv64, v, H, tokens, 64)) != cudaSuccess) return err;
+            tc_state_pass64<<<(unsigned)num_seqs * H * (D / 64), kFusedThreads, P2L<64>::kSmem, stream>>>(
+                region, seq_first_slot, order, cu_seqlens, T_fixed, init_state,
+                static_cast<__nv_bfloat16 *>(out), final_state, H, status, tv64);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
         } else if (P <= 1) {
             const SegPass sp{1 << 30, 1, 0, 1, 0, nullptr, nullptr};
             tc_state_pass<<<(unsigned)num_seqs * H * kTiles, kP2Threads, kSmem, stream>>>(
