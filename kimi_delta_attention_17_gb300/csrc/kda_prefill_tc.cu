@@ -4,14 +4,16 @@
 // The algebra is the chunkwise form of "Understanding Kimi Delta Attention"
 // (sections "The triangular system" and "Putting the chunks together"):
 //
-//   phase 1 (every chunk and head in parallel; persistent, one CTA per SM):
+//   phase 1 (every chunk and head in parallel; persistent, one CTA per SM,
+//   whose two halves work on consecutive items: the elementwise steps of
+//   item n + 1 beside the solve and W of item n):
 //     G      in-chunk cumulative log-decay (registers, one thread per channel)
 //     A, H   decay-gated K K^T and Q K^T, from ONE tcgen05.mma (below)
 //     T      (I - A)^{-1}: blocked forward substitution in fp32 shared memory
 //     W = (T B) L                               one MMA, B = Diag(beta)
 //     s Qbar, Kbar^T, exp(G_n)                  elementwise
-//   phase 2 (one CTA per sequence, head and 32-column slab of the state,
-//   chunks in order, state in registers, warp-specialised):
+//   phase 2 (one CTA per sequence, head and 32- or 64-column slab of the
+//   state, chunks in order, state in registers, warp-specialised):
 //     U = (T B) V                               one MMA, a chunk ahead
 //     [s Qbar S; W S] = [s Qbar; W] S           one MMA, M = 128
 //     Z = U - W S                               elementwise
@@ -84,8 +86,9 @@ constexpr uint32_t kA2Lbo = 2048, kA2Sbo = 128;  // K-major: channel groups adja
 // bound by instruction issue and the solve by its dependent stages (MMA round
 // trips, barriers, a shuffle chain), so each fills the other's idle issue
 // slots. Elementwise thread (c, hb) owns key/value channel c and the 16-token
-// blocks 2 hb, 2 hb + 1; solve-side warp w reads TMEM lanes 32 (w mod 4) ...
-// What the two sides hand over is double-buffered by item parity: the TMEM
+// blocks hb and 3 - hb; solve-side warp w reads TMEM lanes 32 (w mod 4) to
+// 32 (w mod 4) + 31. What the two sides hand over is double-buffered by item
+// parity: the TMEM
 // accumulators (two 256-column halves), L^T, beta and the steep flag.
 constexpr int kP1Threads = 512;
 constexpr int kP1E = 256, kP1S = 256;   // elementwise side: threads 0-255; solve side: 256-511
@@ -100,7 +103,7 @@ struct P1 {  // shared-memory offsets, bytes
     static constexpr int Ms = 197632;   // fp32 [6][16][kMS]: M_IK = T_II A_IK
     static constexpr int Rs = 205312;   // fp32 [3][16][kMS]: partial sums of T_IJ
     static constexpr int beta = 209152; // fp32 [2][64] by item parity
-    static constexpr int bar = 209664;  // 9 mbarriers (see intra_chunk_body)
+    static constexpr int bar = 209664;  // 10 mbarriers (see intra_chunk_body)
     static constexpr int tmem = 209744;
     static constexpr int flags = 209760;  // int [2] steep, by item parity; int error flag
     static constexpr int exch = 209776; // fp32 [2][4][128]: block totals and local references of G
