@@ -400,7 +400,6 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
             float bn, gn;
             unsigned char *reg = ws + ((size_t)phys(sl) * H + hc) * TcRegion::bytes;
             if (g_tile) wait(bar_ldg, (uint32_t)par);  // a failure shows in the error flag after the barrier
-            if (pro.l2norm) wait(bar_ld, (uint32_t)par);
             if (tid == 0) {
                 // Item n - 2's TMEM half, L^T and beta slots, and the operands
                 // item n - 1's product read, are free before anything is written.
@@ -467,29 +466,6 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
                 ref_s[b * D + c] = G[7];
                 accb[bb] = acc;
             }
-            if (pro.l2norm) {
-                // Reciprocal norms of k and q per token (the query scale folded
-                // in): two threads per (tensor, token) each sum 64 channels of
-                // the staged row, in 16-byte pieces rotated by the token so that
-                // a warp's reads spread over the banks; one shuffle combines them.
-                const int pair = tid >> 1, part = tid & 1;
-                const int tsr = pair >> 6, tok = pair & 63;  // tensor 0: k, 1: q
-                const __nv_bfloat16 *row = (tsr ? qs : ks) + tok * D;
-                float ss = 0.f;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int piece = 8 * part + ((j + tok) & 7);  // 8 channels
-                    const uint4 w = *reinterpret_cast<const uint4 *>(row + 8 * piece);
-                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float lo = __uint_as_float(u[e] << 16), hi = __uint_as_float(u[e] & 0xFFFF0000u);
-                        ss += lo * lo + hi * hi;
-                    }
-                }
-                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-                if (part == 0) fac_s[pair] = rsqrtf(ss + kL2Eps) * (tsr ? scale : 1.f);
-            }
             // A block's total decay bounds every factor of its references (the
             // log-decay is non-increasing within the block); over kSteepNats
             // anywhere, the whole item takes the steep-decay form (the decision
@@ -532,7 +508,33 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
             }
             const float Gend = off;
             unsigned char *ltp = sm + P1::lt + par * 16384;
-            if (!pro.l2norm) wait(bar_ld, (uint32_t)par);  // q, k (a failure skips the rest below)
+            wait(bar_ld, (uint32_t)par);  // q, k (a failure skips the rest below)
+            if (pro.l2norm) {
+                // Reciprocal norms of k and q per token (the query scale folded
+                // in): two threads per (tensor, token) each sum 64 channels of
+                // the staged row, in 16-byte pieces rotated by the token so that
+                // a warp's reads spread over the banks; one shuffle combines them.
+                const int pair = tid >> 1, part = tid & 1;
+                const int tsr = pair >> 6, tok = pair & 63;  // tensor 0: k, 1: q
+                const __nv_bfloat16 *row = (tsr ? qs : ks) + tok * D;
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int piece = 8 * part + ((j + tok) & 7);  // 8 channels
+                    const uint4 w = *reinterpret_cast<const uint4 *>(row + 8 * piece);
+                    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(u[e] << 16), hi = __uint_as_float(u[e] & 0xFFFF0000u);
+                        ss += lo * lo + hi * hi;
+                    }
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (part == 0) fac_s[pair] = rsqrtf(ss + kL2Eps) * (tsr ? scale : 1.f);
+                // Every thread reads the norms below; the rows are cleared past
+                // a ragged chunk's length only after every norm has been summed.
+                bar_sync(kBarE, kP1E);
+            }
             if (len < C) {
                 // A ragged chunk: the staged q, k rows past len (the next
                 // sequence's, or zeros past the tensor) are cleared, each thread
