@@ -141,6 +141,11 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Steep item (kSteepNats): the diagonal 16 x 16 blocks of A and H in fp32,
 // sum_c x_ic k_jc 2^(G_ic - G_jc) (G in base-2 units) with the pair decay formed directly (its
@@ -439,17 +444,24 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
 #pragma unroll
                     for (int t = 0; t < 16; ++t) gv[t] = gs[(16 * b + t) * D + c];
                     if (pro.gate == KDA_GATE_LOGSIGMOID) {
+                        // log2 sigmoid(x) = min(x, 0) log2 e - log2(1 + 2^(-|x| log2 e)),
+                        // already in the base-2 units of G.
 #pragma unroll
                         for (int t = 0; t < 16; ++t)
-                            gv[t] = fminf(gv[t], 0.f) - __logf(1.f + __expf(-fabsf(gv[t])));
+                            gv[t] = fmaf(fminf(gv[t], 0.f), kLog2e, -lg2(1.f + ex2(-fabsf(gv[t]) * kLog2e)));
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            acc += 16 * b + t < len ? gv[t] : 0.f;
+                            G[t] = acc;
+                        }
                     } else {
 #pragma unroll
                         for (int t = 0; t < 16; ++t) gv[t] = pro.lower * __fdividef(1.f, 1.f + __expf(-gv[t]));
-                    }
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        acc = fmaf(16 * b + t < len ? gv[t] : 0.f, kLog2e, acc);
-                        G[t] = acc;
+                        for (int t = 0; t < 16; ++t) {
+                            acc = fmaf(16 * b + t < len ? gv[t] : 0.f, kLog2e, acc);
+                            G[t] = acc;
+                        }
                     }
                 } else if (pro.decay == KDA_DECAY_SCALAR) {
                     // One decay per head: every channel's prefix is the same.
@@ -586,14 +598,24 @@ __device__ __forceinline__ void intra_chunk_body(const CUtensorMap *tm_q, const 
                         for (int r = 0; r < 8; ++r) gs[(i0 + r) * D + c] = Gi[r];
                     }
                     // Staged rows past len are zero (see above), so no masks here.
+                    float fk8[8], fq8[8];  // the group's norm factors, four 16-byte loads
+                    if (pro.l2norm) {
+#pragma unroll
+                        for (int h4 = 0; h4 < 2; ++h4) {
+                            const float4 a4 = *reinterpret_cast<const float4 *>(fac_s + i0 + 4 * h4);
+                            const float4 b4 = *reinterpret_cast<const float4 *>(fac_s + C + i0 + 4 * h4);
+                            fk8[4 * h4] = a4.x; fk8[4 * h4 + 1] = a4.y; fk8[4 * h4 + 2] = a4.z; fk8[4 * h4 + 3] = a4.w;
+                            fq8[4 * h4] = b4.x; fq8[4 * h4 + 1] = b4.y; fq8[4 * h4 + 2] = b4.z; fq8[4 * h4 + 3] = b4.w;
+                        }
+                    }
 #pragma unroll
                     for (int r = 0; r < 8; ++r) {
                         const int i = i0 + r;
                         kv[r] = __bfloat162float(ks[i * D + c]);
                         qv[r] = __bfloat162float(qs[i * D + c]);
                         if (pro.l2norm) {
-                            kv[r] *= fac_s[i];
-                            qv[r] *= fac_s[C + i];
+                            kv[r] *= fk8[r];
+                            qv[r] *= fq8[r];
                         }
                         E[r] = ex2(Gi[r] - Rlr);
                         kF[r] = kv[r] * ex2(Rlc - Gi[r]);
