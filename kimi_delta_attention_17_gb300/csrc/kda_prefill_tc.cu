@@ -2004,17 +2004,17 @@ cudaError_t value_rows_map(CUtensorMap *m, const void *base, int H, long long to
 }
 
 // Whether the fused single launch is expected to beat the two launches, from
-// a cost model of the measured rates on this part: phase 1 about 12.2k
-// cycles per (chunk, head) item and SM; the state pass about 3.1k cycles per
-// chunk with 32-column slabs and 3.7k with 64-column ones. Two launches take
+// a cost model of the measured rates on this part: phase 1 about 9.4k
+// cycles per (chunk, head) item and SM; the state pass about 2.9k cycles per
+// chunk with 32-column slabs and 3.76k with 64-column ones. Two launches take
 // phase 1 on every SM, then the chain; the fused one runs phase 1 on the SMs
 // the 64-column state pass leaves and the chain beside it.
 bool fuse_pays(long long items, int chain_chunks, long long n_state, int sm_count) {
     if (n_state < 1 || n_state > sm_count - 8) return false;
-    const double p1_all = 12.2 * (double)items / (double)(items < sm_count ? items : sm_count);
-    const double p1_rest = 12.2 * (double)items / (double)(sm_count - n_state);
-    const double two = p1_all + 3.1 * chain_chunks;
-    const double fused = (p1_rest > 3.7 * chain_chunks ? p1_rest : 3.7 * chain_chunks) + 12.2;
+    const double p1_all = 9.4 * (double)items / (double)(items < sm_count ? items : sm_count);
+    const double p1_rest = 9.4 * (double)items / (double)(sm_count - n_state);
+    const double two = p1_all + 2.9 * chain_chunks;
+    const double fused = (p1_rest > 3.76 * chain_chunks ? p1_rest : 3.76 * chain_chunks) + 9.4;
     return fused < 0.95 * two;
 }
 
