@@ -29,10 +29,15 @@
 // which turns the gated products into plain matmuls of rescaled rows. Each
 // 16-token block I of the chunk has its reference at its 8th token, r(I); a
 // row i in block I is scaled by E_i = exp(G_i - G_r(I)) and a column j in
-// block J <= I by exp(G_r(I) - G_j) = exp(G_r(I) - G_r(J)) / E_j. Every factor
-// spans at most 8 tokens of decay where it can exceed 1, so nothing overflows
-// fp32 for per-token log-decays down to about -10 (the factors that shrink
-// may underflow to zero, exactly where the true product is negligible). The
+// block J <= I by exp(G_r(I) - G_r(J)) / E_j. Every factor that can exceed 1
+// spans at most 8 tokens of one block's decay, so while no channel decays by
+// more than kSteepNats within a 16-token block every factor stays far inside
+// fp32 and bf16 range (the factors that shrink may underflow to zero, exactly
+// where the true product is negligible). An item with a steeper block takes
+// the steep-decay form: rows referenced to the point before their block,
+// columns to their block's last token (every factor then <= 1), and the
+// diagonal blocks, which no single reference splits safely, formed directly
+// in fp32 with the pair decay exp(G_i - G_j). The
 // ten (I, J) column versions stack into one B operand of 160 rows, and the
 // K-tilde / Q-tilde rows into one A operand of 128 rows, so a single
 // M=128, N=160, K=128 MMA yields every block of A (rows 0-63) and H (rows
@@ -1039,11 +1044,12 @@ tc_intra_chunk(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 }
 
 // ---------------------------------------------------------------- phase 2
-// One CTA of 576 threads per (sequence, head, TN-column slab of the state)
-// and, with the segmented pass, per segment: TN = 32 (four CTAs per head) in
-// the two-launch prefill, TN = 64 (two) in the fused one. Compute thread t
-// owns TMEM lane / state row 32 (w % 4) + (t % 32) of warp w = t / 32 and the
-// TN / 4 slab columns from (TN / 4) (w / 4).
+// One CTA per (sequence, head, TN-column slab of the state) and, with the
+// segmented pass, per segment: TN = 32 (four CTAs of 608 threads per head) in
+// the two-launch prefill, TN = 64 (two CTAs of 512 threads) in the fused one
+// and in tc_state_pass64. Compute thread t of warp w = t / 32 owns TMEM lane /
+// state row 32 (w % 4) + (t % 32) and a group of the slab's columns (the warp
+// roles below).
 // Per chunk, with S the state entering it:
 //                  U  = (T B) V                 (formed a chunk ahead)
 //   round trip 1:  D1 = [s Qbar; W] S          (rows 0-63: Qbar S, 64-127: W S)
