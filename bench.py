@@ -219,11 +219,20 @@ def kernel_sources_sha256():
     return h.hexdigest()
 
 
+def traffic_key(spec):
+    """The entry of profiles/ncu_traffic.json captured on this workload, or None."""
+    if spec == kin.LONG_128K:
+        return "prefill_long_t131072"
+    if spec == kin.VARLEN_8:
+        return "prefill_varlen_8seq_h32"
+    return None
+
+
 def measured_traffic(key):
     """DRAM bytes per launch from the committed ncu capture (profiles/ncu_traffic.json),
-    or None when the kernel sources have changed since it was taken."""
+    or None when the kernel sources have changed since it was taken (or key is None)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    if not os.path.exists(path):
+    if key is None or not os.path.exists(path):
         return None
     t = json.load(open(path))
     if t.get("kernel_sources_sha256") != kernel_sources_sha256() or key not in t:
@@ -367,7 +376,8 @@ def prefill_workload_variant(spec, dev, K, world, peaks):
         "roofline": {"bound": "hbm", "kernel": "kda_chunk_fwd (all phases)",
                      "achieved": vbytes / (vms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": vbytes / (vms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                     "traffic": None, "algorithmic_bytes_per_launch": vbytes,
+                     "traffic": measured_traffic(traffic_key(spec)),
+                     "algorithmic_bytes_per_launch": vbytes,
                      "phases_ms": phases,
                      "tensor_tflops": flops / (vms / 1e3) / 1e12,
                      "tensor_frac": flops / (vms / 1e3) / 1e12 / peaks["bf16_tflops"]},
@@ -807,8 +817,7 @@ def bench_ours(args):
                              ": tc_prefill_fused, one cooperative launch" if fused_ran else ""),
                          "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"],
-                         "traffic": (measured_traffic("prefill_long_t131072")
-                                     if spec == kin.LONG_128K else None),
+                         "traffic": measured_traffic(traffic_key(spec)),
                          "algorithmic_bytes_per_launch": pbytes,
                          "peak_source": peaks["source"],
                          "phases_ms": phase_ms, "dominant_phase": dominant,
