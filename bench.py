@@ -810,7 +810,7 @@ def bench_ours(args):
             "data": "synthetic",
             "config": {"workload": spec.name, "B": B, "T": T, "H": H, "d_k": d, "d_v": d,
                        "chunk": 64, "storage": spec.dtype, "num_seqs": N,
-                       "l2": "inputs (%.2f GB) larger than L2, no flush" % (pbytes / 1e9),
+                       "l2": "inputs and outputs (%.2f GB) larger than L2, no flush" % (pbytes / 1e9),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm",
                          "kernel": "kda_chunk_fwd (all phases%s)" % (
