@@ -88,8 +88,9 @@ def test_decay_range_order_of_magnitude():
         S0 = np.ones((1, 1, dk, dv))
         _, fin = oracle.scan(np.zeros((1, T, 1, dk)), np.zeros((1, T, 1, dk)),
                              np.zeros((1, T, 1, dv)), g, np.zeros((1, T, 1)), 1.0, S0)
-        inv_gamma = 1.0 / fin[0, 0, 0, 0]
-        assert round(np.log10(inv_gamma)) == case["log10"]
+        ratio = fin[0, 0, 0, 0]  # gamma: the part of the initial state kept after T tokens
+        assert 0.0 < ratio < 1.0
+        assert round(-np.log10(ratio)) == case["log10"]  # log10(1 / gamma)
 
 
 def test_half_lives():
