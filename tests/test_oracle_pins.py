@@ -107,6 +107,7 @@ def test_half_lives():
                                np.ones((1, 1, 1, 1)))
         r = fin[0, 0, 0, 0]
         assert out[0, -1, 0, 0] == pytest.approx(r, rel=1e-15)
+        assert 0.0 < r < 1.0  # a strict decay keeps part of the state
         return T * np.log(2.0) / -np.log(r)
 
     hl = half_life(slow["a"], 1000)
